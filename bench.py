@@ -1,0 +1,438 @@
+"""Benchmark of the Gated DeltaNet hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
+                    [--no-extra] [--no-cpu-baseline]
+
+Headline workload: packed recurrent decode of a Qwen3.5-0.8B-like GDN layer
+(256 cached rows, 16 heads, d = 128, fp32 states in a slot cache of 512
+slots, updated in place).  A step is one decode call over the 256 rows; the
+metric is decode rows per second.  The JSON line also carries the prefill
+workloads (varlen GVA prefill, 4 x 32768 prefix-cache prefill with state
+emission, one mixed continuous-batching step) in prefill tokens/s.
+
+Under torchrun each rank runs its own replica of the workload on its own GPU
+(weak scaling, no collective on the data path); the timed region is bracketed
+by barriers and the slowest rank's time is used.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (the only other implementation of this path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gdn_inputs as gi  # noqa: E402
+
+DECODE_ROWS, H, D = 256, 16, 128
+# Algorithmic bytes per decode row: state read + write, q, k, v, o, g, beta, slot index.
+DECODE_BYTES_PER_ROW = 2 * H * D * D * 4 + 2 * H * D * 2 + 2 * H * D * 2 + 2 * H * 4 + 4
+# Algorithmic flops per prefill token (GVA H_k=16, H_v=32, d=128, C=64):
+# shared K K^T and Q K^T per key head, then per value head the WY products,
+# W S0, Q S0, (M o QK^T) U and K~^T U.
+C = 64
+
+
+def prefill_flops_per_token(h_k, h_v, d):
+    return h_k * 4 * C * d + h_v * (2 * C * d + 4 * C * d + 6 * d * d)
+
+
+def prefill_bytes_per_token(h_k, h_v, d):
+    return 2 * h_k * d * 2 + 2 * h_v * d * 2 + 2 * h_v * 4
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained", j["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks sampler
+# ---------------------------------------------------------------------------
+
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(rows), "reasons": reasons}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (timing only; no data-path collective)
+# ---------------------------------------------------------------------------
+
+def dist_setup(torch):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(torch, world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(torch, world, x: float) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def bf16(torch, bits, dev):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def decode_setup(torch, seed, dev):
+    wl = gi.decode_qwen35_08b(seed)
+    b = wl["decode"]
+    cache = torch.zeros((wl["n_slots"], H, D, D), dtype=torch.float32, device=dev)
+    idx = torch.from_numpy(wl["src_slot"].astype(np.int64)).to(dev)
+    cache[idx] = torch.from_numpy(np.swapaxes(b.init_state, -1, -2).copy()).to(dev)
+    t = {"q": bf16(torch, b.q, dev), "k": bf16(torch, b.k, dev), "v": bf16(torch, b.v, dev),
+         "g": torch.from_numpy(b.g).to(dev), "beta": torch.from_numpy(b.beta).to(dev),
+         "src": torch.from_numpy(wl["src_slot"]).to(dev), "cache": cache,
+         "o": torch.empty((DECODE_ROWS, H, D), dtype=torch.bfloat16, device=dev)}
+    return wl, t
+
+
+def run_decode(gdn, t):
+    gdn.gdn_decode_packed(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cache"], t["src"], t["o"])
+
+
+def time_decode(torch, gdn, t, steps, warmup, world):
+    for _ in range(warmup):
+        run_decode(gdn, t)
+    torch.cuda.synchronize()
+    barrier(torch, world)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for i in range(steps):
+        ev[i][0].record()
+        run_decode(gdn, t)
+        ev[i][1].record()
+    end.record()
+    torch.cuda.synchronize()
+    barrier(torch, world)
+    total_ms = start.elapsed_time(end)
+    per_launch = [a.elapsed_time(b) for a, b in ev]
+    return total_ms, per_launch
+
+
+def time_decode_e2e(torch, gdn, t, steps, warmup, world):
+    """Each step: pinned host -> device copy of the step's q, k, v, g, beta,
+    the decode call, device -> host copy of o.  The state cache stays
+    resident on the device (it is the cache)."""
+    host = {n: t[n].cpu().pin_memory() for n in ("q", "k", "v", "g", "beta")}
+    o_host = torch.empty(t["o"].shape, dtype=t["o"].dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host.values())
+    d2h = o_host.numel() * o_host.element_size()
+
+    def step():
+        for n, x in host.items():
+            t[n].copy_(x, non_blocking=True)
+        run_decode(gdn, t)
+        o_host.copy_(t["o"], non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(torch, world)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    barrier(torch, world)
+    return s.elapsed_time(e), h2d, d2h
+
+
+def prefill_case(torch, gdn, wl, dev, reps, E=0):
+    b = wl["prefill"]
+    q, k, v = bf16(torch, b.q, dev), bf16(torch, b.k, dev), bf16(torch, b.v, dev)
+    g, beta = torch.from_numpy(b.g).to(dev), torch.from_numpy(b.beta).to(dev)
+    cu = torch.from_numpy(b.cu_seqlens.astype(np.int32)).to(dev)
+    cu_h = [int(x) for x in b.cu_seqlens]
+    n = b.num_seqs
+    cache = torch.zeros((n, b.h_v, b.d, b.d), dtype=torch.float32, device=dev)
+    dst = torch.arange(n, dtype=torch.int32, device=dev)
+    o = torch.empty((b.total_tokens, b.h_v, b.d), dtype=torch.bfloat16, device=dev)
+    n_emit = gdn.gdn_prefill_num_emits(cu_h, E) if E else 0
+    cs = torch.empty((max(n_emit, 1), b.h_v, b.d, b.d), dtype=torch.float32, device=dev) if E else None
+
+    def call():
+        gdn.gdn_prefill_varlen(q, k, v, g, beta, cu, cu_h, o, state=cache, dst_slot=dst,
+                               chunk_states=cs, emit_every_chunks=E)
+
+    call()
+    torch.cuda.synchronize()
+    ev = []
+    for _ in range(reps):
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        z.record()
+        ev.append((a, z))
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(z) for a, z in ev)
+    T = b.total_tokens
+    fl = prefill_flops_per_token(b.h_k, b.h_v, b.d) * T
+    return {"workload": wl["name"], "seqlens": b.seqlens if n <= 16 else f"{n} x {b.seqlens[0]}",
+            "tokens": T, "ms": ms, "tokens_per_s": T / (ms * 1e-3),
+            "algorithmic_tflops": fl / (ms * 1e-3) / 1e12, "emit_every_chunks": E,
+            "emitted_states": n_emit}
+
+
+def mixed_case(torch, gdn, dev, reps):
+    wl = gi.mixed_step(0)
+    dec, pre = wl["decode"], wl["prefill"]
+    nd = dec.num_seqs
+    cat = lambda n: np.concatenate([getattr(dec, n), getattr(pre, n)])
+    q, k, v = bf16(torch, cat("q"), dev), bf16(torch, cat("k"), dev), bf16(torch, cat("v"), dev)
+    g, beta = torch.from_numpy(cat("g")).to(dev), torch.from_numpy(cat("beta")).to(dev)
+    slots = torch.from_numpy(wl["src_slot"]).to(dev)
+    cache = torch.zeros((wl["n_slots"], H, D, D), dtype=torch.float32, device=dev)
+    cache[slots[:nd].long()] = torch.from_numpy(np.swapaxes(dec.init_state, -1, -2).copy()).to(dev)
+    o = torch.empty((q.shape[0], H, D), dtype=torch.bfloat16, device=dev)
+    cu = torch.from_numpy(pre.cu_seqlens.astype(np.int32)).to(dev)
+    cu_h = [int(x) for x in pre.cu_seqlens]
+
+    def call():
+        gdn.gdn_mixed_step(nd, q, k, v, g, beta, cu, cu_h, cache, slots[:nd], o, pre_dst_slot=slots[nd:])
+
+    call()
+    torch.cuda.synchronize()
+    ev = []
+    for _ in range(reps):
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        z.record()
+        ev.append((a, z))
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(z) for a, z in ev)
+    return {"workload": wl["name"], "decode_rows": nd, "prefill_seqlens": pre.seqlens, "ms": ms,
+            "tokens_per_s": (nd + pre.total_tokens) / (ms * 1e-3)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_decode_rate(n_rows, n_steps, seed=0):
+    """Time the fp64 oracle on n_rows decode rows x n_steps tokens each, all
+    host cores; returns (rows/s, seconds, threads)."""
+    import oracle
+    b = gi.token_batch([n_steps] * n_rows, H, H, D, seed, init_state=True)
+    threads = oracle.max_threads()
+    t0 = time.perf_counter()
+    oracle.run_chains(b, n_threads=threads)
+    dt = time.perf_counter() - t0
+    return n_rows * n_steps / dt, dt, threads
+
+
+def cpu_baseline(target_s=10.0):
+    """Oracle on a bounded sample of the decode workload: all 256 rows, as
+    many recurrent steps as fit in about target_s seconds."""
+    steps = 1
+    while True:
+        rate, dt, threads = oracle_decode_rate(DECODE_ROWS, steps)
+        if dt >= target_s or steps >= 4096:
+            break
+        steps = max(steps * 2, int(steps * target_s / max(dt, 1e-3) * 1.1))
+    return {"value": rate, "unit": "decode rows/s", "cores": threads, "kind": "oracle",
+            "seconds": dt,
+            "sample": f"{DECODE_ROWS} rows x {steps} recurrent steps of the 256-row decode workload "
+                      f"(H=16, d=128), fp64 token recurrence, OpenMP over (row, head) chains"}
+
+
+def reference_arm(args):
+    import torch
+    world, rank, _ = dist_setup(torch)
+    if rank != 0:
+        return
+    rows = 64
+    rate, dt, threads = oracle_decode_rate(rows, 1)
+    for _ in range(args.warmup):
+        oracle_decode_rate(rows, 1)
+    times = []
+    for _ in range(args.steps):
+        r, d, threads = oracle_decode_rate(rows, 1)
+        times.append(d)
+    tot = sum(times)
+    value = rows * args.steps / tot
+    line = {"impl": "reference", "metric": "GDN decode rows/s", "value": value, "unit": "rows/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode_r256_h16_d128 (each step: a 64-row sample)",
+                       "rows_per_step": rows, "heads": H, "d": D},
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{rows} of the 256 decode rows per step, 1 recurrent step"},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
+    ap.add_argument("--no-extra", action="store_true", help="skip the prefill/mixed workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        reference_arm(args)
+        return
+
+    import torch
+    world, rank, local = dist_setup(torch)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    dev = f"cuda:{local}"
+    from linear_attention_serving_gdn_gb300 import _build
+    if rank == 0 or world == 1:
+        _build.build()
+    barrier(torch, world)
+    import linear_attention_serving_gdn_gb300 as gdn
+    peaks = load_peaks()
+
+    wl, t = decode_setup(torch, seed=rank, dev=dev)
+    with Clocks(torch.cuda.current_device()) as clk:
+        total_ms, per_launch = time_decode(torch, gdn, t, args.steps, args.warmup, world)
+    clocks = clk.summary()
+    total_ms = max_over_ranks(torch, world, total_ms)
+    e2e_ms, h2d, d2h = time_decode_e2e(torch, gdn, t, args.steps, args.warmup, world)
+    e2e_ms = max_over_ranks(torch, world, e2e_ms)
+
+    rows_total = DECODE_ROWS * args.steps * world
+    value = rows_total / (total_ms * 1e-3)
+    launch_ms = statistics.mean(per_launch)
+    bytes_per_launch = DECODE_BYTES_PER_ROW * DECODE_ROWS
+    achieved = bytes_per_launch / (launch_ms * 1e-3) / 1e9
+    line = {
+        "metric": "GDN decode rows/s (packed recurrent decode, fp32 state)",
+        "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 state / bf16 activations", "data": "synthetic",
+        "config": {"workload": wl["name"], "rows": DECODE_ROWS, "heads": H, "d_k": D, "d_v": D,
+                   "cache_slots": wl["n_slots"], "state_bytes": DECODE_ROWS * H * D * D * 4,
+                   "l2_policy": "inputs larger than L2 (256 MiB of states read+written per step)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel<128>", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": None, "peak_source": peaks["source"] + " (burst copy)",
+                     "bytes_per_launch": bytes_per_launch, "launch_ms": launch_ms},
+        "e2e": {"value": rows_total / (e2e_ms * 1e-3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_extra:
+        extra = []
+        extra.append(prefill_case(torch, gdn, gi.prefill_qwen3next_gva(0), dev, reps=5))
+        extra.append(prefill_case(torch, gdn, gi.prefix_cache_prefill(0), dev, reps=3, E=17))
+        extra.append(mixed_case(torch, gdn, dev, reps=5))
+        for x in extra:
+            if "algorithmic_tflops" in x:
+                x["tensor_frac_of_bf16_peak"] = x["algorithmic_tflops"] / peaks["bf16_tflops"]
+        line["workloads"] = extra
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

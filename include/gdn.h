@@ -1,0 +1,213 @@
+/*
+ * gdn.h -- C ABI of libgdn, the Gated DeltaNet linear-attention hot path for
+ * one NVIDIA GB300 (sm_103a).
+ *
+ * The operation.  For each (sequence or decode row, value head h) the library
+ * runs the gated delta rule of Gated DeltaNet (Yang, Kautz, Hatamizadeh,
+ * "Gated Delta Networks: Improving Mamba2 with Delta Rule", ICLR 2025) on a
+ * per-head fp32 state S in R^{d_k x d_v}:
+ *
+ *     alpha_t = exp(g_t)
+ *     S_t     = alpha_t S_{t-1} - beta_t k_t (k_t^T (alpha_t S_{t-1})) + beta_t k_t v_t^T
+ *     o_t     = scale * S_t^T q_t
+ *
+ * Value head h reads the q/k of key head h / (h_v / h_k) (grouped value
+ * attention with contiguous groups).
+ *
+ * Routes, after the vLLM page "Enable batch-invariant mixed decode and
+ * prefill for Qwen GDN" (sections "Why" and "How"): cached decode rows always
+ * run on the packed recurrent decode kernel, also when fresh prefills share
+ * the step, so a row's arithmetic never depends on what else is batched with
+ * it; fresh prefill rows run through the chunked prefill on a fixed 64-token
+ * chunk grid anchored at each sequence's first token of the call.  The
+ * prefill can emit the carried state at chunk boundaries (the vLLM page
+ * "GatedDeltaNet Automatic Prefix Caching", section "Purpose") so that prefix
+ * caches can be filled and later resumed on the lcm(64, block) grid (the vLLM
+ * page "Enable GDN batch-invariant prefix caching", section "Purpose").
+ *
+ * Conventions shared by every entry point.
+ *   - All tensors are dense, row-major, in device memory unless the argument
+ *     name ends in _host.  bf16 tensors are passed as gdn_bf16 (raw bits).
+ *   - Token-major activations: q, k [T][h_k][d_k]; v, o [T][h_v][d_v];
+ *     g, beta [T][h_v] fp32.  Decode rows are tokens.
+ *   - State cache: float state[num_slots][h_v][d_v][d_k], i.e. each slot holds
+ *     S^T per value head with d_k contiguous.  Slots are chosen per row or
+ *     sequence by int32 index arrays in device memory.
+ *   - Ownership: the caller owns every buffer.  The library allocates no
+ *     device or host memory, keeps no state between calls, never
+ *     synchronises the host, and enqueues all work on `stream` (a
+ *     cudaStream_t; NULL = legacy default stream).
+ *   - Errors: arguments are validated on the host before anything is
+ *     launched; a bad argument returns GDN_ERR_INVALID_ARG or
+ *     GDN_ERR_UNSUPPORTED and launches nothing.  A failed launch returns
+ *     GDN_ERR_CUDA.  Problems only the device can see (a slot index out of
+ *     range) skip the affected row or sequence, zero its outputs and OR a
+ *     GDN_DEV_* bit into *dev_status when dev_status is not NULL; kernels
+ *     never trap.
+ *   - Only d_k == d_v in {64, 128} is supported; h_v % h_k == 0.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t gdn_bf16; /* bfloat16 bit pattern */
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1, /* null pointer, bad size, non-monotone cu_seqlens, ... */
+    GDN_ERR_UNSUPPORTED = 2, /* head dims or shapes this build does not implement */
+    GDN_ERR_CUDA = 3         /* a CUDA runtime call or launch failed */
+} gdn_status_t;
+
+/* Bits ORed into *dev_status by kernels. */
+#define GDN_DEV_BAD_SLOT 0x1 /* a slot index was >= num_slots; the row/sequence was skipped */
+#define GDN_DEV_TIMEOUT 0x2  /* a bounded wait expired inside a kernel; its outputs are invalid */
+
+typedef struct {
+    int32_t h_k;  /* query/key heads */
+    int32_t h_v;  /* value heads (multiple of h_k) */
+    int32_t d_k;  /* key head dim */
+    int32_t d_v;  /* value head dim */
+    float scale;  /* multiplies o; the literal recurrence uses 1.0 */
+} gdn_dims_t;
+
+/*
+ * Packed recurrent decode: one token per cached row.
+ * vLLM page "Enable batch-invariant mixed decode and prefill for Qwen GDN",
+ * section "How" (the shared packed recurrent decode helper for cached rows);
+ * state recycling between slots after "GatedDeltaNet Automatic Prefix
+ * Caching", section "Purpose" (copy the last computed block into the newly
+ * scheduled slot).
+ *
+ *   num_rows   rows (tokens); 0 is a no-op.
+ *   q, k       [num_rows][h_k][d_k] bf16;  v [num_rows][h_v][d_v] bf16
+ *   g, beta    [num_rows][h_v] fp32 (alpha = exp(g))
+ *   state      [num_slots][h_v][d_v][d_k] fp32, read at src_slot[r] and
+ *              written at dst_slot[r] (in place when equal).
+ *   src_slot   [num_rows] int32; a negative entry marks a padded row: it is
+ *              skipped and its o rows are zeroed.
+ *   dst_slot   [num_rows] int32, or NULL for dst == src.  Two rows of one
+ *              call must not share a destination slot.
+ *   o          [num_rows][h_v][d_v] bf16 output.
+ *   dev_status optional device int32 (see GDN_DEV_*).
+ * Each (row, head) reads and writes its 64 KiB (d=128) state exactly once;
+ * results of a row depend only on that row's inputs and state, bit for bit.
+ */
+gdn_status_t gdn_decode_packed(const gdn_dims_t *dims, int32_t num_rows,
+                               const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                               const float *g, const float *beta,
+                               float *state, int64_t num_slots,
+                               const int32_t *src_slot, const int32_t *dst_slot,
+                               gdn_bf16 *o, int32_t *dev_status, void *stream);
+
+/*
+ * Chunked varlen prefill on the 64-token chunk grid.
+ * vLLM page "Enable batch-invariant mixed decode and prefill for Qwen GDN",
+ * section "How" (fresh prefill rows go through chunk prefill), and
+ * "GatedDeltaNet Automatic Prefix Caching", section "Purpose" (optional
+ * per-chunk intermediate states as one flat stream).
+ *
+ *   num_seqs          sequences; sequence s holds tokens
+ *                     [cu_seqlens[s], cu_seqlens[s+1]).  Empty sequences are
+ *                     allowed (their final state is the initial state).
+ *   cu_seqlens        device int32 [num_seqs+1], cu_seqlens[0] == 0.
+ *   cu_seqlens_host   host mirror of cu_seqlens (same values), used for
+ *                     validation and launch sizing; never dereferenced on
+ *                     the device.
+ *   q, k, v, g, beta  token-major as above, T = cu_seqlens_host[num_seqs].
+ *   state, num_slots  slot cache as above.
+ *   src_slot          device int32 [num_seqs]: initial state slot; a negative
+ *                     entry (or src_slot == NULL) starts from S = 0.
+ *   dst_slot          device int32 [num_seqs]: slot receiving the final state;
+ *                     a negative entry (or dst_slot == NULL) skips the write.
+ *   o                 [T][h_v][d_v] bf16.
+ *   chunk_states      optional fp32 stream [n_emit][h_v][d_v][d_k].  When
+ *   emit_every_chunks E > 0, after every E-th FULL 64-token chunk c of
+ *                     sequence s (i.e. (c+1) % E == 0) the carried state is
+ *                     written at entry emit_offset(s) + (c+1)/E - 1 where
+ *                     emit_offset(s) = sum_{s' < s} floor(L_s' / (64 E)).
+ *                     E = 17 puts states on the 1088-token block grid.
+ *   chunk_states_capacity  entries available in chunk_states; must be at
+ *                     least gdn_prefill_num_emits(...).
+ * Resuming a sequence from the state emitted after token 64*E*j with its
+ * tokens [64*E*j, L) reproduces the uninterrupted outputs and final state
+ * bit for bit; so does running a sequence alone or inside any batch.
+ */
+gdn_status_t gdn_prefill_varlen(const gdn_dims_t *dims, int32_t num_seqs,
+                                const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                                const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                                const float *g, const float *beta,
+                                float *state, int64_t num_slots,
+                                const int32_t *src_slot, const int32_t *dst_slot,
+                                gdn_bf16 *o,
+                                float *chunk_states, int32_t emit_every_chunks,
+                                int64_t chunk_states_capacity,
+                                int32_t *dev_status, void *stream);
+
+/*
+ * One mixed continuous-batching step: num_decodes cached decode rows at the
+ * front of the token batch, then num_prefills fresh prefill sequences.
+ * vLLM page "Enable batch-invariant mixed decode and prefill for Qwen GDN",
+ * sections "How" and "Test plan" (the route regression: decode rows alone and
+ * at the front of a mixed batch give bitwise equal outputs and states).
+ *
+ *   Token rows [0, num_decodes) are decode rows; prefill sequence s holds
+ *   rows num_decodes + [cu_seqlens_p[s], cu_seqlens_p[s+1]).
+ *   dec_src_slot/dec_dst_slot: as gdn_decode_packed (num_decodes entries).
+ *   pre_src_slot/pre_dst_slot: as gdn_prefill_varlen (num_prefills entries).
+ *   Remaining arguments as gdn_prefill_varlen; o covers all rows.
+ * The decode rows run on the same kernel and arithmetic as
+ * gdn_decode_packed, so their outputs and states are bitwise identical to a
+ * decode-only call, whatever prefills share the step.
+ */
+gdn_status_t gdn_mixed_step(const gdn_dims_t *dims, int32_t num_decodes, int32_t num_prefills,
+                            const int32_t *cu_seqlens_p, const int32_t *cu_seqlens_p_host,
+                            const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                            const float *g, const float *beta,
+                            float *state, int64_t num_slots,
+                            const int32_t *dec_src_slot, const int32_t *dec_dst_slot,
+                            const int32_t *pre_src_slot, const int32_t *pre_dst_slot,
+                            gdn_bf16 *o,
+                            float *chunk_states, int32_t emit_every_chunks,
+                            int64_t chunk_states_capacity,
+                            int32_t *dev_status, void *stream);
+
+/* ---- host-only helpers (no device work) ------------------------------- */
+
+/* Total emitted states of a prefill call: sum_s floor(L_s / (64 E)); 0 when
+ * E <= 0; -1 on a bad argument. */
+int64_t gdn_prefill_num_emits(const int32_t *cu_seqlens_host, int32_t num_seqs,
+                              int32_t emit_every_chunks);
+
+/* Per-sequence first entry in chunk_states: out[s] = emit_offset(s) for
+ * s in [0, num_seqs], out[num_seqs] = total.  Returns GDN_OK or
+ * GDN_ERR_INVALID_ARG. */
+gdn_status_t gdn_prefill_emit_offsets(const int32_t *cu_seqlens_host, int32_t num_seqs,
+                                      int32_t emit_every_chunks, int64_t *out);
+
+/* Prefix-cache grid ("Enable GDN batch-invariant prefix caching", section
+ * "Purpose"): the cache block size rounded up to a multiple of the 64-token
+ * chunk (1056 -> 1088); returns -1 for block_size <= 0. */
+int32_t gdn_align_block_size(int32_t block_size);
+
+/* Usable prefix hit: floored onto the lcm(64, aligned block) grid unless the
+ * hit covers the full prompt (1100 -> 1088, 200 -> 0 with 1056-token
+ * blocks).  Returns -1 on a bad argument. */
+int64_t gdn_floor_prefix_hit(int64_t hit_tokens, int64_t prompt_tokens, int32_t block_size);
+
+/* Emission stride, in chunks, of the grid above (1088 / 64 = 17). */
+int32_t gdn_grid_emit_every_chunks(int32_t block_size);
+
+const char *gdn_status_string(gdn_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,283 @@
+"""Gated DeltaNet linear-attention hot path for one GB300 (sm_103a).
+
+A thin ctypes binding over ``libgdn.so`` (C ABI in ``include/gdn.h``).  The
+functions below carry the C names; they only check and marshal PyTorch
+tensors (dtype, device, contiguity, shapes) into pointers and the current CUDA
+stream.  Every step of the computation runs in the library's CUDA kernels;
+there is no fallback of any kind: if the library is missing, every entry
+point raises.
+
+Layouts (all row-major, device memory):
+  q, k        [T][h_k][d_k]  bfloat16
+  v, o        [T][h_v][d_v]  bfloat16
+  g, beta     [T][h_v]       float32   (alpha = exp(g))
+  state       [num_slots][h_v][d_v][d_k] float32   (S^T per slot and head)
+  chunk_states [n_emit][h_v][d_v][d_k] float32
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "GdnError", "load_library", "library_path",
+    "gdn_decode_packed", "gdn_prefill_varlen", "gdn_mixed_step",
+    "gdn_prefill_num_emits", "gdn_prefill_emit_offsets", "gdn_align_block_size",
+    "gdn_floor_prefix_hit", "gdn_grid_emit_every_chunks", "gdn_status_string",
+    "EXPORTED_SYMBOLS", "GDN_DEV_BAD_SLOT", "GDN_DEV_TIMEOUT",
+]
+
+GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA = 0, 1, 2, 3
+GDN_DEV_BAD_SLOT, GDN_DEV_TIMEOUT = 0x1, 0x2
+
+EXPORTED_SYMBOLS = (
+    "gdn_decode_packed", "gdn_prefill_varlen", "gdn_mixed_step",
+    "gdn_prefill_num_emits", "gdn_prefill_emit_offsets", "gdn_align_block_size",
+    "gdn_floor_prefix_hit", "gdn_grid_emit_every_chunks", "gdn_status_string",
+)
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, fn: str):
+        self.status = status
+        super().__init__(f"{fn}: {gdn_status_string(status)}")
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("h_k", ctypes.c_int32), ("h_v", ctypes.c_int32), ("d_k", ctypes.c_int32),
+                ("d_v", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libgdn.so (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        raise ImportError(f"libgdn.so is not built ({_build.LIB}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(_build.LIB)
+    lib.gdn_decode_packed.restype = ctypes.c_int
+    lib.gdn_decode_packed.argtypes = [ctypes.POINTER(Dims), _I32, _P, _P, _P, _P, _P, _P, _I64,
+                                      _P, _P, _P, _P, _P]
+    lib.gdn_prefill_varlen.restype = ctypes.c_int
+    lib.gdn_prefill_varlen.argtypes = [ctypes.POINTER(Dims), _I32, _P, _P, _P, _P, _P, _P, _P,
+                                       _P, _I64, _P, _P, _P, _P, _I32, _I64, _P, _P]
+    lib.gdn_mixed_step.restype = ctypes.c_int
+    lib.gdn_mixed_step.argtypes = [ctypes.POINTER(Dims), _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
+                                   _P, _I64, _P, _P, _P, _P, _P, _P, _I32, _I64, _P, _P]
+    lib.gdn_prefill_num_emits.restype = _I64
+    lib.gdn_prefill_num_emits.argtypes = [_P, _I32, _I32]
+    lib.gdn_prefill_emit_offsets.restype = ctypes.c_int
+    lib.gdn_prefill_emit_offsets.argtypes = [_P, _I32, _I32, _P]
+    lib.gdn_align_block_size.restype = _I32
+    lib.gdn_align_block_size.argtypes = [_I32]
+    lib.gdn_floor_prefix_hit.restype = _I64
+    lib.gdn_floor_prefix_hit.argtypes = [_I64, _I64, _I32]
+    lib.gdn_grid_emit_every_chunks.restype = _I32
+    lib.gdn_grid_emit_every_chunks.argtypes = [_I32]
+    lib.gdn_status_string.restype = ctypes.c_char_p
+    lib.gdn_status_string.argtypes = [ctypes.c_int]
+    _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+
+def _dev(t, name, dtype, ndim=None, optional=False):
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    return t
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _host_i32(x, name):
+    if isinstance(x, torch.Tensor):
+        if x.is_cuda:
+            raise ValueError(f"{name} must live in host memory")
+        x = x.to(torch.int32).contiguous()
+        return x, ctypes.c_void_p(x.data_ptr())
+    arr = (ctypes.c_int32 * len(x))(*[int(v) for v in x])
+    return arr, ctypes.cast(arr, ctypes.c_void_p)
+
+
+def _check(status, fn):
+    if status != GDN_OK:
+        raise GdnError(status, fn)
+
+
+def _dims(q, v, scale):
+    return Dims(q.shape[1], v.shape[1], q.shape[2], v.shape[2], float(scale))
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+
+def gdn_decode_packed(q, k, v, g, beta, state, src_slot, o, dst_slot=None, dev_status=None,
+                      scale: float = 1.0, stream=None) -> None:
+    """Packed recurrent decode of ``q.shape[0]`` cached rows (see gdn.h)."""
+    lib = load_library()
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    q, k, v = _dev(q, "q", bf, 3), _dev(k, "k", bf, 3), _dev(v, "v", bf, 3)
+    g, beta = _dev(g, "g", f32, 2), _dev(beta, "beta", f32, 2)
+    state = _dev(state, "state", f32, 4)
+    src_slot = _dev(src_slot, "src_slot", i32, 1)
+    dst_slot = _dev(dst_slot, "dst_slot", i32, 1, optional=True)
+    o = _dev(o, "o", bf, 3)
+    dev_status = _dev(dev_status, "dev_status", i32, optional=True)
+    rows = q.shape[0]
+    if not (k.shape == q.shape and v.shape[0] == rows and o.shape == v.shape
+            and g.shape == (rows, v.shape[1]) and beta.shape == g.shape
+            and src_slot.shape[0] == rows and (dst_slot is None or dst_slot.shape[0] == rows)
+            and state.shape[1:] == (v.shape[1], v.shape[2], q.shape[2])):
+        raise ValueError("inconsistent decode shapes")
+    d = _dims(q, v, scale)
+    _check(lib.gdn_decode_packed(ctypes.byref(d), rows, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                 _ptr(beta), _ptr(state), state.shape[0], _ptr(src_slot),
+                                 _ptr(dst_slot), _ptr(o), _ptr(dev_status), _stream(stream)),
+           "gdn_decode_packed")
+
+
+def gdn_prefill_varlen(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, o, state=None,
+                       src_slot=None, dst_slot=None, chunk_states=None, emit_every_chunks: int = 0,
+                       dev_status=None, scale: float = 1.0, stream=None) -> None:
+    """Chunked varlen prefill (see gdn.h).  ``cu_seqlens_host`` is a host
+    sequence (list or CPU tensor) with the same values as ``cu_seqlens``."""
+    lib = load_library()
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    q, k, v = _dev(q, "q", bf, 3), _dev(k, "k", bf, 3), _dev(v, "v", bf, 3)
+    g, beta = _dev(g, "g", f32, 2), _dev(beta, "beta", f32, 2)
+    o = _dev(o, "o", bf, 3)
+    cu_seqlens = _dev(cu_seqlens, "cu_seqlens", i32, 1)
+    state = _dev(state, "state", f32, 4, optional=True)
+    src_slot = _dev(src_slot, "src_slot", i32, 1, optional=True)
+    dst_slot = _dev(dst_slot, "dst_slot", i32, 1, optional=True)
+    chunk_states = _dev(chunk_states, "chunk_states", f32, 4, optional=True)
+    dev_status = _dev(dev_status, "dev_status", i32, optional=True)
+    keep, cu_h = _host_i32(cu_seqlens_host, "cu_seqlens_host")
+    n = cu_seqlens.shape[0] - 1
+    if len(keep) != n + 1:
+        raise ValueError("cu_seqlens_host must have num_seqs + 1 entries")
+    T = q.shape[0]
+    if not (k.shape == q.shape and v.shape[0] == T and o.shape == v.shape
+            and g.shape == (T, v.shape[1]) and beta.shape == g.shape):
+        raise ValueError("inconsistent prefill shapes")
+    d = _dims(q, v, scale)
+    cap = 0 if chunk_states is None else chunk_states.shape[0]
+    _check(lib.gdn_prefill_varlen(ctypes.byref(d), n, _ptr(cu_seqlens), cu_h, _ptr(q), _ptr(k),
+                                  _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+                                  0 if state is None else state.shape[0], _ptr(src_slot),
+                                  _ptr(dst_slot), _ptr(o), _ptr(chunk_states),
+                                  int(emit_every_chunks), cap, _ptr(dev_status), _stream(stream)),
+           "gdn_prefill_varlen")
+
+
+def gdn_mixed_step(num_decodes: int, q, k, v, g, beta, cu_seqlens_p, cu_seqlens_p_host, state,
+                   dec_src_slot, o, dec_dst_slot=None, pre_src_slot=None, pre_dst_slot=None,
+                   chunk_states=None, emit_every_chunks: int = 0, dev_status=None,
+                   scale: float = 1.0, stream=None) -> None:
+    """Mixed step: decode rows [0, num_decodes) then prefill sequences."""
+    lib = load_library()
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    q, k, v = _dev(q, "q", bf, 3), _dev(k, "k", bf, 3), _dev(v, "v", bf, 3)
+    g, beta = _dev(g, "g", f32, 2), _dev(beta, "beta", f32, 2)
+    o = _dev(o, "o", bf, 3)
+    state = _dev(state, "state", f32, 4)
+    dec_src_slot = _dev(dec_src_slot, "dec_src_slot", i32, 1, optional=num_decodes == 0)
+    dec_dst_slot = _dev(dec_dst_slot, "dec_dst_slot", i32, 1, optional=True)
+    pre_src_slot = _dev(pre_src_slot, "pre_src_slot", i32, 1, optional=True)
+    pre_dst_slot = _dev(pre_dst_slot, "pre_dst_slot", i32, 1, optional=True)
+    chunk_states = _dev(chunk_states, "chunk_states", f32, 4, optional=True)
+    dev_status = _dev(dev_status, "dev_status", i32, optional=True)
+    cu_seqlens_p = _dev(cu_seqlens_p, "cu_seqlens_p", i32, 1, optional=True)
+    n_p = 0 if cu_seqlens_p is None else cu_seqlens_p.shape[0] - 1
+    keep, cu_h = _host_i32(cu_seqlens_p_host if cu_seqlens_p_host is not None else [0], "cu_seqlens_p_host")
+    if n_p and len(keep) != n_p + 1:
+        raise ValueError("cu_seqlens_p_host must have num_prefills + 1 entries")
+    T = q.shape[0]
+    if not (k.shape == q.shape and v.shape[0] == T and o.shape == v.shape
+            and g.shape == (T, v.shape[1]) and beta.shape == g.shape):
+        raise ValueError("inconsistent mixed-step shapes")
+    if n_p and int(keep[-1]) + num_decodes != T:
+        raise ValueError("token count does not match num_decodes + cu_seqlens_p_host[-1]")
+    d = _dims(q, v, scale)
+    cap = 0 if chunk_states is None else chunk_states.shape[0]
+    _check(lib.gdn_mixed_step(ctypes.byref(d), int(num_decodes), n_p, _ptr(cu_seqlens_p), cu_h,
+                              _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+                              state.shape[0], _ptr(dec_src_slot), _ptr(dec_dst_slot),
+                              _ptr(pre_src_slot), _ptr(pre_dst_slot), _ptr(o), _ptr(chunk_states),
+                              int(emit_every_chunks), cap, _ptr(dev_status), _stream(stream)),
+           "gdn_mixed_step")
+
+
+# ---------------------------------------------------------------------------
+# host-only helpers
+# ---------------------------------------------------------------------------
+
+def gdn_prefill_num_emits(cu_seqlens_host, emit_every_chunks: int) -> int:
+    keep, p = _host_i32(cu_seqlens_host, "cu_seqlens_host")
+    n = load_library().gdn_prefill_num_emits(p, len(keep) - 1, int(emit_every_chunks))
+    if n < 0:
+        raise ValueError("invalid cu_seqlens_host")
+    return int(n)
+
+
+def gdn_prefill_emit_offsets(cu_seqlens_host, emit_every_chunks: int) -> list[int]:
+    keep, p = _host_i32(cu_seqlens_host, "cu_seqlens_host")
+    out = (ctypes.c_int64 * len(keep))()
+    _check(load_library().gdn_prefill_emit_offsets(p, len(keep) - 1, int(emit_every_chunks),
+                                                   ctypes.cast(out, ctypes.c_void_p)),
+           "gdn_prefill_emit_offsets")
+    return [int(x) for x in out]
+
+
+def gdn_align_block_size(block_size: int) -> int:
+    return int(load_library().gdn_align_block_size(int(block_size)))
+
+
+def gdn_floor_prefix_hit(hit_tokens: int, prompt_tokens: int, block_size: int) -> int:
+    return int(load_library().gdn_floor_prefix_hit(int(hit_tokens), int(prompt_tokens), int(block_size)))
+
+
+def gdn_grid_emit_every_chunks(block_size: int) -> int:
+    return int(load_library().gdn_grid_emit_every_chunks(int(block_size)))
+
+
+def gdn_status_string(status: int) -> str:
+    return load_library().gdn_status_string(int(status)).decode()

@@ -1,0 +1,236 @@
+// C ABI of libgdn: host-side validation, then kernel launches on the caller's
+// stream.  See include/gdn.h for the contract of each entry point.
+#include <limits.h>
+
+#include "gdn_internal.cuh"
+
+namespace {
+
+using gdn::kChunk;
+
+bool dims_ok(const gdn_dims_t *d, gdn_status_t *why) {
+    if (!d) {
+        *why = GDN_ERR_INVALID_ARG;
+        return false;
+    }
+    if (d->h_k <= 0 || d->h_v <= 0 || d->d_k <= 0 || d->d_v <= 0 || d->h_v % d->h_k != 0) {
+        *why = GDN_ERR_INVALID_ARG;
+        return false;
+    }
+    if (d->d_k != d->d_v || (d->d_k != 64 && d->d_k != 128)) {
+        *why = GDN_ERR_UNSUPPORTED;
+        return false;
+    }
+    return true;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validates a host cu_seqlens mirror: starts at 0, non-decreasing.
+bool cu_ok(const int32_t *cu, int32_t n) {
+    if (!cu || cu[0] != 0) return false;
+    for (int32_t i = 0; i < n; ++i)
+        if (cu[i + 1] < cu[i]) return false;
+    return true;
+}
+
+int64_t num_emits(const int32_t *cu, int32_t n, int32_t E) {
+    if (E <= 0) return 0;
+    int64_t tot = 0;
+    for (int32_t i = 0; i < n; ++i) tot += (cu[i + 1] - cu[i]) / (static_cast<int64_t>(kChunk) * E);
+    return tot;
+}
+
+gdn_status_t decode_impl(const gdn_dims_t *dims, int32_t num_rows, const gdn_bf16 *q,
+                         const gdn_bf16 *k, const gdn_bf16 *v, const float *g, const float *beta,
+                         float *state, int64_t num_slots, const int32_t *src_slot,
+                         const int32_t *dst_slot, gdn_bf16 *o, int32_t *dev_status,
+                         cudaStream_t stream) {
+    gdn_status_t why = GDN_OK;
+    if (!dims_ok(dims, &why)) return why;
+    if (num_rows < 0 || num_slots < 0) return GDN_ERR_INVALID_ARG;
+    if (num_rows == 0) return GDN_OK;
+    if (!q || !k || !v || !g || !beta || !state || !src_slot || !o) return GDN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(state) || !aligned16(o))
+        return GDN_ERR_INVALID_ARG;
+    gdn::DecodeArgs a;
+    a.num_rows = num_rows;
+    a.h_k = dims->h_k;
+    a.h_v = dims->h_v;
+    a.scale = dims->scale;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.g = g;
+    a.beta = beta;
+    a.state = state;
+    a.num_slots = num_slots;
+    a.src_slot = src_slot;
+    a.dst_slot = dst_slot;
+    a.o = o;
+    a.dev_status = dev_status;
+    return gdn::launch_decode(a, dims->d_k, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status_t prefill_impl(const gdn_dims_t *dims, int32_t num_seqs, const int32_t *cu_seqlens,
+                          const int32_t *cu_host, const gdn_bf16 *q, const gdn_bf16 *k,
+                          const gdn_bf16 *v, const float *g, const float *beta, float *state,
+                          int64_t num_slots, const int32_t *src_slot, const int32_t *dst_slot,
+                          gdn_bf16 *o, float *chunk_states, int32_t E, int64_t capacity,
+                          int32_t *dev_status, cudaStream_t stream) {
+    gdn_status_t why = GDN_OK;
+    if (!dims_ok(dims, &why)) return why;
+    if (num_seqs < 0 || num_slots < 0 || E < 0) return GDN_ERR_INVALID_ARG;
+    if (num_seqs == 0) return GDN_OK;
+    if (!cu_seqlens || !cu_ok(cu_host, num_seqs)) return GDN_ERR_INVALID_ARG;
+    const int64_t T = cu_host[num_seqs];
+    if ((src_slot || dst_slot) && !state) return GDN_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(state) || !aligned16(o) ||
+        !aligned16(chunk_states))
+        return GDN_ERR_INVALID_ARG;
+    if (E > 0) {
+        const int64_t need = num_emits(cu_host, num_seqs, E);
+        if (need > 0 && (!chunk_states || capacity < need)) return GDN_ERR_INVALID_ARG;
+    }
+    if (static_cast<int64_t>(num_seqs) * dims->h_v > INT_MAX) return GDN_ERR_UNSUPPORTED;
+    int32_t max_len = 0;
+    for (int32_t i = 0; i < num_seqs; ++i)
+        if (cu_host[i + 1] - cu_host[i] > max_len) max_len = cu_host[i + 1] - cu_host[i];
+    gdn::PrefillArgs a;
+    a.num_seqs = num_seqs;
+    a.h_k = dims->h_k;
+    a.h_v = dims->h_v;
+    a.scale = dims->scale;
+    a.cu_seqlens = cu_seqlens;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.g = g;
+    a.beta = beta;
+    a.state = state;
+    a.num_slots = num_slots;
+    a.src_slot = src_slot;
+    a.dst_slot = dst_slot;
+    a.o = o;
+    a.chunk_states = E > 0 ? chunk_states : nullptr;
+    a.emit_every_chunks = E;
+    a.dev_status = dev_status;
+    return gdn::launch_prefill(a, dims->d_k, T, max_len, stream) == cudaSuccess ? GDN_OK
+                                                                                  : GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status_t gdn_decode_packed(const gdn_dims_t *dims, int32_t num_rows, const gdn_bf16 *q,
+                               const gdn_bf16 *k, const gdn_bf16 *v, const float *g,
+                               const float *beta, float *state, int64_t num_slots,
+                               const int32_t *src_slot, const int32_t *dst_slot, gdn_bf16 *o,
+                               int32_t *dev_status, void *stream) {
+    return decode_impl(dims, num_rows, q, k, v, g, beta, state, num_slots, src_slot, dst_slot, o,
+                       dev_status, static_cast<cudaStream_t>(stream));
+}
+
+gdn_status_t gdn_prefill_varlen(const gdn_dims_t *dims, int32_t num_seqs,
+                                const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                                const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                                const float *g, const float *beta, float *state,
+                                int64_t num_slots, const int32_t *src_slot,
+                                const int32_t *dst_slot, gdn_bf16 *o, float *chunk_states,
+                                int32_t emit_every_chunks, int64_t chunk_states_capacity,
+                                int32_t *dev_status, void *stream) {
+    return prefill_impl(dims, num_seqs, cu_seqlens, cu_seqlens_host, q, k, v, g, beta, state,
+                        num_slots, src_slot, dst_slot, o, chunk_states, emit_every_chunks,
+                        chunk_states_capacity, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+gdn_status_t gdn_mixed_step(const gdn_dims_t *dims, int32_t num_decodes, int32_t num_prefills,
+                            const int32_t *cu_seqlens_p, const int32_t *cu_seqlens_p_host,
+                            const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                            const float *g, const float *beta, float *state, int64_t num_slots,
+                            const int32_t *dec_src_slot, const int32_t *dec_dst_slot,
+                            const int32_t *pre_src_slot, const int32_t *pre_dst_slot,
+                            gdn_bf16 *o, float *chunk_states, int32_t emit_every_chunks,
+                            int64_t chunk_states_capacity, int32_t *dev_status, void *stream) {
+    gdn_status_t why = GDN_OK;
+    if (!dims_ok(dims, &why)) return why;
+    if (num_decodes < 0 || num_prefills < 0) return GDN_ERR_INVALID_ARG;
+    if (num_prefills > 0 && !cu_ok(cu_seqlens_p_host, num_prefills)) return GDN_ERR_INVALID_ARG;
+    if (num_decodes > 0 && (!dec_src_slot || !state)) return GDN_ERR_INVALID_ARG;
+    // The prefill part starts num_decodes rows into every token-major tensor;
+    // rows are 16-byte multiples for the supported head dims.
+    const size_t hk = static_cast<size_t>(dims->h_k) * dims->d_k;
+    const size_t hv = static_cast<size_t>(dims->h_v) * dims->d_v;
+    const size_t nd = static_cast<size_t>(num_decodes);
+    auto off16 = [&](const gdn_bf16 *p, size_t row) { return p ? p + nd * row : nullptr; };
+    auto offf = [&](const float *p) { return p ? p + nd * dims->h_v : nullptr; };
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // Validate both halves before launching either.
+    if (num_prefills > 0) {
+        const int64_t T = cu_seqlens_p_host[num_prefills];
+        if (T > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
+        if (!cu_seqlens_p || emit_every_chunks < 0) return GDN_ERR_INVALID_ARG;
+        if (emit_every_chunks > 0) {
+            const int64_t need = num_emits(cu_seqlens_p_host, num_prefills, emit_every_chunks);
+            if (need > 0 && (!chunk_states || chunk_states_capacity < need)) return GDN_ERR_INVALID_ARG;
+        }
+    }
+    if (num_decodes > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
+    gdn_status_t s = decode_impl(dims, num_decodes, q, k, v, g, beta, state, num_slots,
+                                 dec_src_slot, dec_dst_slot, o, dev_status, st);
+    if (s != GDN_OK) return s;
+    return prefill_impl(dims, num_prefills, cu_seqlens_p, cu_seqlens_p_host, off16(q, hk),
+                        off16(k, hk), off16(v, hv), offf(g), offf(beta), state, num_slots,
+                        pre_src_slot, pre_dst_slot, o ? o + nd * hv : nullptr, chunk_states,
+                        emit_every_chunks, chunk_states_capacity, dev_status, st);
+}
+
+int64_t gdn_prefill_num_emits(const int32_t *cu_seqlens_host, int32_t num_seqs,
+                              int32_t emit_every_chunks) {
+    if (num_seqs < 0 || (num_seqs > 0 && !cu_ok(cu_seqlens_host, num_seqs))) return -1;
+    return num_emits(cu_seqlens_host, num_seqs, emit_every_chunks);
+}
+
+gdn_status_t gdn_prefill_emit_offsets(const int32_t *cu_seqlens_host, int32_t num_seqs,
+                                      int32_t emit_every_chunks, int64_t *out) {
+    if (!out || num_seqs < 0 || (num_seqs > 0 && !cu_ok(cu_seqlens_host, num_seqs)))
+        return GDN_ERR_INVALID_ARG;
+    out[0] = 0;
+    for (int32_t i = 0; i < num_seqs; ++i)
+        out[i + 1] = out[i] + (emit_every_chunks > 0
+                                   ? (cu_seqlens_host[i + 1] - cu_seqlens_host[i]) /
+                                         (static_cast<int64_t>(kChunk) * emit_every_chunks)
+                                   : 0);
+    return GDN_OK;
+}
+
+int32_t gdn_align_block_size(int32_t block_size) {
+    if (block_size <= 0 || block_size > INT_MAX - kChunk) return -1;
+    return (block_size + kChunk - 1) / kChunk * kChunk;
+}
+
+int32_t gdn_grid_emit_every_chunks(int32_t block_size) {
+    const int32_t b = gdn_align_block_size(block_size);
+    return b < 0 ? -1 : b / kChunk;  // lcm(64, b) == b once b is a multiple of 64
+}
+
+int64_t gdn_floor_prefix_hit(int64_t hit_tokens, int64_t prompt_tokens, int32_t block_size) {
+    const int32_t b = gdn_align_block_size(block_size);
+    if (b < 0 || hit_tokens < 0 || prompt_tokens < 0 || hit_tokens > prompt_tokens) return -1;
+    if (hit_tokens == prompt_tokens) return hit_tokens;
+    return hit_tokens / b * b;
+}
+
+const char *gdn_status_string(gdn_status_t status) {
+    switch (status) {
+        case GDN_OK: return "GDN_OK";
+        case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: invalid argument";
+        case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: unsupported shape";
+        case GDN_ERR_CUDA: return "GDN_ERR_CUDA: CUDA launch or runtime error";
+    }
+    return "unknown gdn_status_t";
+}
+
+}  // extern "C"

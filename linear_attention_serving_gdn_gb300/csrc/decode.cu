@@ -1,0 +1,111 @@
+// Packed recurrent decode: one token per cached row against its fp32 state.
+//
+// vLLM page "Enable batch-invariant mixed decode and prefill for Qwen GDN",
+// section "How": cached rows always go through this packed recurrent decode,
+// alone or at the front of a mixed batch.
+//
+// The kernel is bound by HBM: each (row, value head) state S^T [d_v][d_k] fp32
+// (64 KiB at d = 128) is read once and written once; q, k, v, g, beta and o
+// add about 1.6 %.  Work is split into items of 16 state rows (8 KiB); a
+// persistent grid of warps walks the items with a grid stride, so each warp
+// keeps 16 KiB of float4 loads in flight per item and the grid fills every SM
+// regardless of the row count.  Arithmetic per state row is in row_update.cuh.
+#include "row_update.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kDecodeThreads = 256;
+constexpr int kRowsPerGroup = 4;  // rows of S^T per warp-wide access (lane octets)
+constexpr int kGroupsPerItem = 4;
+constexpr int kRowsPerItem = kRowsPerGroup * kGroupsPerItem;  // 16
+
+template <int D>
+__global__ void __launch_bounds__(kDecodeThreads)
+decode_kernel(const DecodeArgs a) {
+    constexpr int V4 = D / 32;                   // float4 per lane per row
+    constexpr int kItemsPerHead = D / kRowsPerItem;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane >> 3;
+    const int l8 = lane & 7;
+    const int64_t n_items = static_cast<int64_t>(a.num_rows) * a.h_v * kItemsPerHead;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int group = a.h_v / a.h_k;
+
+    for (int64_t it = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+         it < n_items; it += nwarps) {
+        const int blk = static_cast<int>(it % kItemsPerHead);
+        const int64_t rh = it / kItemsPerHead;
+        const int h = static_cast<int>(rh % a.h_v);
+        const int r = static_cast<int>(rh / a.h_v);
+        const int row0 = blk * kRowsPerItem;
+        uint16_t *orow = a.o + (static_cast<size_t>(r) * a.h_v + h) * D;
+
+        const int src = a.src_slot[r];
+        const int dst = a.dst_slot ? a.dst_slot[r] : src;
+        if (src < 0 || src >= a.num_slots || dst < 0 || dst >= a.num_slots) {
+            if (src >= 0) report(a.dev_status, GDN_DEV_BAD_SLOT);
+            if (lane < kRowsPerItem) orow[row0 + lane] = 0;
+            continue;
+        }
+        const float *sp = a.state + (static_cast<size_t>(src) * a.h_v + h) * D * D;
+        float *dp = a.state + (static_cast<size_t>(dst) * a.h_v + h) * D * D;
+
+        float4 s[kGroupsPerItem][V4];
+#pragma unroll
+        for (int i = 0; i < kGroupsPerItem; ++i) {
+            const int j = row0 + i * kRowsPerGroup + sub;
+#pragma unroll
+            for (int m = 0; m < V4; ++m)
+                s[i][m] = __ldcg(reinterpret_cast<const float4 *>(sp + static_cast<size_t>(j) * D +
+                                                                  4 * (l8 + 8 * m)));
+        }
+        const int kh = h / group;
+        float kk[V4 * 4], qq[V4 * 4];
+        load_bf16_slice<V4>(a.k + (static_cast<size_t>(r) * a.h_k + kh) * D, l8, kk);
+        load_bf16_slice<V4>(a.q + (static_cast<size_t>(r) * a.h_k + kh) * D, l8, qq);
+        const size_t gh = static_cast<size_t>(r) * a.h_v + h;
+        const float alpha = expf(a.g[gh]);
+        const float beta = a.beta[gh];
+        const float kq = octet_dot<V4>(kk, qq);
+        const uint16_t *vrow = a.v + gh * D;
+
+#pragma unroll
+        for (int i = 0; i < kGroupsPerItem; ++i) {
+            const int j = row0 + i * kRowsPerGroup + sub;
+            const float vj = bf16_bits_to_float(vrow[j]);
+            const float oj = update_row<V4>(s[i], kk, qq, alpha, beta, vj, kq, a.scale);
+#pragma unroll
+            for (int m = 0; m < V4; ++m)
+                __stcg(reinterpret_cast<float4 *>(dp + static_cast<size_t>(j) * D + 4 * (l8 + 8 * m)),
+                       s[i][m]);
+            if (l8 == 0) orow[j] = float_to_bf16_bits(oj);
+        }
+    }
+}
+
+template <int D>
+cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t stream) {
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D>, kDecodeThreads, 0);
+    if (e != cudaSuccess) return e;
+    const int64_t items = static_cast<int64_t>(a.num_rows) * a.h_v * (D / kRowsPerItem);
+    const int64_t need = (items + (kDecodeThreads / 32) - 1) / (kDecodeThreads / 32);
+    const int64_t cap = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
+    const int grid = static_cast<int>(need < cap ? need : cap);
+    decode_kernel<D><<<grid, kDecodeThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs &a, int d, cudaStream_t stream) {
+    if (a.num_rows == 0) return cudaSuccess;
+    return d == 128 ? launch_decode_d<128>(a, stream) : launch_decode_d<64>(a, stream);
+}
+
+}  // namespace gdn

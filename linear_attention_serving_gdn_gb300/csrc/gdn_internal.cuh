@@ -1,0 +1,68 @@
+// Internal declarations shared by the libgdn translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+
+namespace gdn {
+
+constexpr int kChunk = 64;  // prefill chunk grid, tokens
+
+struct DecodeArgs {
+    int32_t num_rows, h_k, h_v;
+    float scale;
+    const uint16_t *q, *k, *v;
+    const float *g, *beta;
+    float *state;
+    int64_t num_slots;
+    const int32_t *src_slot, *dst_slot;
+    uint16_t *o;
+    int32_t *dev_status;
+};
+
+struct PrefillArgs {
+    int32_t num_seqs, h_k, h_v;
+    float scale;
+    const int32_t *cu_seqlens;
+    const uint16_t *q, *k, *v;
+    const float *g, *beta;
+    float *state;
+    int64_t num_slots;
+    const int32_t *src_slot, *dst_slot;
+    uint16_t *o;
+    float *chunk_states;
+    int32_t emit_every_chunks;
+    int32_t *dev_status;
+};
+
+// Launchers (decode.cu, prefill.cu).  Arguments are validated by the caller.
+cudaError_t launch_decode(const DecodeArgs &a, int d, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillArgs &a, int d, int64_t total_tokens,
+                           int32_t max_seqlen, cudaStream_t stream);
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
+    __nv_bfloat16 h = __float2bfloat16_rn(f);
+    return *reinterpret_cast<uint16_t *>(&h);
+}
+
+// Sum over the 8 lanes of an aligned lane octet; every lane of the octet gets
+// the same bits (xor butterfly, each level adds two commuted partial sums).
+__device__ __forceinline__ float octet_sum(float x) {
+    x += __shfl_xor_sync(0xffffffffu, x, 4);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    return x;
+}
+
+__device__ __forceinline__ void report(int32_t *dev_status, int32_t bit) {
+    if (dev_status) atomicOr(dev_status, bit);
+}
+
+}  // namespace gdn

@@ -1,0 +1,73 @@
+// One recurrent step on rows of S^T, held in registers by lane octets.
+//
+// Layout: a row j of S^T (column j of S, d_k floats) is spread over the 8
+// lanes of an aligned lane octet; lane l8 holds the float4s at columns
+// 4*(l8 + 8*m), m = 0..V4-1, so one warp-wide float4 access touches 4 rows x
+// 128 contiguous bytes.  Per row j, with u the rank-one update of the gated
+// delta rule (Gated DeltaNet, Yang, Kautz, Hatamizadeh, ICLR 2025):
+//
+//     a_j  = sum_i S_ij k_i,   b_j = sum_i S_ij q_i
+//     u_j  = beta (v_j - alpha a_j)
+//     S'_ij = alpha S_ij + k_i u_j                  (= alpha S - beta k k^T(alpha S) + beta k v^T)
+//     o_j  = scale (alpha b_j + u_j (k . q))        (= scale (S'^T q)_j)
+//
+// Columns j are independent, so any set of rows can be processed by any warp
+// and the result of a row never depends on which other rows share the launch.
+#pragma once
+
+#include "gdn_internal.cuh"
+
+namespace gdn {
+
+template <int V4>
+__device__ __forceinline__ void load_bf16_slice(const uint16_t *p, int l8, float (&x)[V4 * 4]) {
+#pragma unroll
+    for (int m = 0; m < V4; ++m) {
+        const uint2 w = *reinterpret_cast<const uint2 *>(p + 4 * (l8 + 8 * m));
+        x[4 * m + 0] = __uint_as_float(w.x << 16);
+        x[4 * m + 1] = __uint_as_float(w.x & 0xffff0000u);
+        x[4 * m + 2] = __uint_as_float(w.y << 16);
+        x[4 * m + 3] = __uint_as_float(w.y & 0xffff0000u);
+    }
+}
+
+// k . q over the full head dim; identical bits on all lanes of the octet.
+template <int V4>
+__device__ __forceinline__ float octet_dot(const float (&kk)[V4 * 4], const float (&qq)[V4 * 4]) {
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < V4 * 4; ++e) acc = fmaf(kk[e], qq[e], acc);
+    return octet_sum(acc);
+}
+
+// Updates the lane's slice of one row in place and returns o_j.
+template <int V4>
+__device__ __forceinline__ float update_row(float4 (&s)[V4], const float (&kk)[V4 * 4],
+                                            const float (&qq)[V4 * 4], float alpha, float beta,
+                                            float vj, float kq, float scale) {
+    float a = 0.f, b = 0.f;
+#pragma unroll
+    for (int m = 0; m < V4; ++m) {
+        a = fmaf(s[m].x, kk[4 * m + 0], a);
+        b = fmaf(s[m].x, qq[4 * m + 0], b);
+        a = fmaf(s[m].y, kk[4 * m + 1], a);
+        b = fmaf(s[m].y, qq[4 * m + 1], b);
+        a = fmaf(s[m].z, kk[4 * m + 2], a);
+        b = fmaf(s[m].z, qq[4 * m + 2], b);
+        a = fmaf(s[m].w, kk[4 * m + 3], a);
+        b = fmaf(s[m].w, qq[4 * m + 3], b);
+    }
+    a = octet_sum(a);
+    b = octet_sum(b);
+    const float u = beta * (vj - alpha * a);
+#pragma unroll
+    for (int m = 0; m < V4; ++m) {
+        s[m].x = fmaf(kk[4 * m + 0], u, alpha * s[m].x);
+        s[m].y = fmaf(kk[4 * m + 1], u, alpha * s[m].y);
+        s[m].z = fmaf(kk[4 * m + 2], u, alpha * s[m].z);
+        s[m].w = fmaf(kk[4 * m + 3], u, alpha * s[m].w);
+    }
+    return scale * fmaf(u, kq, alpha * b);
+}
+
+}  // namespace gdn

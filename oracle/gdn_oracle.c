@@ -80,24 +80,22 @@ static void run_chain(int64_t tok0, int64_t n_tok, int head, int h_k, int h_v,
         const double alpha = exp((double)g[(size_t)tok * h_v + head]);
         const double b = (double)beta[(size_t)tok * h_v + head];
 
-        /* ka_j = sum_i k_i (alpha S_ij) */
-        for (int j = 0; j < d_v; ++j) {
-            double acc = 0.0;
-            for (int i = 0; i < d_k; ++i) acc += kt[i] * (alpha * s[(size_t)i * d_v + j]);
-            ka[j] = acc;
-        }
+        /* ka_j = sum_i k_i (alpha S_ij), summed over i in ascending order */
+        for (int j = 0; j < d_v; ++j) ka[j] = 0.0;
+        for (int i = 0; i < d_k; ++i)
+            for (int j = 0; j < d_v; ++j) ka[j] += kt[i] * (alpha * s[(size_t)i * d_v + j]);
         /* S_ij <- alpha S_ij - beta k_i ka_j + beta k_i v_j */
         for (int i = 0; i < d_k; ++i)
             for (int j = 0; j < d_v; ++j) {
                 double *sij = &s[(size_t)i * d_v + j];
                 *sij = alpha * *sij - b * kt[i] * ka[j] + b * kt[i] * vt[j];
             }
-        /* o_j = scale * sum_i S_ij q_i */
-        for (int j = 0; j < d_v; ++j) {
-            double acc = 0.0;
-            for (int i = 0; i < d_k; ++i) acc += s[(size_t)i * d_v + j] * qt[i];
-            o[(size_t)t * d_v + j] = scale * acc;
-        }
+        /* o_j = scale * sum_i S_ij q_i, summed over i in ascending order */
+        double *ot = o + (size_t)t * d_v;
+        for (int j = 0; j < d_v; ++j) ot[j] = 0.0;
+        for (int i = 0; i < d_k; ++i)
+            for (int j = 0; j < d_v; ++j) ot[j] += s[(size_t)i * d_v + j] * qt[i];
+        for (int j = 0; j < d_v; ++j) ot[j] *= scale;
         if (emit_every > 0 && (t + 1) % emit_every == 0) {
             memcpy(emits + (size_t)((t + 1) / emit_every - 1) * d_k * d_v, s,
                    sizeof(double) * (size_t)d_k * d_v);

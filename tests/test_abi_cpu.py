@@ -1,0 +1,127 @@
+"""The C-ABI library loads, exports every symbol include/gdn.h declares, and
+rejects bad arguments on the host before any CUDA call.  No GPU needed: every
+call here either is a host-only helper or fails validation."""
+import ctypes
+import json
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    from linear_attention_serving_gdn_gb300 import _build
+    _build.build()
+    import linear_attention_serving_gdn_gb300 as gdn
+    return gdn.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_three_entry_points():
+    names = declared_functions()
+    for n in ("gdn_prefill_varlen", "gdn_decode_packed", "gdn_mixed_step"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import linear_attention_serving_gdn_gb300 as gdn
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in gdn.h but not exported"
+    assert set(declared_functions()) == set(gdn.EXPORTED_SYMBOLS)
+
+
+def test_prefix_grid_helpers_match_the_page(lib):
+    import linear_attention_serving_gdn_gb300 as gdn
+    ex = json.load(open(os.path.join(ROOT, "tests", "golden", "prefix_grid.json")))
+    assert gdn.gdn_align_block_size(ex["block_size_in"]) == ex["block_size_aligned"]
+    assert gdn.gdn_grid_emit_every_chunks(ex["block_size_in"]) == ex["grid"] // ex["chunk"]
+    for h in ex["hits"]:
+        assert gdn.gdn_floor_prefix_hit(h["hit"], h["prompt"], ex["block_size_in"]) == h["floored"]
+    assert gdn.gdn_floor_prefix_hit(2000, 2000, 1056) == 2000
+    assert gdn.gdn_align_block_size(0) == -1
+    assert gdn.gdn_floor_prefix_hit(5, 4, 1056) == -1
+
+
+def test_emit_counts_and_offsets(lib):
+    import linear_attention_serving_gdn_gb300 as gdn
+    cu = [0, 1088, 1088 + 2175, 1088 + 2175 + 32768, 1088 + 2175 + 32768 + 5]
+    assert gdn.gdn_prefill_num_emits(cu, 17) == 1 + 1 + 30 + 0
+    assert gdn.gdn_prefill_emit_offsets(cu, 17) == [0, 1, 2, 32, 32]
+    assert gdn.gdn_prefill_num_emits(cu, 1) == 17 + 33 + 512 + 0
+    assert gdn.gdn_prefill_num_emits(cu, 0) == 0
+    with pytest.raises(ValueError):
+        gdn.gdn_prefill_num_emits([0, 5, 3], 1)
+
+
+def _Dims(*a):
+    from linear_attention_serving_gdn_gb300 import Dims
+    return Dims(*a)
+
+
+FAKE = ctypes.c_void_p(0x10000)   # aligned, never dereferenced: validation fails first
+
+
+def _decode(lib, dims, rows=4, q=FAKE, src=FAKE, state=FAKE):
+    return lib.gdn_decode_packed(ctypes.byref(dims), rows, q, FAKE, FAKE, FAKE, FAKE, state, 8,
+                                 src, None, FAKE, None, None)
+
+
+def test_decode_rejects_bad_arguments_on_the_host(lib):
+    ok = _Dims(16, 16, 128, 128, 1.0)
+    assert _decode(lib, _Dims(16, 16, 96, 96, 1.0)) == 2          # unsupported head dim
+    assert _decode(lib, _Dims(16, 16, 128, 64, 1.0)) == 2         # d_k != d_v
+    assert _decode(lib, _Dims(16, 24, 128, 128, 1.0)) == 1        # h_v % h_k != 0
+    assert _decode(lib, ok, rows=-1) == 1
+    assert _decode(lib, ok, q=None) == 1
+    assert _decode(lib, ok, src=None) == 1
+    assert _decode(lib, ok, state=ctypes.c_void_p(0x10004)) == 1   # misaligned
+    assert lib.gdn_decode_packed(None, 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, FAKE, None, FAKE,
+                                 None, None) == 1
+    assert _decode(lib, ok, rows=0) == 0                           # empty: no-op
+
+
+def _prefill(lib, cu_host, n, E=0, cap=0, cs=None, dims=None):
+    dims = dims or _Dims(16, 32, 128, 128, 1.0)
+    arr = (ctypes.c_int32 * len(cu_host))(*cu_host)
+    return lib.gdn_prefill_varlen(ctypes.byref(dims), n, FAKE, arr, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                  FAKE, 8, None, None, FAKE, cs, E, cap, None, None)
+
+
+def test_prefill_rejects_bad_arguments_on_the_host(lib):
+    assert _prefill(lib, [0, 10, 5], 2) == 1                       # non-monotone
+    assert _prefill(lib, [3, 10], 1) == 1                          # does not start at 0
+    assert _prefill(lib, [0, 2000], 1, E=1, cap=30, cs=FAKE) == 1  # 31 emits needed
+    assert _prefill(lib, [0, 2000], 1, E=1, cap=31, cs=None) == 1  # stream missing
+    assert _prefill(lib, [0, 2000], 1, E=-1) == 1
+    assert _prefill(lib, [0, 10], 1, dims=_Dims(16, 32, 256, 256, 1.0)) == 2
+    assert _prefill(lib, [0], 0) == 0                              # no sequences: no-op
+
+
+def test_mixed_step_rejects_bad_arguments_on_the_host(lib):
+    dims = _Dims(16, 16, 128, 128, 1.0)
+    bad = (ctypes.c_int32 * 3)(0, 7, 2)
+    assert lib.gdn_mixed_step(ctypes.byref(dims), 4, 2, FAKE, bad, FAKE, FAKE, FAKE, FAKE, FAKE,
+                              FAKE, 8, FAKE, None, None, None, FAKE, None, 0, 0, None, None) == 1
+    good = (ctypes.c_int32 * 2)(0, 7)
+    assert lib.gdn_mixed_step(ctypes.byref(dims), -1, 1, FAKE, good, FAKE, FAKE, FAKE, FAKE, FAKE,
+                              FAKE, 8, FAKE, None, None, None, FAKE, None, 0, 0, None, None) == 1
+    assert lib.gdn_mixed_step(ctypes.byref(dims), 4, 1, FAKE, good, FAKE, FAKE, FAKE, FAKE, FAKE,
+                              FAKE, 8, None, None, None, None, FAKE, None, 0, 0, None, None) == 1
+
+
+def test_status_strings(lib):
+    import linear_attention_serving_gdn_gb300 as gdn
+    assert gdn.gdn_status_string(0) == "GDN_OK"
+    assert "invalid" in gdn.gdn_status_string(1)

@@ -18,9 +18,9 @@ from tests import test_oracle_pins as pins
 
 MUTATIONS = {
     "sign_of_erase_term": ("*sij = alpha * *sij - b * kt[i] * ka[j]", "*sij = alpha * *sij + b * kt[i] * ka[j]"),
-    "decay_dropped_in_erase": ("acc += kt[i] * (alpha * s[(size_t)i * d_v + j]);", "acc += kt[i] * s[(size_t)i * d_v + j];"),
-    "state_transposed_in_erase": ("acc += kt[i] * (alpha * s[(size_t)i * d_v + j]);", "acc += kt[i] * (alpha * s[(size_t)j * d_v + i]);"),
-    "key_used_as_query": ("acc += s[(size_t)i * d_v + j] * qt[i];", "acc += s[(size_t)i * d_v + j] * kt[i];"),
+    "decay_dropped_in_erase": ("ka[j] += kt[i] * (alpha * s[(size_t)i * d_v + j]);", "ka[j] += kt[i] * s[(size_t)i * d_v + j];"),
+    "state_transposed_in_erase": ("ka[j] += kt[i] * (alpha * s[(size_t)i * d_v + j]);", "ka[j] += kt[i] * (alpha * s[(size_t)j * d_v + i]);"),
+    "key_used_as_query": ("ot[j] += s[(size_t)i * d_v + j] * qt[i];", "ot[j] += s[(size_t)i * d_v + j] * kt[i];"),
     "value_term_dropped": (" + b * kt[i] * vt[j];", ";"),
     "gva_mapping_modulo": ("const int kh = head / (h_v / h_k);", "const int kh = head % h_k;"),
     "first_emission_skipped": ("(t + 1) % emit_every == 0", "(t + 1) % emit_every == 0 && t + 1 > emit_every"),
