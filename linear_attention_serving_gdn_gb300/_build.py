@@ -17,7 +17,9 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-OUT_DIR = os.path.join(HERE, "_lib")
+# GDN_LIB_DIR / GDN_NVCC_EXTRA: alternative output directory and extra nvcc
+# flags (e.g. -DGDN_DEBUG_CHECKS for a self-checking build).
+OUT_DIR = os.environ.get("GDN_LIB_DIR") or os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libgdn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -53,6 +55,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
     cc = nvcc()
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I", INCLUDE, "--expt-relaxed-constexpr"]
+    common += os.environ.get("GDN_NVCC_EXTRA", "").split()
     if ptxas_verbose:
         common += ["-Xptxas", "-v"]
 

@@ -116,6 +116,8 @@ gdn_status_t prefill_impl(const gdn_dims_t *dims, int32_t num_seqs, const int32_
     a.chunk_states = E > 0 ? chunk_states : nullptr;
     a.emit_every_chunks = E;
     a.dev_status = dev_status;
+    a.total_tokens = T;
+    a.chunk_capacity = E > 0 ? capacity : 0;
     return gdn::launch_prefill(a, dims->d_k, T, max_len, stream) == cudaSuccess ? GDN_OK
                                                                                   : GDN_ERR_CUDA;
 }

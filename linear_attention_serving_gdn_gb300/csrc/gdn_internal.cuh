@@ -36,6 +36,8 @@ struct PrefillArgs {
     float *chunk_states;
     int32_t emit_every_chunks;
     int32_t *dev_status;
+    int64_t total_tokens;    // rows of q, k, v, g, beta, o
+    int64_t chunk_capacity;  // entries of chunk_states
 };
 
 // Launchers (decode.cu, prefill.cu).  Arguments are validated by the caller.
@@ -64,5 +66,26 @@ __device__ __forceinline__ float octet_sum(float x) {
 __device__ __forceinline__ void report(int32_t *dev_status, int32_t bit) {
     if (dev_status) atomicOr(dev_status, bit);
 }
+
+// Self-checks for debugging builds (-DGDN_DEBUG_CHECKS): a failed check
+// records (site, value) of the first failure in dev_status[1..3], sets bit
+// 0x100 of dev_status[0], and the guarded access is skipped.  In normal
+// builds the guard is the constant true.
+#ifdef GDN_DEBUG_CHECKS
+__device__ __forceinline__ bool debug_guard(bool ok, int32_t *st, int site, long long val) {
+    if (!ok && st) {
+        if (atomicCAS(st + 1, 0, site) == 0) {
+            st[2] = static_cast<int32_t>(val);
+            st[3] = static_cast<int32_t>(val >> 32);
+        }
+        atomicOr(st, 0x100);
+        __threadfence_system();
+    }
+    return ok;
+}
+#define GDN_GUARD(st, cond, site, val) ::gdn::debug_guard((cond), (st), (site), static_cast<long long>(val))
+#else
+#define GDN_GUARD(st, cond, site, val) true
+#endif
 
 }  // namespace gdn
