@@ -296,6 +296,51 @@ def mixed_case(torch, gdn, dev, reps):
             "tokens_per_s": (nd + pre.total_tokens) / (ms * 1e-3)}
 
 
+def run_extra(torch, gdn, dev, wanted, peaks):
+    extra = []
+    if "prefill" in wanted:
+        extra.append(prefill_case(torch, gdn, gi.prefill_qwen3next_gva(0), dev, reps=5))
+    if "prefix" in wanted:
+        extra.append(prefill_case(torch, gdn, gi.prefix_cache_prefill(0), dev, reps=3, E=17))
+    if "mixed" in wanted:
+        extra.append(mixed_case(torch, gdn, dev, reps=5))
+    for x in extra:
+        if "algorithmic_tflops" in x:
+            x["roofline"] = {"bound": "tensor", "kernel": "prefill_chunk_tc_kernel<128>",
+                             "achieved": x["algorithmic_tflops"], "peak": peaks["bf16_tflops"],
+                             "unit": "TFLOP/s", "frac": x["algorithmic_tflops"] / peaks["bf16_tflops"],
+                             "traffic": measured_traffic("prefill_chunk_tc_kernel<128>", x["workload"]),
+                             "peak_source": peaks["source"] + " (dense bf16 burst; fp16 runs at the same rate)"}
+    return extra
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the CUDA sources a kernel is built from (to tie ncu counters to it)."""
+    import hashlib
+    csrc = os.path.join(ROOT, "linear_attention_serving_gdn_gb300", "csrc")
+    files = {"decode_kernel<128>": ["decode.cu", "row_update.cuh", "gdn_internal.cuh"],
+             "prefill_chunk_tc_kernel<128>": ["prefill.cu", "tc_ptx.cuh", "gdn_internal.cuh"]}[kernel]
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str = "decode_r256_h16_d128"):
+    """DRAM bytes per launch (read + write) from the committed ncu summary,
+    or None when the kernel's sources changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "ncu_dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        rec = json.load(open(p)).get(kernel, {}).get(workload)
+    except (ValueError, AttributeError):
+        return None
+    if not rec or rec.get("source_hash") != kernel_source_hash(kernel):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline and reference arm)
 # ---------------------------------------------------------------------------
@@ -365,6 +410,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the prefill/mixed workloads")
+    ap.add_argument("--workloads", default="decode,prefill,prefix,mixed",
+                    help="comma list of decode (headline), prefill, prefix, mixed")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -385,6 +432,14 @@ def main():
     import linear_attention_serving_gdn_gb300 as gdn
     peaks = load_peaks()
 
+    wanted = set(args.workloads.split(","))
+    if args.no_extra:
+        wanted &= {"decode"}
+    if "decode" not in wanted:
+        extra = run_extra(torch, gdn, dev, wanted, load_peaks())
+        if rank == 0:
+            print(json.dumps({"metric": "GDN prefill tokens/s", "workloads": extra}), flush=True)
+        return
     wl, t = decode_setup(torch, seed=rank, dev=dev)
     with Clocks(torch.cuda.current_device()) as clk:
         total_ms, per_launch = time_decode(torch, gdn, t, args.steps, args.warmup, world)
@@ -409,22 +464,16 @@ def main():
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": "decode_kernel<128>", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": None, "peak_source": peaks["source"] + " (burst copy)",
+                     "traffic": measured_traffic("decode_kernel<128>"),
+                     "peak_source": peaks["source"] + " (burst copy)",
                      "bytes_per_launch": bytes_per_launch, "launch_ms": launch_ms},
         "e2e": {"value": rows_total / (e2e_ms * 1e-3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
-    if not args.no_extra:
-        extra = []
-        extra.append(prefill_case(torch, gdn, gi.prefill_qwen3next_gva(0), dev, reps=5))
-        extra.append(prefill_case(torch, gdn, gi.prefix_cache_prefill(0), dev, reps=3, E=17))
-        extra.append(mixed_case(torch, gdn, dev, reps=5))
-        for x in extra:
-            if "algorithmic_tflops" in x:
-                x["tensor_frac_of_bf16_peak"] = x["algorithmic_tflops"] / peaks["bf16_tflops"]
-        line["workloads"] = extra
+    if wanted - {"decode"}:
+        line["workloads"] = run_extra(torch, gdn, dev, wanted, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
