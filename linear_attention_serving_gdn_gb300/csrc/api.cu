@@ -94,9 +94,6 @@ gdn_status_t prefill_impl(const gdn_dims_t *dims, int32_t num_seqs, const int32_
         if (need > 0 && (!chunk_states || capacity < need)) return GDN_ERR_INVALID_ARG;
     }
     if (static_cast<int64_t>(num_seqs) * dims->h_v > INT_MAX) return GDN_ERR_UNSUPPORTED;
-    int32_t max_len = 0;
-    for (int32_t i = 0; i < num_seqs; ++i)
-        if (cu_host[i + 1] - cu_host[i] > max_len) max_len = cu_host[i + 1] - cu_host[i];
     gdn::PrefillArgs a;
     a.num_seqs = num_seqs;
     a.h_k = dims->h_k;
@@ -118,8 +115,7 @@ gdn_status_t prefill_impl(const gdn_dims_t *dims, int32_t num_seqs, const int32_
     a.dev_status = dev_status;
     a.total_tokens = T;
     a.chunk_capacity = E > 0 ? capacity : 0;
-    return gdn::launch_prefill(a, dims->d_k, T, max_len, stream) == cudaSuccess ? GDN_OK
-                                                                                  : GDN_ERR_CUDA;
+    return gdn::launch_prefill(a, dims->d_k, cu_host, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 }  // namespace

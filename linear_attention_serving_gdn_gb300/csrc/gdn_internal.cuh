@@ -42,8 +42,8 @@ struct PrefillArgs {
 
 // Launchers (decode.cu, prefill.cu).  Arguments are validated by the caller.
 cudaError_t launch_decode(const DecodeArgs &a, int d, cudaStream_t stream);
-cudaError_t launch_prefill(const PrefillArgs &a, int d, int64_t total_tokens,
-                           int32_t max_seqlen, cudaStream_t stream);
+// cu_host: host mirror of a.cu_seqlens (sizes the launch and orders the chains).
+cudaError_t launch_prefill(const PrefillArgs &a, int d, const int32_t *cu_host, cudaStream_t stream);
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
     return __uint_as_float(static_cast<uint32_t>(b) << 16);

@@ -20,20 +20,29 @@
 //     O     = scale [diag(gamma) Q S0 + P U],  P_ts = exp(G_t - G_s) q_t.k_s (s <= t)
 //     S_C   = gamma_C S0 + Ktil^T U,           Ktil_t = exp(G_C - G_t) k_t
 //
-// Everything is computed transposed so that TMEM lane j is value column j:
-//     D1 = S0^T [Q;K]^T   (M = d_v, N = 128 tokens, K = d_k)
-//     D3 = V'^T (T'')^T   (T'' = T diag(beta); M = d_v, N = 64, K = 64)
+// Products are computed transposed so that TMEM lane j is value column j:
+//     D1 = S0^T [Q;K]^T  (M = d_v, N = 128 tokens, K = d_k), double-buffered
+//     D3 = V'^T T''^T    (T'' = T diag(beta); reuses the K half of D1)
 //     D5 = gamma_C S0^T + U^T Ktil     (the fp32 state, accumulated in TMEM)
 //     D6 = U^T P^T
-// and the Gram [Q;K] K^T (M = 128 tokens, N = 64, K = d_k) sits in its own
-// TMEM columns.  Every tensor-core operand is fp16 (inputs convert exactly
-// from bf16 except below 2^-14), accumulation and the state carry are fp32.
+// and the Gram [Q;K] K^T (M = 128 tokens, N = 64, K = d_k).  Operands are
+// fp16 (inputs convert exactly from bf16 except below 2^-14); accumulation
+// and the state carry are fp32.
 //
-// One CTA (4 warps; thread j owns TMEM lane j) runs one (sequence, value
-// head) chain through its chunks in order.  A chunk's arithmetic depends only
-// on its own inputs and the fp32 state entering it, so results do not depend
-// on the batch, and restarting from an emitted state reproduces the
-// uninterrupted run bit for bit.
+// One CTA runs one (sequence, value head) chain, warp-specialised:
+//   chain group (warps 0-3, thread j owns TMEM lane j): the steps that
+//     depend on the state, S1 -> V' -> S3 -> U -> S5/S6 -> new state, plus
+//     the output of the previous chunk while S1 runs;
+//   prep group (warps 4-7): the chunk-local operands of the next chunk
+//     (fp16 Q/K tiles, decays, Gram, P, A, T = (I + A)^-1, T'') into a
+//     double-buffered stage, handed over through mbarriers.
+// A chunk's arithmetic depends only on its own inputs and the fp32 state
+// entering it, so results do not depend on the batch, and restarting from an
+// emitted state reproduces the uninterrupted run bit for bit.
+//
+// Every shared-memory index that depends on the thread index is masked to
+// its array's range, so no address can leave the allocation even for a
+// thread outside the branch that guards it.
 #include <cuda_fp16.h>
 
 #include "gdn_internal.cuh"
@@ -42,46 +51,63 @@
 namespace gdn {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kAS = 65;  // fp32 row stride of the 64x64 scratch matrices
-// Upper bound on the wait for one group of MMAs, in SM clock cycles (~1 s):
-// a wait that runs out reports GDN_DEV_TIMEOUT instead of hanging.
+constexpr int kThreads = 256;  // chain group + prep group
+constexpr int kGroup = 128;
+constexpr int kBarChain = 1;   // named barrier ids (0 is __syncthreads)
+constexpr int kBarPrep = 2;
+// Upper bound on every wait, in SM clock cycles (~1 s): a wait that runs out
+// reports GDN_DEV_TIMEOUT instead of hanging.
 constexpr long long kWaitCycles = 2000000000LL;
+constexpr int kMaxOrder = 2048;
+
+struct PrefillLaunch {
+    PrefillArgs a;
+    int32_t n_order;
+    int32_t order[kMaxOrder];  // launch rank -> sequence, longest first
+};
 
 template <int D>
 struct Smem {
     // Tensor-core operand tiles (K-major, 128-byte swizzle, 1024-aligned).
-    static constexpr uint32_t kQK = 0;                        // fp16 [128 rows: q then k][D]
-    static constexpr uint32_t kS0T = kQK + 128 * D * 2;       // fp16 [128 rows j][D]  (S0^T)
-    static constexpr uint32_t kVpT = kS0T + 128 * D * 2;      // fp16 [128 rows j][64] (V'^T); O staging
-    static constexpr uint32_t kUT = kVpT + 128 * 64 * 2;      // fp16 [128 rows j][64] (U^T)
-    static constexpr uint32_t kTpp = kUT + 128 * 64 * 2;      // fp16 [64 rows t][64]  (T diag(beta))
-    static constexpr uint32_t kP = kTpp + 64 * 64 * 2;        // fp16 [64 rows t][64]  (P)
-    static constexpr uint32_t kKtT = kP + 64 * 64 * 2;        // fp16 [D rows i][64]   (Ktil^T)
+    static constexpr uint32_t kQKBytes = 128 * D * 2;          // fp16 [128 rows: q then k][D]
+    static constexpr uint32_t kQK0 = 0;
+    static constexpr uint32_t kQK1 = kQK0 + kQKBytes;
+    static constexpr uint32_t kTpp0 = kQK1 + kQKBytes;         // fp16 [64 rows t][64]  T''
+    static constexpr uint32_t kTpp1 = kTpp0 + 8192;
+    static constexpr uint32_t kP0 = kTpp1 + 8192;              // fp16 [64 rows t][64]  P
+    static constexpr uint32_t kP1 = kP0 + 8192;
+    static constexpr uint32_t kKtT0 = kP1 + 8192;              // fp16 [D rows i][64]   Ktil^T
+    static constexpr uint32_t kKtT1 = kKtT0 + D * 128;
+    static constexpr uint32_t kS0T = kKtT1 + D * 128;          // fp16 [128 rows j][D]  S0^T
+    static constexpr uint32_t kVpT = kS0T + 128 * D * 2;       // fp16 [128 rows j][64] V'^T
+    static constexpr uint32_t kUT = kVpT + 16384;              // fp16 [128 rows j][64] U^T
     // Plain buffers.
-    static constexpr uint32_t kV = kKtT + D * 64 * 2;         // bf16 [64][D] values of the chunk
-    static constexpr uint32_t kA = kV + 64 * D * 2;           // fp32 [64][kAS] strictly lower A
-    static constexpr uint32_t kT = kA + 64 * kAS * 4;         // fp32 [64][kAS] T = (I + A)^-1
-    static constexpr uint32_t kW = kT + 64 * kAS * 4;         // fp32 [3][16][16] inverse scratch
-    static constexpr uint32_t kG = kW + 3 * 256 * 4;          // fp32 [64] cumulative log decay
-    static constexpr uint32_t kGam = kG + 64 * 4;             // fp32 [64] exp(G_t)
-    static constexpr uint32_t kDec = kGam + 64 * 4;           // fp32 [64] exp(G_C - G_t)
-    static constexpr uint32_t kBeta = kDec + 64 * 4;          // fp32 [64]
-    static constexpr uint32_t kGraw = kBeta + 64 * 4;         // fp32 [64] g of the chunk
-    static constexpr uint32_t kBar = kGraw + 64 * 4;          // mbarrier (8 B)
-    static constexpr uint32_t kTmem = kBar + 8;               // TMEM base address (4 B)
-    static constexpr uint32_t kFlag = kTmem + 4;              // int (4 B)
-    static constexpr uint32_t kEoff = kFlag + 4;              // long long [4] block reduction
-    static constexpr uint32_t kBytes = kEoff + 32;
-    static constexpr uint32_t kAlloc = kBytes + 1024;         // + alignment slack
+    static constexpr uint32_t kGam0 = kUT + 16384;             // f32 [64] exp(G_t), stage 0
+    static constexpr uint32_t kGam1 = kGam0 + 256;
+    static constexpr uint32_t kGamC = kGam1 + 256;             // f32 [2][64] chain group's copies
+    static constexpr uint32_t kM = kGamC + 512;                // f32 [64][64] A, then T (rotated rows)
+    static constexpr uint32_t kW = kM + 16384;                 // f32 [3][16][16] block products
+    static constexpr uint32_t kG = kW + 3072;                  // f32 [64] cumulative log decay
+    static constexpr uint32_t kBeta = kG + 256;                // f32 [64]
+    static constexpr uint32_t kGraw = kBeta + 256;             // f32 [64]
+    static constexpr uint32_t kDec = kGraw + 256;              // f32 [64] exp(G_C - G_t)
+    static constexpr uint32_t kBars = kDec + 256;              // 6 mbarriers
+    static constexpr uint32_t kTmem = kBars + 48;              // TMEM base address
+    static constexpr uint32_t kFail = kTmem + 4;               // int
+    static constexpr uint32_t kEoff = kFail + 4;               // long long [8]
+    static constexpr uint32_t kBytes = kEoff + 64;
+    static constexpr uint32_t kAlloc = kBytes + 1024;          // + alignment slack
+    static_assert(kS0T % 1024 == 0 && kVpT % 1024 == 0 && kUT % 1024 == 0 && kKtT0 % 1024 == 0, "");
+    static_assert(kKtT1 % 1024 == 0 && kBars % 8 == 0, "");
+    static_assert(kTpp0 % 1024 == 0 && kP0 % 1024 == 0 && kQK1 % 1024 == 0, "");
+    static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
-// TMEM column map (512 columns allocated; lane j = value column j).
-constexpr uint32_t kColD1 = 0;     // [0,64): (Q S0)^T, [64,128): (K S0)^T
-constexpr uint32_t kColD3 = 128;   // U^T (fp32)
-constexpr uint32_t kColD6 = 192;   // (P U)^T
-constexpr uint32_t kColD5 = 256;   // S^T state, D columns
-constexpr uint32_t kColGram = 384; // lanes 0..63: Q K^T rows, 64..127: K K^T rows
+// TMEM column map (512 columns; lane j = value column j).
+constexpr uint32_t kColD1 = 0;      // two buffers of 128: [0,64) (Q S0)^T, [64,128) (K S0)^T then U^T
+constexpr uint32_t kColD5 = 256;    // S^T state, D columns
+constexpr uint32_t kColD6 = 384;    // (P U)^T
+constexpr uint32_t kColGram = 448;  // lanes 0..63: Q K^T rows, 64..127: K K^T rows
 constexpr uint32_t kTmemCols = 512;
 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
@@ -103,11 +129,8 @@ __device__ __forceinline__ float half_bits_to_float(uint16_t h) {
     return __half2float(*reinterpret_cast<__half *>(&h));
 }
 
-// Writes 64 fp32 values (scaled) as one fp16 row of a 64-wide K-major tile.
-__device__ __forceinline__ void store_row64_f16(uint8_t *tile, uint32_t rows, uint32_t r, const float *x,
-                                                int32_t *st = nullptr) {
-    (void)st;
-    if (!GDN_GUARD(st, r < rows && tc::sw128_chunk_offset(r, 7, rows) + 16 <= rows * 128u, 31, r)) return;
+// Writes 64 fp32 values as one fp16 row r (< rows) of a 64-wide K-major tile.
+__device__ __forceinline__ void store_row64_f16(uint8_t *tile, uint32_t rows, uint32_t r, const float *x) {
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
         uint4 v;
@@ -134,20 +157,12 @@ __device__ __forceinline__ void store_f16_chunks32(uint8_t *tile, uint32_t r, in
 }
 
 __device__ __forceinline__ uint32_t lane_addr(uint32_t tbase, int warp, uint32_t col) {
-    return tbase + (static_cast<uint32_t>(warp * 32) << 16) + col;
+    return tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + col;
 }
 
-// Loads `n` (multiple of 32) consecutive fp32 TMEM columns of this thread's lane.
 template <int N>
 __device__ __forceinline__ void tmem_load_row(uint32_t taddr, float (&x)[N]) {
     static_assert(N % 32 == 0, "");
-#ifdef GDN_DEBUG_CHECKS
-    if ((taddr & 0xffffu) + N > kTmemCols) {
-#pragma unroll
-        for (int i = 0; i < N; ++i) x[i] = 0.f;
-        return;
-    }
-#endif
 #pragma unroll
     for (int c = 0; c < N; c += 32) {
         uint32_t r[32];
@@ -156,6 +171,41 @@ __device__ __forceinline__ void tmem_load_row(uint32_t taddr, float (&x)[N]) {
         for (int i = 0; i < 32; ++i) x[c + i] = __uint_as_float(r[i]);
     }
 }
+
+// Group barrier (named barrier over the group's 128 threads).
+__device__ __forceinline__ void group_sync(int id) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(kGroup) : "memory");
+}
+
+// Group barrier that returns true if any thread of the group passed `pred`.
+__device__ __forceinline__ bool group_any(int id, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(kGroup)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
+
+// Bounded wait for the phase of `bar` with the given parity.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    const long long start = clock64();
+    while (!tc::mbar_try_wait(bar, parity))
+        if (clock64() - start > kWaitCycles) return false;
+    return true;
+}
+
+// Rotated row layout of the 64x64 fp32 scratch: conflict-free for row and
+// column walks.
+__device__ __forceinline__ int midx(int r, int c) { return r * 64 + ((c + r) & 63); }
 
 // Sum over s' < s of floor(L_s' / (64 E)), by the whole block.
 __device__ int64_t emit_offset(const int32_t *cu, int s, int E, long long *part) {
@@ -172,73 +222,111 @@ __device__ int64_t emit_offset(const int32_t *cu, int s, int E, long long *part)
     return tot;
 }
 
-// T = (I + A)^-1 for a 64x64 strictly lower-triangular A (fp32, row stride
-// kAS): the four 16x16 diagonal blocks by column forward substitution, then
-// the block diagonals below, T_ab = -T_aa sum_{b<=m<a} A_am T_mb.  Only the
-// lower block triangle of T is written.
-__device__ void invert_unit_lower_64(const float *A, float *T, float *W, int tid) {
-    if (tid < 64) {
-        // Indices are masked so that every address stays inside the 64x64
-        // matrices for any thread, whatever the compiler does with the branch.
-        const int b = (tid >> 4) & 3, c = tid & 15, base = b * 16;
-        float x[16];
+// In place, M := (I + M)^-1 for a 64x64 strictly lower-triangular M (the
+// diagonal of M is ignored and the result has unit diagonal), in two parts
+// run by the prep group (p = thread index within the group, 0..127).
+//
+// Part 1 (threads p < 64, block b = p / 16, column c = p % 16): the four
+// 16x16 diagonal blocks by right-looking forward substitution; each step
+// finishes x_j and updates the later rows independently of each other.
+// The new columns are kept in x[] and written by invert_diag_store after a
+// group barrier, once every thread has read the block's A entries.
+__device__ __forceinline__ void invert_diag_solve(const float *M, int p, float (&x)[16]) {
+    const int c = p & 15, base = ((p >> 4) & 3) * 16;
+    float acc[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = (i == c) ? 1.f : 0.f;
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
 #pragma unroll
-        for (int i = 1; i < 16; ++i) {
-            float acc = 0.f;
+    for (int j = 0; j < 16; ++j) {
+        const float xj = (j < c) ? 0.f : (j == c ? 1.f : -acc[j]);
+        x[j] = xj;
 #pragma unroll
-            for (int j = 0; j < i; ++j) acc = fmaf(A[(base + i) * kAS + base + j], x[j], acc);
-            if (i > c) x[i] = -acc;
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) T[(base + i) * kAS + base + c] = x[i];
+        for (int i = j + 1; i < 16; ++i) acc[i] = fmaf(M[midx(base + i, base + j)], xj, acc[i]);
     }
-    __syncthreads();
-    for (int lev = 1; lev < 4; ++lev) {
-        const int nblk = 4 - lev;
-        for (int e = tid; e < nblk * 256; e += kThreads) {
-            const int b = e >> 8, i = (e >> 4) & 15, c = e & 15, a = b + lev;
-            float acc = 0.f;
-            for (int m = b; m < a; ++m)
+}
+
+__device__ __forceinline__ void invert_diag_store(float *M, int p, const float (&x)[16]) {
+    const int c = p & 15, base = ((p >> 4) & 3) * 16;
 #pragma unroll
-                for (int kk = 0; kk < 16; ++kk)
-                    acc = fmaf(A[(a * 16 + i) * kAS + m * 16 + kk], T[(m * 16 + kk) * kAS + b * 16 + c], acc);
-            W[b * 256 + i * 16 + c] = acc;
-        }
-        __syncthreads();
-        for (int e = tid; e < nblk * 256; e += kThreads) {
-            const int b = e >> 8, i = (e >> 4) & 15, c = e & 15, a = b + lev;
-            float acc = 0.f;
+    for (int i = 0; i < 16; ++i) M[midx(base + i, base + c)] = x[i];
+}
+
+// Part 2 (all 128 threads): block rows a = 1..3, T_ab = -T_aa sum_{b<=m<a}
+// A_am T_mb for every b < a.  Thread p owns row i = p / 8 of the blocks and
+// columns c0 = p % 8 and c0 + 8, for all b at once (independent
+// accumulators).  A_ab is overwritten only after the block row's products.
+template <int A_ROW>
+__device__ __forceinline__ void invert_block_row(float *M, float *W, int p) {
+    const int i = (p >> 3) & 15, c0 = p & 7;
+    const int row = A_ROW * 16 + i;
+    float acc[A_ROW][2];
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk)
-                acc = fmaf(T[(a * 16 + i) * kAS + a * 16 + kk], W[b * 256 + kk * 16 + c], acc);
-            T[(a * 16 + i) * kAS + b * 16 + c] = -acc;
+    for (int b = 0; b < A_ROW; ++b) acc[b][0] = acc[b][1] = 0.f;
+#pragma unroll
+    for (int m = 0; m < A_ROW; ++m) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float av = M[midx(row, m * 16 + k)];
+#pragma unroll
+            for (int b = 0; b <= m; ++b) {
+                acc[b][0] = fmaf(av, M[midx(m * 16 + k, b * 16 + c0)], acc[b][0]);
+                acc[b][1] = fmaf(av, M[midx(m * 16 + k, b * 16 + c0 + 8)], acc[b][1]);
+            }
         }
-        __syncthreads();
     }
+#pragma unroll
+    for (int b = 0; b < A_ROW; ++b) {
+        W[b * 256 + i * 16 + c0] = acc[b][0];
+        W[b * 256 + i * 16 + c0 + 8] = acc[b][1];
+    }
+    group_sync(kBarPrep);
+#pragma unroll
+    for (int b = 0; b < A_ROW; ++b) acc[b][0] = acc[b][1] = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const float tv = M[midx(row, A_ROW * 16 + k)];
+#pragma unroll
+        for (int b = 0; b < A_ROW; ++b) {
+            acc[b][0] = fmaf(tv, W[b * 256 + k * 16 + c0], acc[b][0]);
+            acc[b][1] = fmaf(tv, W[b * 256 + k * 16 + c0 + 8], acc[b][1]);
+        }
+    }
+#pragma unroll
+    for (int b = 0; b < A_ROW; ++b) {
+        M[midx(row, b * 16 + c0)] = -acc[b][0];
+        M[midx(row, b * 16 + c0 + 8)] = -acc[b][1];
+    }
+    group_sync(kBarPrep);
 }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-prefill_chunk_tc_kernel(const PrefillArgs a) {
-    using L = Smem<D>;
+prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
+    using SM = Smem<D>;
+    const PrefillArgs &a = L.a;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sQK = sm + L::kQK, *sS0T = sm + L::kS0T, *sVpT = sm + L::kVpT, *sUT = sm + L::kUT;
-    uint8_t *sTpp = sm + L::kTpp, *sP = sm + L::kP, *sKtT = sm + L::kKtT;
-    uint16_t *sV = reinterpret_cast<uint16_t *>(sm + L::kV);
-    float *sA = reinterpret_cast<float *>(sm + L::kA), *sT = reinterpret_cast<float *>(sm + L::kT);
-    float *sW = reinterpret_cast<float *>(sm + L::kW), *sG = reinterpret_cast<float *>(sm + L::kG);
-    float *sGam = reinterpret_cast<float *>(sm + L::kGam), *sDec = reinterpret_cast<float *>(sm + L::kDec);
-    float *sBeta = reinterpret_cast<float *>(sm + L::kBeta), *sGraw = reinterpret_cast<float *>(sm + L::kGraw);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::kBar);
-    uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(sm + L::kTmem);
-    int *flag = reinterpret_cast<int *>(sm + L::kFlag);
-    long long *part = reinterpret_cast<long long *>(sm + L::kEoff);
+    // Stage s (chunk parity) buffers, by offset from stage 0.
+    auto sQK = [&](int st) { return sm + SM::kQK0 + st * SM::kQKBytes; };
+    auto sTpp = [&](int st) { return sm + SM::kTpp0 + st * 8192; };
+    auto sP = [&](int st) { return sm + SM::kP0 + st * 8192; };
+    auto sKtT = [&](int st) { return sm + SM::kKtT0 + st * (D * 128); };
+    auto sGam = [&](int st) { return reinterpret_cast<float *>(sm + SM::kGam0 + st * 256); };
+    auto sGamC = [&](int st) { return reinterpret_cast<float *>(sm + SM::kGamC + st * 256); };
+    uint8_t *sS0T = sm + SM::kS0T, *sVpT = sm + SM::kVpT, *sUT = sm + SM::kUT;
+    float *sM = reinterpret_cast<float *>(sm + SM::kM), *sW = reinterpret_cast<float *>(sm + SM::kW);
+    float *sG = reinterpret_cast<float *>(sm + SM::kG), *sBeta = reinterpret_cast<float *>(sm + SM::kBeta);
+    float *sGraw = reinterpret_cast<float *>(sm + SM::kGraw);
+    float *sDec = reinterpret_cast<float *>(sm + SM::kDec);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SM::kBars);
+    uint64_t *mma_bar = bars + 0, *gram_bar = bars + 1, *ready = bars + 2, *freeb = bars + 4;
+    uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(sm + SM::kTmem);
+    int *fail = reinterpret_cast<int *>(sm + SM::kFail);
+    long long *part = reinterpret_cast<long long *>(sm + SM::kEoff);
 
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int seq = blockIdx.x / a.h_v, h = blockIdx.x % a.h_v;
+    const int rank = blockIdx.x / a.h_v, h = blockIdx.x % a.h_v;
+    const int seq = rank < L.n_order ? L.order[rank] : rank;
     const int kh = h / (a.h_v / a.h_k);
     const int t0 = a.cu_seqlens[seq];
     const int Lseq = a.cu_seqlens[seq + 1] - t0;
@@ -247,6 +335,7 @@ prefill_chunk_tc_kernel(const PrefillArgs a) {
     const int src = a.src_slot ? a.src_slot[seq] : -1;
     const int dst = a.dst_slot ? a.dst_slot[seq] : -1;
     const size_t ldq = static_cast<size_t>(a.h_k) * D, ldv = static_cast<size_t>(a.h_v) * D;
+    const int n_chunks = (Lseq + kChunk - 1) / kChunk;
 
     if (src >= a.num_slots || dst >= a.num_slots) {
         if (tid == 0) report(a.dev_status, GDN_DEV_BAD_SLOT);
@@ -258,326 +347,450 @@ prefill_chunk_tc_kernel(const PrefillArgs a) {
         return;
     }
 
-    // ---- set-up: TMEM, barrier, initial state ----------------------------------
+    // ---- set-up ----------------------------------------------------------------------
     if (warp == 0) {
         tc::tmem_alloc(tmem_ptr, kTmemCols);
         tc::tmem_relinquish();
     }
     if (tid == 0) {
-        tc::mbar_init(bar, 1);
-        *flag = 0;
+        tc::mbar_init(mma_bar, 1);
+        tc::mbar_init(gram_bar, 1);
+        tc::mbar_init(ready + 0, kGroup);
+        tc::mbar_init(ready + 1, kGroup);
+        tc::mbar_init(freeb + 0, kGroup);
+        tc::mbar_init(freeb + 1, kGroup);
+        *fail = 0;
     }
-    // Rows >= D of the transposed operand tiles stay zero (d = 64 pads M to 128).
-    if (D < 128) {
+    if (D < 128) {  // rows >= D of the transposed operand tiles stay zero (d = 64 pads M to 128)
         for (int e = tid; e < 128 * D * 2 / 16; e += kThreads)
             reinterpret_cast<uint4 *>(sS0T)[e] = make_uint4(0, 0, 0, 0);
-        for (int e = tid; e < 128 * 64 * 2 / 16; e += kThreads) {
+        for (int e = tid; e < 16384 / 16; e += kThreads) {
             reinterpret_cast<uint4 *>(sVpT)[e] = make_uint4(0, 0, 0, 0);
             reinterpret_cast<uint4 *>(sUT)[e] = make_uint4(0, 0, 0, 0);
         }
-    }
-    // Strict upper triangles of the scratch matrices stay zero.
-    for (int e = tid; e < 64 * kAS; e += kThreads) {
-        sA[e] = 0.f;
-        sT[e] = 0.f;
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tbase = *tmem_ptr;
     const uint32_t my_lane = lane_addr(tbase, warp, 0);
-    (void)GDN_GUARD(a.dev_status, tbase == 0, 50, tbase);
-    (void)GDN_GUARD(a.dev_status, (tc::smem_u32(sm) & 1023u) == 0 && tc::smem_u32(sm) + L::kBytes <= 232448u, 51,
-                    tc::smem_u32(sm));
-    const int j = tid;  // value column owned by this thread (valid when j < D)
 
-    // Initial state S0^T row j: fp32 into TMEM (D5), fp16 into the S0^T
-    // operand tile; or, for an empty sequence, straight to the destination.
-    if (j < D) {
-        const float *sp = (src >= 0 && GDN_GUARD(a.dev_status, src < a.num_slots, 3, src))
-                              ? a.state + ((static_cast<size_t>(src) * a.h_v + h) * D + j) * D
-                              : nullptr;
-        float *dp = (Lseq == 0 && dst >= 0 && GDN_GUARD(a.dev_status, dst < a.num_slots, 4, dst))
-                        ? a.state + ((static_cast<size_t>(dst) * a.h_v + h) * D + j) * D
-                        : nullptr;
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t r[32];
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (sp) v = __ldcg(reinterpret_cast<const float4 *>(sp + c0 + i));
-                r[i] = __float_as_uint(v.x);
-                r[i + 1] = __float_as_uint(v.y);
-                r[i + 2] = __float_as_uint(v.z);
-                r[i + 3] = __float_as_uint(v.w);
-                if (dp) __stcg(reinterpret_cast<float4 *>(dp + c0 + i), v);
-            }
-            if (Lseq > 0) {
-                tc::tmem_st32(my_lane + kColD5 + c0, r);
-                store_f16_chunks32(sS0T, j, c0, r);
-            }
-        }
-    }
-
-    const uint32_t aQK = tc::smem_u32(sQK), aS0T = tc::smem_u32(sS0T), aVpT = tc::smem_u32(sVpT);
-    const uint32_t aUT = tc::smem_u32(sUT), aTpp = tc::smem_u32(sTpp), aP = tc::smem_u32(sP);
-    const uint32_t aKtT = tc::smem_u32(sKtT);
-    uint32_t phase = 0;
-    const int n_chunks = (Lseq + kChunk - 1) / kChunk;
-    bool failed = false;
-
-    // Issues nothing itself; every thread waits for the last commit.
-    auto wait_mma = [&]() -> bool {
-        const long long start = clock64();
-        bool ok = false;
-        while (!(ok = tc::mbar_try_wait(bar, phase)))
-            if (clock64() - start > kWaitCycles) break;
-        phase ^= 1u;
-        tc::fence_after_sync();
-        return __syncthreads_or(!ok) == 0;
-    };
-
-    for (int c = 0; c < n_chunks && !failed; ++c) {
-        const int tok0 = t0 + c * kChunk;
-        const int n = min(kChunk, Lseq - c * kChunk);
-
-        // ---- L: chunk inputs -> smem (q, k as fp16 operand tiles; v as bf16) ----
-        for (int e = tid; e < 64 * (D / 8); e += kThreads) {
-            const int r = e / (D / 8), cc = e % (D / 8);
-            uint4 qv = make_uint4(0, 0, 0, 0), kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-            if (r < n && GDN_GUARD(a.dev_status, tok0 + r < a.total_tokens, 1, tok0 + r)) {
-                const size_t row = static_cast<size_t>(tok0 + min(r, n - 1));  // always a row of this chunk
-                qv = bf16x8_to_f16x8(__ldg(reinterpret_cast<const uint4 *>(a.q + row * ldq + kh * D + cc * 8)));
-                kv = bf16x8_to_f16x8(__ldg(reinterpret_cast<const uint4 *>(a.k + row * ldq + kh * D + cc * 8)));
-                vv = __ldg(reinterpret_cast<const uint4 *>(a.v + row * ldv + static_cast<size_t>(h) * D + cc * 8));
-            }
-            if (!GDN_GUARD(a.dev_status, tc::sw128_chunk_offset(64 + r, cc, 128) + 16 <= 128u * D * 2 &&
-                                            r * D + cc * 8 + 8 <= 64 * D, 11, e))
-                continue;
-            *reinterpret_cast<uint4 *>(sQK + tc::sw128_chunk_offset(r, cc, 128)) = qv;
-            *reinterpret_cast<uint4 *>(sQK + tc::sw128_chunk_offset(64 + r, cc, 128)) = kv;
-            *reinterpret_cast<uint4 *>(sV + r * D + cc * 8) = vv;
-        }
-        if (tid < 64) {
-            const size_t gi = static_cast<size_t>(tok0 + min(tid, n - 1)) * a.h_v + h;
-            const bool in = tid < n && GDN_GUARD(a.dev_status, tok0 + tid < a.total_tokens, 2, tok0 + tid);
-            sGraw[tid] = in ? a.g[gi] : 0.f;
-            sBeta[tid] = in ? a.beta[gi] : 0.f;
-        }
-        __syncthreads();
-        if (warp == 0) {
-            // inclusive prefix sum of g over the chunk, fixed order
-            const int l = tid;
-            const float g0 = sGraw[2 * l], g1 = sGraw[2 * l + 1];
-            const float pair = g0 + g1;
-            float incl = pair;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (l >= o) incl += y;
-            }
-            const float excl = incl - pair;
-            sG[2 * l] = excl + g0;
-            sG[2 * l + 1] = excl + g0 + g1;
-        }
-        __syncwarp();
-        __syncthreads();
-        if (tid < 64) {
-            sGam[tid] = expf(sG[tid]);
-            sDec[tid] = expf(sG[63] - sG[tid]);
-        }
-        tc::fence_proxy_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-
-        // ---- M1: Gram [Q;K] K^T and D1 = S0^T [Q;K]^T ----------------------------
-        if (tid == 0) {
-            tc::fence_after_sync();
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
-                tc::mma_f16(tbase + kColGram, tc::desc_k_sw128(aQK + off), tc::desc_k_sw128(aQK + off + 64 * 128),
-                            tc::idesc_f16_f32acc(128, 64), kk > 0);
-            }
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
-                tc::mma_f16(tbase + kColD1, tc::desc_k_sw128(aS0T + off), tc::desc_k_sw128(aQK + off),
-                            tc::idesc_f16_f32acc(128, 128), kk > 0);
-            }
-            tc::mma_commit(bar);
-        }
-        __syncwarp();
-        if (!wait_mma()) {
-            failed = true;
-            break;
-        }
-
-        // ---- G: P (from Q K^T rows) and A (from K K^T rows) ------------------------
-        {
-            float x[64];
-            tmem_load_row<64>(my_lane + kColGram, x);
-            if (tid < 64) {
-                const int t = tid & 63;
-                const float Gt = sG[t];
-#pragma unroll
-                for (int s = 0; s < 64; ++s) x[s] = (s <= t) ? expf(Gt - sG[s]) * x[s] : 0.f;
-                store_row64_f16(sP, 64, t, x, a.dev_status);
-            } else {
-                const int i = tid & 63;
-                const float Gi = sG[i], bi = sBeta[i];
-#pragma unroll
-                for (int s = 0; s < 64; ++s)
-                    if (s < i && GDN_GUARD(a.dev_status, i * kAS + s < 64 * kAS, 15, i)) sA[i * kAS + s] = bi * (expf(Gi - sG[s]) * x[s]);
-            }
-        }
-        // Ktil^T[i][t] = exp(G_C - G_t) k_t[i]
-        if (tid < D) {
-            const int i = tid & (D - 1);
-            float x[64];
-#pragma unroll
-            for (int t = 0; t < 64; ++t) {
-                const uint16_t kb = *reinterpret_cast<const uint16_t *>(sQK + tc::sw128_offset(64 + t, i, 128));
-                x[t] = sDec[t] * half_bits_to_float(kb);
-            }
-            store_row64_f16(sKtT, D, i, x, a.dev_status);
-        }
-        __syncthreads();
-
-        // ---- I: T = (I + A)^-1, T'' = T diag(beta) ----------------------------------
-        invert_unit_lower_64(sA, sT, sW, tid);
-        if (tid < 64) {
-            // Row index masked: the loads stay inside T even if they are
-            // executed for threads outside the branch.
-            const int t = tid & 63;
-            float x[64];
-#pragma unroll
-            for (int s = 0; s < 64; ++s) x[s] = (s <= t) ? sT[t * kAS + s] * sBeta[s] : 0.f;
-            store_row64_f16(sTpp, 64, t, x, a.dev_status);
-        }
-
-        // ---- C2: V'^T = V^T - (K S0)^T diag(gamma); gamma_C scales the state -----
+    if (warp < 4) {
+        // ============================ chain group ==============================
+        const int j = tid;  // value column (valid when j < D)
+        const int jm = j & (D - 1);
+        // Initial state row j: fp32 into D5, fp16 into the S0^T tile; or, for
+        // an empty sequence, straight to the destination slot.
         if (j < D) {
-            float ks[64];
-            tmem_load_row<64>(my_lane + kColD1 + 64, ks);
-#pragma unroll
-            for (int t = 0; t < 64; ++t) {
-                const uint16_t vb = sV[t * D + (j & (D - 1))];
-                ks[t] = __uint_as_float(static_cast<uint32_t>(vb) << 16) - sGam[t] * ks[t];
-            }
-            store_row64_f16(sVpT, 128, j, ks, a.dev_status);
-        }
-        tc::fence_proxy_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            tc::fence_after_sync();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                tc::mma_f16(tbase + kColD3, tc::desc_k_sw128(aVpT + kk * 32), tc::desc_k_sw128(aTpp + kk * 32),
-                            tc::idesc_f16_f32acc(128, 64), kk > 0);
-            tc::mma_commit(bar);
-        }
-        __syncwarp();
-        if (j < D) {
-            const float gC = sGam[63];
+            const float *sp = src >= 0 ? a.state + ((static_cast<size_t>(src) * a.h_v + h) * D + jm) * D : nullptr;
+            float *dp = (Lseq == 0 && dst >= 0) ? a.state + ((static_cast<size_t>(dst) * a.h_v + h) * D + jm) * D
+                                                : nullptr;
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t r[32];
-                tc::tmem_ld32(my_lane + kColD5 + c0, r);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(gC * __uint_as_float(r[i]));
-                tc::tmem_st32(my_lane + kColD5 + c0, r);
-            }
-        }
-        tc::fence_before_sync();
-        if (!wait_mma()) {
-            failed = true;
-            break;
-        }
-
-        // ---- C4: U^T to fp16; D5 += U^T Ktil, D6 = U^T P^T ---------------------------
-        if (j < D) {
-            float u[64];
-            tmem_load_row<64>(my_lane + kColD3, u);
-            store_row64_f16(sUT, 128, j, u, a.dev_status);
-        }
-        tc::fence_proxy_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            tc::fence_after_sync();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                tc::mma_f16(tbase + kColD5, tc::desc_k_sw128(aUT + kk * 32), tc::desc_k_sw128(aKtT + kk * 32),
-                            tc::idesc_f16_f32acc(128, D), 1);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                tc::mma_f16(tbase + kColD6, tc::desc_k_sw128(aUT + kk * 32), tc::desc_k_sw128(aP + kk * 32),
-                            tc::idesc_f16_f32acc(128, 64), kk > 0);
-            tc::mma_commit(bar);
-        }
-        __syncwarp();
-        if (!wait_mma()) {
-            failed = true;
-            break;
-        }
-
-        // ---- C6: new state, emission, outputs -----------------------------------------
-        uint16_t *sO = reinterpret_cast<uint16_t *>(sVpT);  // V'^T is consumed: reuse as O staging
-        if (j < D) {
-            const bool emit = E > 0 && a.chunk_states && n == kChunk && ((c + 1) % E) == 0;
-            float *ep = nullptr;
-            if (emit) {
-                const int64_t idx = eoff + (c + 1) / E - 1;
-                if (GDN_GUARD(a.dev_status, idx >= 0 && idx < a.chunk_capacity, 5, idx))
-                    ep = a.chunk_states + ((static_cast<size_t>(idx) * a.h_v + h) * D + j) * D;
-            }
-            float *dp = (c == n_chunks - 1 && dst >= 0 && GDN_GUARD(a.dev_status, dst < a.num_slots, 4, dst))
-                            ? a.state + ((static_cast<size_t>(dst) * a.h_v + h) * D + j) * D
-                            : nullptr;
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t r[32];
-                tc::tmem_ld32(my_lane + kColD5 + c0, r);
-                store_f16_chunks32(sS0T, j, c0, r);
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
-                    const float4 v = make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
-                                                 __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-                    if (ep) __stcg(reinterpret_cast<float4 *>(ep + c0 + i), v);
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (sp) v = __ldcg(reinterpret_cast<const float4 *>(sp + c0 + i));
+                    r[i] = __float_as_uint(v.x);
+                    r[i + 1] = __float_as_uint(v.y);
+                    r[i + 2] = __float_as_uint(v.z);
+                    r[i + 3] = __float_as_uint(v.w);
                     if (dp) __stcg(reinterpret_cast<float4 *>(dp + c0 + i), v);
                 }
-            }
-            float qs[64], pu[64];
-            tmem_load_row<64>(my_lane + kColD1, qs);
-            tmem_load_row<64>(my_lane + kColD6, pu);
-#pragma unroll
-            for (int t = 0; t < 64; ++t) {
-                const float ov = a.scale * fmaf(sGam[t], qs[t], pu[t]);
-                if (GDN_GUARD(a.dev_status, t * D + j < 64 * 128, 17, t * D + j)) sO[t * D + j] = float_to_bf16_bits(ov);
+                if (Lseq > 0) {
+                    tc::tmem_st32(my_lane + kColD5 + c0, r);
+                    store_f16_chunks32(sS0T, jm, c0, r);
+                }
             }
         }
+        tc::fence_proxy_async_smem();
         tc::fence_before_sync();
-        __syncthreads();
-        for (int e = tid; e < n * (D / 8); e += kThreads) {
-            const int t = e / (D / 8), cc = e % (D / 8);
-            if (!GDN_GUARD(a.dev_status, tok0 + t < a.total_tokens, 6, tok0 + t)) continue;
-            *reinterpret_cast<uint4 *>(a.o + static_cast<size_t>(tok0 + t) * ldv + static_cast<size_t>(h) * D +
-                                       cc * 8) = *reinterpret_cast<const uint4 *>(sO + t * D + cc * 8);
+        group_sync(kBarChain);
+
+        // Shared-memory descriptors; a K step adds its byte offset / 16.
+        const uint64_t dS0T = tc::desc_k_sw128(tc::smem_u32(sS0T));
+        const uint64_t dVpT = tc::desc_k_sw128(tc::smem_u32(sVpT));
+        const uint64_t dUT = tc::desc_k_sw128(tc::smem_u32(sUT));
+        constexpr uint32_t kIdN128 = tc::idesc_f16_f32acc(128, 128), kIdN64 = tc::idesc_f16_f32acc(128, 64);
+        constexpr uint32_t kIdND = tc::idesc_f16_f32acc(128, D);
+        uint32_t mma_phase = 0;
+        bool failed = false;
+        int prev_n = 0, prev_tok0 = 0;
+
+        // Output of a finished chunk: o_t = scale (gamma_t (Q S0)_t + (P U)_t),
+        // staged as bf16 [t][D] in the V'^T tile (free between S3 of that chunk
+        // and C2 of the next) and stored with 16-byte writes.
+        uint16_t *sOst = reinterpret_cast<uint16_t *>(sVpT);
+        auto output = [&](int buf, int n_out, int tok_out) {
+            if (j < D) {
+                float qs[64], pu[64];
+                tmem_load_row<64>(my_lane + kColD1 + 128 * buf, qs);
+                tmem_load_row<64>(my_lane + kColD6, pu);
+                const float *gam = sGamC(buf);
+#pragma unroll
+                for (int t = 0; t < 64; ++t) sOst[t * D + jm] = float_to_bf16_bits(a.scale * fmaf(gam[t], qs[t], pu[t]));
+            }
+            tc::fence_before_sync();
+            group_sync(kBarChain);
+            for (int e = tid; e < n_out * (D / 8); e += kGroup) {
+                const int t = e / (D / 8), cc = e % (D / 8);
+                *reinterpret_cast<uint4 *>(a.o + static_cast<size_t>(tok_out + t) * ldv + static_cast<size_t>(h) * D +
+                                           cc * 8) = *reinterpret_cast<const uint4 *>(sOst + t * D + cc * 8);
+            }
+            group_sync(kBarChain);
+        };
+
+        for (int c = 0; c < n_chunks; ++c) {
+            const int s = c & 1;
+            const int tok0 = t0 + c * kChunk;
+            const int n = min(kChunk, Lseq - c * kChunk);
+            const uint32_t d1 = tbase + kColD1 + 128 * s;
+            const uint32_t d1_lane = my_lane + kColD1 + 128 * s;
+
+            // ---- values of the chunk (independent of the prep group), staged as
+            //      bf16 [t][D] in the U^T tile (free until C4 of this chunk) ----
+            uint16_t *sVst = reinterpret_cast<uint16_t *>(sUT);
+            {
+                constexpr int kPer = 64 * (D / 8) / kGroup;
+                uint4 vv[kPer];
+#pragma unroll
+                for (int it = 0; it < kPer; ++it) {
+                    const int e = tid + it * kGroup;
+                    const int r = e / (D / 8), cc = e % (D / 8);
+                    const size_t row = static_cast<size_t>(tok0 + min(r, n - 1));  // always a row of this chunk
+                    vv[it] = __ldg(reinterpret_cast<const uint4 *>(a.v + row * ldv + static_cast<size_t>(h) * D + cc * 8));
+                }
+#pragma unroll
+                for (int it = 0; it < kPer; ++it) {
+                    const int e = tid + it * kGroup;
+                    const int r = e / (D / 8), cc = e % (D / 8);
+                    *reinterpret_cast<uint4 *>(sVst + r * D + cc * 8) = r < n ? vv[it] : make_uint4(0, 0, 0, 0);
+                }
+            }
+
+            // ---- wait for the chunk's operands ---------------------------------
+            const bool ok_ready = mbar_wait_bounded(ready + s, (c >> 1) & 1);
+            if (group_any(kBarChain, !ok_ready)) {
+                failed = true;
+                break;
+            }
+            tc::fence_after_sync();
+
+            // ---- S1: D1 = S0^T [Q;K]^T --------------------------------------------
+            if (tid == 0) {
+                const uint64_t dQK = tc::desc_k_sw128(tc::smem_u32(sQK(s)));
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4;
+                    tc::mma_f16(d1, dS0T + off, dQK + off, kIdN128, kk > 0);
+                }
+                tc::mma_commit(mma_bar);
+            }
+            __syncwarp();
+            if (tid < 64) sGamC(s)[tid & 63] = sGam(s)[tid & 63];  // kept for the output of this chunk
+
+            // ---- output of the previous chunk while S1 runs ---------------------
+            if (c > 0) output(s ^ 1, prev_n, prev_tok0);
+
+            // ---- C2: V'^T = V^T - (K S0)^T diag(gamma) --------------------------
+            const bool ok1 = mbar_wait_bounded(mma_bar, mma_phase);
+            mma_phase ^= 1u;
+            if (group_any(kBarChain, !ok1)) {
+                failed = true;
+                break;
+            }
+            tc::fence_after_sync();
+            if (j < D) {
+                float ks[64];
+                tmem_load_row<64>(d1_lane + 64, ks);
+                const float *gam = sGam(s);
+#pragma unroll
+                for (int t = 0; t < 64; ++t)
+                    ks[t] = __uint_as_float(static_cast<uint32_t>(sVst[t * D + jm]) << 16) - gam[t] * ks[t];
+                store_row64_f16(sVpT, 128, jm, ks);
+            }
+            tc::fence_proxy_async_smem();
+            tc::fence_before_sync();
+            group_sync(kBarChain);
+            if (tid == 0) {
+                tc::fence_after_sync();
+                const uint64_t dT = tc::desc_k_sw128(tc::smem_u32(sTpp(s)));
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) tc::mma_f16(d1 + 64, dVpT + kk * 2, dT + kk * 2, kIdN64, kk > 0);
+                tc::mma_commit(mma_bar);
+            }
+            __syncwarp();
+            if (j < D) {  // gamma_C scales the state while S3 runs
+                const float gC = sGam(s)[63];
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t r[32];
+                    tc::tmem_ld32(my_lane + kColD5 + c0, r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(gC * __uint_as_float(r[i]));
+                    tc::tmem_st32(my_lane + kColD5 + c0, r);
+                }
+            }
+            tc::fence_before_sync();
+
+            // ---- C4: U^T to fp16; D5 += U^T Ktil, D6 = U^T P^T --------------------
+            const bool ok2 = mbar_wait_bounded(mma_bar, mma_phase);
+            mma_phase ^= 1u;
+            if (group_any(kBarChain, !ok2)) {
+                failed = true;
+                break;
+            }
+            tc::fence_after_sync();
+            if (j < D) {
+                float u[64];
+                tmem_load_row<64>(d1_lane + 64, u);
+                store_row64_f16(sUT, 128, jm, u);
+            }
+            tc::fence_proxy_async_smem();
+            tc::fence_before_sync();
+            group_sync(kBarChain);
+            if (tid == 0) {
+                tc::fence_after_sync();
+                const uint64_t dKt = tc::desc_k_sw128(tc::smem_u32(sKtT(s)));
+                const uint64_t dPs = tc::desc_k_sw128(tc::smem_u32(sP(s)));
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) tc::mma_f16(tbase + kColD5, dUT + kk * 2, dKt + kk * 2, kIdND, 1);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) tc::mma_f16(tbase + kColD6, dUT + kk * 2, dPs + kk * 2, kIdN64, kk > 0);
+                tc::mma_commit(mma_bar);
+            }
+            __syncwarp();
+
+            // ---- C6: new state -> S0^T tile, emission, final state -----------------
+            const bool ok3 = mbar_wait_bounded(mma_bar, mma_phase);
+            mma_phase ^= 1u;
+            if (group_any(kBarChain, !ok3)) {
+                failed = true;
+                break;
+            }
+            tc::fence_after_sync();
+            mbar_arrive(freeb + s);  // every MMA and read of this chunk's stage is done
+            if (j < D) {
+                float *ep = nullptr;
+                if (E > 0 && a.chunk_states && n == kChunk && ((c + 1) % E) == 0) {
+                    const int64_t idx = eoff + (c + 1) / E - 1;
+                    if (idx >= 0 && idx < a.chunk_capacity)
+                        ep = a.chunk_states + ((static_cast<size_t>(idx) * a.h_v + h) * D + jm) * D;
+                }
+                float *dp = (c == n_chunks - 1 && dst >= 0)
+                                ? a.state + ((static_cast<size_t>(dst) * a.h_v + h) * D + jm) * D
+                                : nullptr;
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t r[32];
+                    tc::tmem_ld32(my_lane + kColD5 + c0, r);
+                    store_f16_chunks32(sS0T, jm, c0, r);
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const float4 v = make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                                                     __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                        if (ep) __stcg(reinterpret_cast<float4 *>(ep + c0 + i), v);
+                        if (dp) __stcg(reinterpret_cast<float4 *>(dp + c0 + i), v);
+                    }
+                }
+            }
+            tc::fence_proxy_async_smem();
+            tc::fence_before_sync();
+            group_sync(kBarChain);
+            prev_n = n;
+            prev_tok0 = tok0;
         }
-        __syncthreads();
+        if (!failed && n_chunks > 0) output((n_chunks - 1) & 1, prev_n, prev_tok0);
+        if (failed) {
+            if (tid == 0) {
+                report(a.dev_status, GDN_DEV_TIMEOUT);
+                atomicExch(fail, 1);
+            }
+            // MMAs already issued get a bounded time to finish before the TMEM
+            // they write is released.
+            mbar_wait_bounded(mma_bar, mma_phase);
+        }
+    } else {
+        // ============================= prep group ==============================
+        const int p = tid - kGroup;  // 0..127, TMEM lane p
+        bool failed = false;
+        const uint32_t aIdGram = tc::idesc_f16_f32acc(128, 64);
+        for (int c = 0; c < n_chunks; ++c) {
+            const int s = c & 1;
+            const int tok0 = t0 + c * kChunk;
+            const int n = min(kChunk, Lseq - c * kChunk);
+            if (c >= 2) {
+                const bool ok = mbar_wait_bounded(freeb + s, ((c - 2) >> 1) & 1);
+                if (group_any(kBarPrep, !ok)) {
+                    failed = true;
+                    break;
+                }
+            }
+            // ---- q, k as fp16 operand tiles; g, beta ----------------------------------
+            uint8_t *qk = sQK(s);
+            {
+                float gv = 0.f, bv = 0.f;
+                const int t = p & 63;
+                if (p < 64) {
+                    const size_t gi = static_cast<size_t>(tok0 + min(t, n - 1)) * a.h_v + h;
+                    gv = a.g[gi];
+                    bv = a.beta[gi];
+                }
+                constexpr int kPer = 64 * (D / 8) / kGroup;  // 16-byte chunks per thread per tile
+                uint4 qv[kPer], kv[kPer];
+#pragma unroll
+                for (int it = 0; it < kPer; ++it) {
+                    const int e = p + it * kGroup;
+                    const int r = e / (D / 8), cc = e % (D / 8);
+                    const size_t row = static_cast<size_t>(tok0 + min(r, n - 1));  // always a row of this chunk
+                    qv[it] = __ldg(reinterpret_cast<const uint4 *>(a.q + row * ldq + kh * D + cc * 8));
+                    kv[it] = __ldg(reinterpret_cast<const uint4 *>(a.k + row * ldq + kh * D + cc * 8));
+                }
+#pragma unroll
+                for (int it = 0; it < kPer; ++it) {
+                    const int e = p + it * kGroup;
+                    const int r = e / (D / 8), cc = e % (D / 8);
+                    const uint4 z = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(qk + tc::sw128_chunk_offset(r, cc, 128)) =
+                        r < n ? bf16x8_to_f16x8(qv[it]) : z;
+                    *reinterpret_cast<uint4 *>(qk + tc::sw128_chunk_offset(64 + r, cc, 128)) =
+                        r < n ? bf16x8_to_f16x8(kv[it]) : z;
+                }
+                if (p < 64) {
+                    sGraw[t] = t < n ? gv : 0.f;
+                    sBeta[t] = t < n ? bv : 0.f;
+                }
+            }
+            if (c + 1 < n_chunks) {  // the next chunk's q, k rows into L2
+                const int rn = min(kChunk, Lseq - (c + 1) * kChunk);
+                const int r = p & 63;
+                if (r < rn) {
+                    const size_t row = static_cast<size_t>(tok0 + kChunk + r);
+                    const uint16_t *src_row = (p < 64 ? a.q : a.k) + row * ldq + kh * D;
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(src_row) : "memory");
+                    if (D > 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(src_row + 64) : "memory");
+                }
+            }
+            group_sync(kBarPrep);
+            if (p < 32) {  // inclusive prefix sum of g over the chunk, fixed order
+                const int l = p & 31;
+                const float g0 = sGraw[2 * l], g1 = sGraw[2 * l + 1];
+                const float pair = g0 + g1;
+                float incl = pair;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (l >= o) incl += y;
+                }
+                const float excl = incl - pair;
+                sG[2 * l] = excl + g0;
+                sG[2 * l + 1] = excl + g0 + g1;
+            }
+            group_sync(kBarPrep);
+            if (p < 64) {
+                const int t = p & 63;
+                sGam(s)[t] = expf(sG[t]);
+                sDec[t] = expf(sG[63] - sG[t]);
+            }
+            tc::fence_proxy_async_smem();
+            tc::fence_before_sync();
+            group_sync(kBarPrep);
+
+            // ---- Gram [Q;K] K^T --------------------------------------------------------
+            if (p == 0) {
+                tc::fence_after_sync();
+                const uint64_t dQK = tc::desc_k_sw128(tc::smem_u32(qk));
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4;
+                    tc::mma_f16(tbase + kColGram, dQK + off, dQK + off + (64 * 128 >> 4), aIdGram, kk > 0);
+                }
+                tc::mma_commit(gram_bar);
+            }
+            __syncwarp();
+            const bool okg = mbar_wait_bounded(gram_bar, c & 1);
+            if (group_any(kBarPrep, !okg)) {
+                failed = true;
+                mbar_wait_bounded(gram_bar, c & 1);  // let an issued Gram finish before TMEM is freed
+                break;
+            }
+            tc::fence_after_sync();
+
+            // ---- P rows (lanes 0..63) and A rows (lanes 64..127) -------------------
+            {
+                float x[64];
+                tmem_load_row<64>(my_lane + kColGram, x);
+                const int r = p & 63;
+                const float Gr = sG[r];
+#pragma unroll
+                for (int q4 = 0; q4 < 64; q4 += 4) {
+                    const float4 g4 = *reinterpret_cast<const float4 *>(sG + q4);
+                    x[q4 + 0] = (q4 + 0 <= r) ? __expf(Gr - g4.x) * x[q4 + 0] : 0.f;
+                    x[q4 + 1] = (q4 + 1 <= r) ? __expf(Gr - g4.y) * x[q4 + 1] : 0.f;
+                    x[q4 + 2] = (q4 + 2 <= r) ? __expf(Gr - g4.z) * x[q4 + 2] : 0.f;
+                    x[q4 + 3] = (q4 + 3 <= r) ? __expf(Gr - g4.w) * x[q4 + 3] : 0.f;
+                }
+                if (p < 64) {
+                    store_row64_f16(sP(s), 64, r, x);
+                } else {
+                    const float br = sBeta[r];
+#pragma unroll
+                    for (int q = 0; q < 64; ++q) sM[midx(r, q)] = (q < r) ? br * x[q] : 0.f;
+                }
+            }
+            tc::fence_before_sync();
+            group_sync(kBarPrep);
+
+            // ---- T = (I + A)^-1 (diagonal blocks) || Ktil^T rows 0..63 --------------
+            float xd[16];
+            if (p < 64) {
+                invert_diag_solve(sM, p, xd);
+            } else {
+                const int i = p & 63;
+                float x[64];
+#pragma unroll
+                for (int t = 0; t < 64; ++t) {
+                    const uint16_t kb = *reinterpret_cast<const uint16_t *>(qk + tc::sw128_offset(64 + t, i, 128));
+                    x[t] = sDec[t] * half_bits_to_float(kb);
+                }
+                store_row64_f16(sKtT(s), D, i, x);
+            }
+            group_sync(kBarPrep);
+            if (p < 64) invert_diag_store(sM, p, xd);
+            group_sync(kBarPrep);
+            invert_block_row<1>(sM, sW, p);
+            invert_block_row<2>(sM, sW, p);
+            invert_block_row<3>(sM, sW, p);
+
+            // ---- T'' = T diag(beta) (rows 0..63) || Ktil^T rows 64..127 ---------------
+            if (p >= 64) {
+                const int t = p & 63;
+                float x[64];
+#pragma unroll
+                for (int q = 0; q < 64; ++q) x[q] = (q <= t) ? sM[midx(t, q)] * sBeta[q] : 0.f;
+                store_row64_f16(sTpp(s), 64, t, x);
+            } else if (D > 64) {
+                const int i = 64 + (p & 63);
+                float x[64];
+#pragma unroll
+                for (int t = 0; t < 64; ++t) {
+                    const uint16_t kb =
+                        *reinterpret_cast<const uint16_t *>(qk + tc::sw128_offset(64 + t, i & (D - 1), 128));
+                    x[t] = sDec[t] * half_bits_to_float(kb);
+                }
+                store_row64_f16(sKtT(s), D, i & (D - 1), x);
+            }
+            tc::fence_proxy_async_smem();
+            mbar_arrive(ready + s);
+            group_sync(kBarPrep);  // scratch reuse by the next chunk
+        }
+        if (failed && p == 0) {
+            report(a.dev_status, GDN_DEV_TIMEOUT);
+            atomicExch(fail, 1);
+        }
     }
 
-    if (failed) {
-        if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
-        // Give MMAs that may still be in flight a bounded time to finish
-        // before the TMEM they write is released.
-        const long long start = clock64();
-        while (!tc::mbar_try_wait(bar, phase) && clock64() - start < kWaitCycles) {
-        }
-    }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -585,23 +798,36 @@ prefill_chunk_tc_kernel(const PrefillArgs a) {
 }
 
 template <int D>
-cudaError_t launch_d(const PrefillArgs &a, cudaStream_t stream) {
+cudaError_t launch_d(const PrefillLaunch &L, cudaStream_t stream) {
     const uint32_t smem = Smem<D>::kAlloc;
     cudaError_t e = cudaFuncSetAttribute(prefill_chunk_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    prefill_chunk_tc_kernel<D><<<a.num_seqs * a.h_v, kThreads, smem, stream>>>(a);
+    prefill_chunk_tc_kernel<D><<<L.a.num_seqs * L.a.h_v, kThreads, smem, stream>>>(L);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillArgs &a, int d, int64_t total_tokens, int32_t max_seqlen,
-                           cudaStream_t stream) {
-    (void)total_tokens;
-    (void)max_seqlen;
+cudaError_t launch_prefill(const PrefillArgs &a, int d, const int32_t *cu_host, cudaStream_t stream) {
     if (a.num_seqs == 0) return cudaSuccess;
-    return d == 128 ? launch_d<128>(a, stream) : launch_d<64>(a, stream);
+    static_assert(sizeof(PrefillLaunch) < 32000, "kernel parameter size");
+    // Longest sequences first, so the longest chains start in the first wave.
+    PrefillLaunch L;
+    L.a = a;
+    L.n_order = a.num_seqs < kMaxOrder ? a.num_seqs : kMaxOrder;
+    for (int i = 0; i < L.n_order; ++i) L.order[i] = i;
+    for (int i = 1; i < L.n_order; ++i) {  // insertion sort by length, descending, stable
+        const int v = L.order[i];
+        const int lv = cu_host[v + 1] - cu_host[v];
+        int k = i - 1;
+        while (k >= 0 && (cu_host[L.order[k] + 1] - cu_host[L.order[k]]) < lv) {
+            L.order[k + 1] = L.order[k];
+            --k;
+        }
+        L.order[k + 1] = v;
+    }
+    return d == 128 ? launch_d<128>(L, stream) : launch_d<64>(L, stream);
 }
 
 }  // namespace gdn
