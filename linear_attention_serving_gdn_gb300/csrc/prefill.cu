@@ -30,10 +30,13 @@
 // and the state carry are fp32.
 //
 // One CTA runs one (sequence, value head) chain, warp-specialised:
-//   chain group (warps 0-3, thread j owns TMEM lane j): the steps that
-//     depend on the state, S1 -> V' -> S3 -> U -> S5/S6 -> new state, plus
-//     the output of the previous chunk while S1 runs;
-//   prep group (warps 4-7): the chunk-local operands of the next chunk
+//   chain group (warps 0-7; warps w and w + 4 share TMEM lane quarter w, so
+//     lane j is served by two threads, each taking half of the row's tokens
+//     or state columns): the steps that depend on the state,
+//     S1 -> V' -> S3 -> U -> S5/S6 -> new state, plus the output of the
+//     previous chunk while S1 runs;
+//   prep group (warps 8-15, lanes split the same way): the chunk-local
+//     operands of the next chunk
 //     (fp16 Q/K tiles, decays, Gram, P, A, T = (I + A)^-1, T'') into a
 //     double-buffered stage, handed over through mbarriers.
 // A chunk's arithmetic depends only on its own inputs and the fp32 state
@@ -51,8 +54,8 @@
 namespace gdn {
 namespace {
 
-constexpr int kThreads = 256;  // chain group + prep group
-constexpr int kGroup = 128;
+constexpr int kThreads = 512;  // chain group + prep group
+constexpr int kGroup = 256;    // 8 warps per group: two warps per TMEM lane quarter
 constexpr int kBarChain = 1;   // named barrier ids (0 is __syncthreads)
 constexpr int kBarPrep = 2;
 // Upper bound on every wait, in SM clock cycles (~1 s): a wait that runs out
@@ -94,8 +97,8 @@ struct Smem {
     static constexpr uint32_t kBars = kDec + 256;              // 6 mbarriers
     static constexpr uint32_t kTmem = kBars + 48;              // TMEM base address
     static constexpr uint32_t kFail = kTmem + 4;               // int
-    static constexpr uint32_t kEoff = kFail + 4;               // long long [8]
-    static constexpr uint32_t kBytes = kEoff + 64;
+    static constexpr uint32_t kEoff = kFail + 4;               // long long [16]
+    static constexpr uint32_t kBytes = kEoff + 128;
     static constexpr uint32_t kAlloc = kBytes + 1024;          // + alignment slack
     static_assert(kS0T % 1024 == 0 && kVpT % 1024 == 0 && kUT % 1024 == 0 && kKtT0 % 1024 == 0, "");
     static_assert(kKtT1 % 1024 == 0 && kBars % 8 == 0, "");
@@ -129,19 +132,6 @@ __device__ __forceinline__ float half_bits_to_float(uint16_t h) {
     return __half2float(*reinterpret_cast<__half *>(&h));
 }
 
-// Writes 64 fp32 values as one fp16 row r (< rows) of a 64-wide K-major tile.
-__device__ __forceinline__ void store_row64_f16(uint8_t *tile, uint32_t rows, uint32_t r, const float *x) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        uint4 v;
-        v.x = pack_half2(x[8 * c + 0], x[8 * c + 1]);
-        v.y = pack_half2(x[8 * c + 2], x[8 * c + 3]);
-        v.z = pack_half2(x[8 * c + 4], x[8 * c + 5]);
-        v.w = pack_half2(x[8 * c + 6], x[8 * c + 7]);
-        *reinterpret_cast<uint4 *>(tile + tc::sw128_chunk_offset(r, c, rows)) = v;
-    }
-}
-
 // Writes columns [c0, c0 + 32) of row r (fp32 bit patterns) as fp16 into a
 // 128-row K-major SW128 tile.
 __device__ __forceinline__ void store_f16_chunks32(uint8_t *tile, uint32_t r, int c0, const uint32_t (&x)[32]) {
@@ -154,6 +144,18 @@ __device__ __forceinline__ void store_f16_chunks32(uint8_t *tile, uint32_t r, in
         v.w = pack_half2(__uint_as_float(x[8 * q + 6]), __uint_as_float(x[8 * q + 7]));
         *reinterpret_cast<uint4 *>(tile + tc::sw128_chunk_offset(r, c0 / 8 + q, 128)) = v;
     }
+}
+
+// Writes 8 fp32 values as the 16-byte fp16 chunk `chunk` of row r of a K-major
+// SW128 tile of `rows` rows.
+__device__ __forceinline__ void store_chunk8_f16(uint8_t *tile, uint32_t rows, uint32_t r, uint32_t chunk,
+                                                 const float *x) {
+    uint4 v;
+    v.x = pack_half2(x[0], x[1]);
+    v.y = pack_half2(x[2], x[3]);
+    v.z = pack_half2(x[4], x[5]);
+    v.w = pack_half2(x[6], x[7]);
+    *reinterpret_cast<uint4 *>(tile + tc::sw128_chunk_offset(r, chunk, rows)) = v;
 }
 
 __device__ __forceinline__ uint32_t lane_addr(uint32_t tbase, int warp, uint32_t col) {
@@ -172,7 +174,7 @@ __device__ __forceinline__ void tmem_load_row(uint32_t taddr, float (&x)[N]) {
     }
 }
 
-// Group barrier (named barrier over the group's 128 threads).
+// Group barrier (named barrier over the group's 256 threads).
 __device__ __forceinline__ void group_sync(int id) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(kGroup) : "memory");
 }
@@ -224,7 +226,7 @@ __device__ int64_t emit_offset(const int32_t *cu, int s, int E, long long *part)
 
 // In place, M := (I + M)^-1 for a 64x64 strictly lower-triangular M (the
 // diagonal of M is ignored and the result has unit diagonal), in two parts
-// run by the prep group (p = thread index within the group, 0..127).
+// run by the prep group (p = thread index within the group, 0..255).
 //
 // Part 1 (threads p < 64, block b = p / 16, column c = p % 16): the four
 // 16x16 diagonal blocks by right-looking forward substitution; each step
@@ -251,51 +253,40 @@ __device__ __forceinline__ void invert_diag_store(float *M, int p, const float (
     for (int i = 0; i < 16; ++i) M[midx(base + i, base + c)] = x[i];
 }
 
-// Part 2 (all 128 threads): block rows a = 1..3, T_ab = -T_aa sum_{b<=m<a}
-// A_am T_mb for every b < a.  Thread p owns row i = p / 8 of the blocks and
-// columns c0 = p % 8 and c0 + 8, for all b at once (independent
-// accumulators).  A_ab is overwritten only after the block row's products.
+// Part 2 (all 256 threads of the group): block rows a = 1..3,
+// T_ab = -T_aa sum_{b<=m<a} A_am T_mb for every b < a.  Thread pid owns row
+// i = pid / 16 and column c = pid % 16 of the blocks, for all b at once
+// (independent accumulators).  A_ab is overwritten only after the block
+// row's products.
 template <int A_ROW>
-__device__ __forceinline__ void invert_block_row(float *M, float *W, int p) {
-    const int i = (p >> 3) & 15, c0 = p & 7;
+__device__ __forceinline__ void invert_block_row(float *M, float *W, int pid) {
+    const int i = (pid >> 4) & 15, c = pid & 15;
     const int row = A_ROW * 16 + i;
-    float acc[A_ROW][2];
+    float acc[A_ROW];
 #pragma unroll
-    for (int b = 0; b < A_ROW; ++b) acc[b][0] = acc[b][1] = 0.f;
+    for (int b = 0; b < A_ROW; ++b) acc[b] = 0.f;
 #pragma unroll
     for (int m = 0; m < A_ROW; ++m) {
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
             const float av = M[midx(row, m * 16 + k)];
 #pragma unroll
-            for (int b = 0; b <= m; ++b) {
-                acc[b][0] = fmaf(av, M[midx(m * 16 + k, b * 16 + c0)], acc[b][0]);
-                acc[b][1] = fmaf(av, M[midx(m * 16 + k, b * 16 + c0 + 8)], acc[b][1]);
-            }
+            for (int b = 0; b <= m; ++b) acc[b] = fmaf(av, M[midx(m * 16 + k, b * 16 + c)], acc[b]);
         }
     }
 #pragma unroll
-    for (int b = 0; b < A_ROW; ++b) {
-        W[b * 256 + i * 16 + c0] = acc[b][0];
-        W[b * 256 + i * 16 + c0 + 8] = acc[b][1];
-    }
+    for (int b = 0; b < A_ROW; ++b) W[b * 256 + i * 16 + c] = acc[b];
     group_sync(kBarPrep);
 #pragma unroll
-    for (int b = 0; b < A_ROW; ++b) acc[b][0] = acc[b][1] = 0.f;
+    for (int b = 0; b < A_ROW; ++b) acc[b] = 0.f;
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
         const float tv = M[midx(row, A_ROW * 16 + k)];
 #pragma unroll
-        for (int b = 0; b < A_ROW; ++b) {
-            acc[b][0] = fmaf(tv, W[b * 256 + k * 16 + c0], acc[b][0]);
-            acc[b][1] = fmaf(tv, W[b * 256 + k * 16 + c0 + 8], acc[b][1]);
-        }
+        for (int b = 0; b < A_ROW; ++b) acc[b] = fmaf(tv, W[b * 256 + k * 16 + c], acc[b]);
     }
 #pragma unroll
-    for (int b = 0; b < A_ROW; ++b) {
-        M[midx(row, b * 16 + c0)] = -acc[b][0];
-        M[midx(row, b * 16 + c0 + 8)] = -acc[b][1];
-    }
+    for (int b = 0; b < A_ROW; ++b) M[midx(row, b * 16 + c)] = -acc[b];
     group_sync(kBarPrep);
 }
 
@@ -375,18 +366,20 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
     const uint32_t tbase = *tmem_ptr;
     const uint32_t my_lane = lane_addr(tbase, warp, 0);
 
-    if (warp < 4) {
+    if (warp < 8) {
         // ============================ chain group ==============================
-        const int j = tid;  // value column (valid when j < D)
+        // Thread (j, hf): value column j (TMEM lane j), half hf of the row's work.
+        const int j = tid & 127, hf = tid >> 7;
         const int jm = j & (D - 1);
-        // Initial state row j: fp32 into D5, fp16 into the S0^T tile; or, for
-        // an empty sequence, straight to the destination slot.
+        constexpr int kHalfD = D / 2;  // state columns per thread
+        // Initial state row j, columns [hf D/2, (hf+1) D/2): fp32 into D5, fp16
+        // into the S0^T tile; or, for an empty sequence, to the destination.
         if (j < D) {
             const float *sp = src >= 0 ? a.state + ((static_cast<size_t>(src) * a.h_v + h) * D + jm) * D : nullptr;
             float *dp = (Lseq == 0 && dst >= 0) ? a.state + ((static_cast<size_t>(dst) * a.h_v + h) * D + jm) * D
                                                 : nullptr;
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = hf * kHalfD; c0 < (hf + 1) * kHalfD; c0 += 32) {
                 uint32_t r[32];
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
@@ -417,19 +410,22 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
         uint32_t mma_phase = 0;
         bool failed = false;
         int prev_n = 0, prev_tok0 = 0;
+        uint16_t *sOst = reinterpret_cast<uint16_t *>(sVpT);
+        uint16_t *sVst = reinterpret_cast<uint16_t *>(sUT);
 
         // Output of a finished chunk: o_t = scale (gamma_t (Q S0)_t + (P U)_t),
-        // staged as bf16 [t][D] in the V'^T tile (free between S3 of that chunk
-        // and C2 of the next) and stored with 16-byte writes.
-        uint16_t *sOst = reinterpret_cast<uint16_t *>(sVpT);
+        // tokens t = 32 hf .. 32 hf + 31 per thread, staged as bf16 [t][D] in
+        // the V'^T tile (free between S3 of that chunk and C2 of the next) and
+        // stored with 16-byte writes.
         auto output = [&](int buf, int n_out, int tok_out) {
             if (j < D) {
-                float qs[64], pu[64];
-                tmem_load_row<64>(my_lane + kColD1 + 128 * buf, qs);
-                tmem_load_row<64>(my_lane + kColD6, pu);
-                const float *gam = sGamC(buf);
+                float qs[32], pu[32];
+                tmem_load_row<32>(my_lane + kColD1 + 128 * buf + 32 * hf, qs);
+                tmem_load_row<32>(my_lane + kColD6 + 32 * hf, pu);
+                const float *gam = sGamC(buf) + 32 * hf;
 #pragma unroll
-                for (int t = 0; t < 64; ++t) sOst[t * D + jm] = float_to_bf16_bits(a.scale * fmaf(gam[t], qs[t], pu[t]));
+                for (int i = 0; i < 32; ++i)
+                    sOst[(32 * hf + i) * D + jm] = float_to_bf16_bits(a.scale * fmaf(gam[i], qs[i], pu[i]));
             }
             tc::fence_before_sync();
             group_sync(kBarChain);
@@ -448,25 +444,15 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             const uint32_t d1 = tbase + kColD1 + 128 * s;
             const uint32_t d1_lane = my_lane + kColD1 + 128 * s;
 
-            // ---- values of the chunk (independent of the prep group), staged as
-            //      bf16 [t][D] in the U^T tile (free until C4 of this chunk) ----
-            uint16_t *sVst = reinterpret_cast<uint16_t *>(sUT);
-            {
-                constexpr int kPer = 64 * (D / 8) / kGroup;
-                uint4 vv[kPer];
+            // ---- values of the chunk (independent of the prep group) ------------
+            constexpr int kPerV = 64 * (D / 8) / kGroup;
+            uint4 vv[kPerV];
 #pragma unroll
-                for (int it = 0; it < kPer; ++it) {
-                    const int e = tid + it * kGroup;
-                    const int r = e / (D / 8), cc = e % (D / 8);
-                    const size_t row = static_cast<size_t>(tok0 + min(r, n - 1));  // always a row of this chunk
-                    vv[it] = __ldg(reinterpret_cast<const uint4 *>(a.v + row * ldv + static_cast<size_t>(h) * D + cc * 8));
-                }
-#pragma unroll
-                for (int it = 0; it < kPer; ++it) {
-                    const int e = tid + it * kGroup;
-                    const int r = e / (D / 8), cc = e % (D / 8);
-                    *reinterpret_cast<uint4 *>(sVst + r * D + cc * 8) = r < n ? vv[it] : make_uint4(0, 0, 0, 0);
-                }
+            for (int it = 0; it < kPerV; ++it) {
+                const int e = tid + it * kGroup;
+                const int r = e / (D / 8), cc = e % (D / 8);
+                const size_t row = static_cast<size_t>(tok0 + min(r, n - 1));  // always a row of this chunk
+                vv[it] = __ldg(reinterpret_cast<const uint4 *>(a.v + row * ldv + static_cast<size_t>(h) * D + cc * 8));
             }
 
             // ---- wait for the chunk's operands ---------------------------------
@@ -489,6 +475,13 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             }
             __syncwarp();
             if (tid < 64) sGamC(s)[tid & 63] = sGam(s)[tid & 63];  // kept for the output of this chunk
+            // values -> staging tile (the U^T tile is free until C4 of this chunk)
+#pragma unroll
+            for (int it = 0; it < kPerV; ++it) {
+                const int e = tid + it * kGroup;
+                const int r = e / (D / 8), cc = e % (D / 8);
+                *reinterpret_cast<uint4 *>(sVst + r * D + cc * 8) = r < n ? vv[it] : make_uint4(0, 0, 0, 0);
+            }
 
             // ---- output of the previous chunk while S1 runs ---------------------
             if (c > 0) output(s ^ 1, prev_n, prev_tok0);
@@ -502,13 +495,14 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             }
             tc::fence_after_sync();
             if (j < D) {
-                float ks[64];
-                tmem_load_row<64>(d1_lane + 64, ks);
-                const float *gam = sGam(s);
+                float ks[32];
+                tmem_load_row<32>(d1_lane + 64 + 32 * hf, ks);
+                const float *gam = sGam(s) + 32 * hf;
 #pragma unroll
-                for (int t = 0; t < 64; ++t)
-                    ks[t] = __uint_as_float(static_cast<uint32_t>(sVst[t * D + jm]) << 16) - gam[t] * ks[t];
-                store_row64_f16(sVpT, 128, jm, ks);
+                for (int i = 0; i < 32; ++i)
+                    ks[i] = __uint_as_float(static_cast<uint32_t>(sVst[(32 * hf + i) * D + jm]) << 16) - gam[i] * ks[i];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) store_chunk8_f16(sVpT, 128, jm, 4 * hf + q, ks + 8 * q);
             }
             tc::fence_proxy_async_smem();
             tc::fence_before_sync();
@@ -524,7 +518,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             if (j < D) {  // gamma_C scales the state while S3 runs
                 const float gC = sGam(s)[63];
 #pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 32) {
+                for (int c0 = hf * kHalfD; c0 < (hf + 1) * kHalfD; c0 += 32) {
                     uint32_t r[32];
                     tc::tmem_ld32(my_lane + kColD5 + c0, r);
 #pragma unroll
@@ -543,9 +537,10 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             }
             tc::fence_after_sync();
             if (j < D) {
-                float u[64];
-                tmem_load_row<64>(d1_lane + 64, u);
-                store_row64_f16(sUT, 128, jm, u);
+                float u[32];
+                tmem_load_row<32>(d1_lane + 64 + 32 * hf, u);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) store_chunk8_f16(sUT, 128, jm, 4 * hf + q, u + 8 * q);
             }
             tc::fence_proxy_async_smem();
             tc::fence_before_sync();
@@ -582,7 +577,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                                 ? a.state + ((static_cast<size_t>(dst) * a.h_v + h) * D + jm) * D
                                 : nullptr;
 #pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 32) {
+                for (int c0 = hf * kHalfD; c0 < (hf + 1) * kHalfD; c0 += 32) {
                     uint32_t r[32];
                     tc::tmem_ld32(my_lane + kColD5 + c0, r);
                     store_f16_chunks32(sS0T, jm, c0, r);
@@ -613,7 +608,9 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
         }
     } else {
         // ============================= prep group ==============================
-        const int p = tid - kGroup;  // 0..127, TMEM lane p
+        // Thread (p, hf): TMEM lane / Gram row p, half hf of the row's work.
+        const int pid = tid - kGroup;  // 0..255
+        const int p = pid & 127, hf = pid >> 7;
         bool failed = false;
         const uint32_t aIdGram = tc::idesc_f16_f32acc(128, 64);
         for (int c = 0; c < n_chunks; ++c) {
@@ -631,8 +628,8 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             uint8_t *qk = sQK(s);
             {
                 float gv = 0.f, bv = 0.f;
-                const int t = p & 63;
-                if (p < 64) {
+                const int t = pid & 63;
+                if (pid < 64) {
                     const size_t gi = static_cast<size_t>(tok0 + min(t, n - 1)) * a.h_v + h;
                     gv = a.g[gi];
                     bv = a.beta[gi];
@@ -641,15 +638,25 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 uint4 qv[kPer], kv[kPer];
 #pragma unroll
                 for (int it = 0; it < kPer; ++it) {
-                    const int e = p + it * kGroup;
+                    const int e = pid + it * kGroup;
                     const int r = e / (D / 8), cc = e % (D / 8);
                     const size_t row = static_cast<size_t>(tok0 + min(r, n - 1));  // always a row of this chunk
                     qv[it] = __ldg(reinterpret_cast<const uint4 *>(a.q + row * ldq + kh * D + cc * 8));
                     kv[it] = __ldg(reinterpret_cast<const uint4 *>(a.k + row * ldq + kh * D + cc * 8));
                 }
+                if (c + 1 < n_chunks && pid < 128) {  // the next chunk's q, k rows into L2
+                    const int rn = min(kChunk, Lseq - (c + 1) * kChunk);
+                    const int r = pid & 63;
+                    if (r < rn) {
+                        const size_t row = static_cast<size_t>(tok0 + kChunk + r);
+                        const uint16_t *src_row = (pid < 64 ? a.q : a.k) + row * ldq + kh * D;
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(src_row) : "memory");
+                        if (D > 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(src_row + 64) : "memory");
+                    }
+                }
 #pragma unroll
                 for (int it = 0; it < kPer; ++it) {
-                    const int e = p + it * kGroup;
+                    const int e = pid + it * kGroup;
                     const int r = e / (D / 8), cc = e % (D / 8);
                     const uint4 z = make_uint4(0, 0, 0, 0);
                     *reinterpret_cast<uint4 *>(qk + tc::sw128_chunk_offset(r, cc, 128)) =
@@ -657,24 +664,14 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                     *reinterpret_cast<uint4 *>(qk + tc::sw128_chunk_offset(64 + r, cc, 128)) =
                         r < n ? bf16x8_to_f16x8(kv[it]) : z;
                 }
-                if (p < 64) {
+                if (pid < 64) {
                     sGraw[t] = t < n ? gv : 0.f;
                     sBeta[t] = t < n ? bv : 0.f;
                 }
             }
-            if (c + 1 < n_chunks) {  // the next chunk's q, k rows into L2
-                const int rn = min(kChunk, Lseq - (c + 1) * kChunk);
-                const int r = p & 63;
-                if (r < rn) {
-                    const size_t row = static_cast<size_t>(tok0 + kChunk + r);
-                    const uint16_t *src_row = (p < 64 ? a.q : a.k) + row * ldq + kh * D;
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(src_row) : "memory");
-                    if (D > 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(src_row + 64) : "memory");
-                }
-            }
             group_sync(kBarPrep);
-            if (p < 32) {  // inclusive prefix sum of g over the chunk, fixed order
-                const int l = p & 31;
+            if (pid < 32) {  // inclusive prefix sum of g over the chunk, fixed order
+                const int l = pid & 31;
                 const float g0 = sGraw[2 * l], g1 = sGraw[2 * l + 1];
                 const float pair = g0 + g1;
                 float incl = pair;
@@ -688,8 +685,8 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 sG[2 * l + 1] = excl + g0 + g1;
             }
             group_sync(kBarPrep);
-            if (p < 64) {
-                const int t = p & 63;
+            if (pid < 64) {
+                const int t = pid & 63;
                 sGam(s)[t] = expf(sG[t]);
                 sDec[t] = expf(sG[63] - sG[t]);
             }
@@ -698,7 +695,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             group_sync(kBarPrep);
 
             // ---- Gram [Q;K] K^T --------------------------------------------------------
-            if (p == 0) {
+            if (pid == 0) {
                 tc::fence_after_sync();
                 const uint64_t dQK = tc::desc_k_sw128(tc::smem_u32(qk));
 #pragma unroll
@@ -717,75 +714,76 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             }
             tc::fence_after_sync();
 
-            // ---- P rows (lanes 0..63) and A rows (lanes 64..127) -------------------
+            // ---- P rows (lanes 0..63) and A rows (lanes 64..127), columns 32 hf.. ----
             {
-                float x[64];
-                tmem_load_row<64>(my_lane + kColGram, x);
+                float x[32];
+                tmem_load_row<32>(my_lane + kColGram + 32 * hf, x);
                 const int r = p & 63;
                 const float Gr = sG[r];
 #pragma unroll
-                for (int q4 = 0; q4 < 64; q4 += 4) {
-                    const float4 g4 = *reinterpret_cast<const float4 *>(sG + q4);
-                    x[q4 + 0] = (q4 + 0 <= r) ? __expf(Gr - g4.x) * x[q4 + 0] : 0.f;
-                    x[q4 + 1] = (q4 + 1 <= r) ? __expf(Gr - g4.y) * x[q4 + 1] : 0.f;
-                    x[q4 + 2] = (q4 + 2 <= r) ? __expf(Gr - g4.z) * x[q4 + 2] : 0.f;
-                    x[q4 + 3] = (q4 + 3 <= r) ? __expf(Gr - g4.w) * x[q4 + 3] : 0.f;
+                for (int q4 = 0; q4 < 32; q4 += 4) {
+                    const int q0 = 32 * hf + q4;
+                    const float4 g4 = *reinterpret_cast<const float4 *>(sG + q0);
+                    x[q4 + 0] = (q0 + 0 <= r) ? __expf(Gr - g4.x) * x[q4 + 0] : 0.f;
+                    x[q4 + 1] = (q0 + 1 <= r) ? __expf(Gr - g4.y) * x[q4 + 1] : 0.f;
+                    x[q4 + 2] = (q0 + 2 <= r) ? __expf(Gr - g4.z) * x[q4 + 2] : 0.f;
+                    x[q4 + 3] = (q0 + 3 <= r) ? __expf(Gr - g4.w) * x[q4 + 3] : 0.f;
                 }
                 if (p < 64) {
-                    store_row64_f16(sP(s), 64, r, x);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) store_chunk8_f16(sP(s), 64, r, 4 * hf + q, x + 8 * q);
                 } else {
                     const float br = sBeta[r];
 #pragma unroll
-                    for (int q = 0; q < 64; ++q) sM[midx(r, q)] = (q < r) ? br * x[q] : 0.f;
+                    for (int q = 0; q < 32; ++q) sM[midx(r, 32 * hf + q)] = (32 * hf + q < r) ? br * x[q] : 0.f;
                 }
             }
             tc::fence_before_sync();
             group_sync(kBarPrep);
 
-            // ---- T = (I + A)^-1 (diagonal blocks) || Ktil^T rows 0..63 --------------
+            // ---- T = (I + A)^-1 (diagonal blocks) || Ktil^T --------------------------
             float xd[16];
-            if (p < 64) {
-                invert_diag_solve(sM, p, xd);
+            if (pid < 64) {
+                invert_diag_solve(sM, pid, xd);
             } else {
-                const int i = p & 63;
-                float x[64];
+                // Ktil^T[i][t] = exp(G_C - G_t) k_t[i]: items (row i, 16 tokens)
+                for (int e = pid - 64; e < D * 4; e += kGroup - 64) {
+                    const int i = (e >> 2) & (D - 1), quarter = e & 3;
+                    float x[16];
 #pragma unroll
-                for (int t = 0; t < 64; ++t) {
-                    const uint16_t kb = *reinterpret_cast<const uint16_t *>(qk + tc::sw128_offset(64 + t, i, 128));
-                    x[t] = sDec[t] * half_bits_to_float(kb);
+                    for (int u = 0; u < 16; ++u) {
+                        const int t = quarter * 16 + u;
+                        const uint16_t kb = *reinterpret_cast<const uint16_t *>(qk + tc::sw128_offset(64 + t, i, 128));
+                        x[u] = sDec[t] * half_bits_to_float(kb);
+                    }
+                    store_chunk8_f16(sKtT(s), D, i, 2 * quarter, x);
+                    store_chunk8_f16(sKtT(s), D, i, 2 * quarter + 1, x + 8);
                 }
-                store_row64_f16(sKtT(s), D, i, x);
             }
             group_sync(kBarPrep);
-            if (p < 64) invert_diag_store(sM, p, xd);
+            if (pid < 64) invert_diag_store(sM, pid, xd);
             group_sync(kBarPrep);
-            invert_block_row<1>(sM, sW, p);
-            invert_block_row<2>(sM, sW, p);
-            invert_block_row<3>(sM, sW, p);
+            invert_block_row<1>(sM, sW, pid);
+            invert_block_row<2>(sM, sW, pid);
+            invert_block_row<3>(sM, sW, pid);
 
-            // ---- T'' = T diag(beta) (rows 0..63) || Ktil^T rows 64..127 ---------------
-            if (p >= 64) {
-                const int t = p & 63;
-                float x[64];
+            // ---- T'' = T diag(beta): items (row t, 16 columns) ------------------------
+            {
+                const int t = (pid >> 2) & 63, quarter = pid & 3;
+                float x[16];
 #pragma unroll
-                for (int q = 0; q < 64; ++q) x[q] = (q <= t) ? sM[midx(t, q)] * sBeta[q] : 0.f;
-                store_row64_f16(sTpp(s), 64, t, x);
-            } else if (D > 64) {
-                const int i = 64 + (p & 63);
-                float x[64];
-#pragma unroll
-                for (int t = 0; t < 64; ++t) {
-                    const uint16_t kb =
-                        *reinterpret_cast<const uint16_t *>(qk + tc::sw128_offset(64 + t, i & (D - 1), 128));
-                    x[t] = sDec[t] * half_bits_to_float(kb);
+                for (int u = 0; u < 16; ++u) {
+                    const int q = quarter * 16 + u;
+                    x[u] = (q <= t) ? sM[midx(t, q)] * sBeta[q] : 0.f;
                 }
-                store_row64_f16(sKtT(s), D, i & (D - 1), x);
+                store_chunk8_f16(sTpp(s), 64, t, 2 * quarter, x);
+                store_chunk8_f16(sTpp(s), 64, t, 2 * quarter + 1, x + 8);
             }
             tc::fence_proxy_async_smem();
             mbar_arrive(ready + s);
             group_sync(kBarPrep);  // scratch reuse by the next chunk
         }
-        if (failed && p == 0) {
+        if (failed && pid == 0) {
             report(a.dev_status, GDN_DEV_TIMEOUT);
             atomicExch(fail, 1);
         }
