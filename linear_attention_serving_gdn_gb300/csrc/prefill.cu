@@ -88,8 +88,8 @@ struct Smem {
     static constexpr uint32_t kGam0 = kUT + 16384;             // f32 [64] exp(G_t), stage 0
     static constexpr uint32_t kGam1 = kGam0 + 256;
     static constexpr uint32_t kGamC = kGam1 + 256;             // f32 [2][64] chain group's copies
-    static constexpr uint32_t kM = kGamC + 512;                // f32 [64][64] A, then T (rotated rows)
-    static constexpr uint32_t kW = kM + 16384;                 // f32 [3][16][16] block products
+    static constexpr uint32_t kM = kGamC + 512;                // f32 [64][kLdM] A, then T
+    static constexpr uint32_t kW = kM + 64 * 68 * 4;           // f32 [3][16][16] block products
     static constexpr uint32_t kG = kW + 3072;                  // f32 [64] cumulative log decay
     static constexpr uint32_t kBeta = kG + 256;                // f32 [64]
     static constexpr uint32_t kGraw = kBeta + 256;             // f32 [64]
@@ -103,6 +103,7 @@ struct Smem {
     static_assert(kS0T % 1024 == 0 && kVpT % 1024 == 0 && kUT % 1024 == 0 && kKtT0 % 1024 == 0, "");
     static_assert(kKtT1 % 1024 == 0 && kBars % 8 == 0, "");
     static_assert(kTpp0 % 1024 == 0 && kP0 % 1024 == 0 && kQK1 % 1024 == 0, "");
+    static_assert(kM % 16 == 0 && kW % 16 == 0, "float4 access to the scratch");
     static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
@@ -205,9 +206,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return true;
 }
 
-// Rotated row layout of the 64x64 fp32 scratch: conflict-free for row and
-// column walks.
-__device__ __forceinline__ int midx(int r, int c) { return r * 64 + ((c + r) & 63); }
+// Row stride of the 64x64 fp32 scratch: 68 floats keep 16-byte alignment and
+// put 8 consecutive rows on disjoint bank quads.
+constexpr int kLdM = 68;
 
 // Sum over s' < s of floor(L_s' / (64 E)), by the whole block.
 __device__ int64_t emit_offset(const int32_t *cu, int s, int E, long long *part) {
@@ -225,8 +226,9 @@ __device__ int64_t emit_offset(const int32_t *cu, int s, int E, long long *part)
 }
 
 // In place, M := (I + M)^-1 for a 64x64 strictly lower-triangular M (the
-// diagonal of M is ignored and the result has unit diagonal), in two parts
-// run by the prep group (p = thread index within the group, 0..255).
+// diagonal and upper triangle of M are ignored; the result has unit diagonal
+// and zeros above it inside the diagonal blocks), in two parts run by the
+// prep group (p = thread index within the group, 0..255).
 //
 // Part 1 (threads p < 64, block b = p / 16, column c = p % 16): the four
 // 16x16 diagonal blocks by right-looking forward substitution; each step
@@ -243,50 +245,63 @@ __device__ __forceinline__ void invert_diag_solve(const float *M, int p, float (
         const float xj = (j < c) ? 0.f : (j == c ? 1.f : -acc[j]);
         x[j] = xj;
 #pragma unroll
-        for (int i = j + 1; i < 16; ++i) acc[i] = fmaf(M[midx(base + i, base + j)], xj, acc[i]);
+        for (int i = j + 1; i < 16; ++i) acc[i] = fmaf(M[(base + i) * kLdM + base + j], xj, acc[i]);
     }
 }
 
 __device__ __forceinline__ void invert_diag_store(float *M, int p, const float (&x)[16]) {
     const int c = p & 15, base = ((p >> 4) & 3) * 16;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) M[midx(base + i, base + c)] = x[i];
+    for (int i = 0; i < 16; ++i) M[(base + i) * kLdM + base + c] = x[i];
 }
 
-// Part 2 (all 256 threads of the group): block rows a = 1..3,
-// T_ab = -T_aa sum_{b<=m<a} A_am T_mb for every b < a.  Thread pid owns row
-// i = pid / 16 and column c = pid % 16 of the blocks, for all b at once
-// (independent accumulators).  A_ab is overwritten only after the block
-// row's products.
+__device__ __forceinline__ void fma4(float4 &acc, float a, const float4 &t) {
+    acc.x = fmaf(a, t.x, acc.x);
+    acc.y = fmaf(a, t.y, acc.y);
+    acc.z = fmaf(a, t.z, acc.z);
+    acc.w = fmaf(a, t.w, acc.w);
+}
+
+// Part 2: block rows a = 1..3, T_ab = -T_aa sum_{b<=m<a} A_am T_mb for every
+// b < a.  Thread p < 64 a owns block b = p / 64, row i = (p / 4) % 16 and the
+// four columns 4 (p % 4) .. + 3 of T_ab (float4 accesses; b is uniform over a
+// warp).  A_ab is overwritten only after the block row's products.
 template <int A_ROW>
-__device__ __forceinline__ void invert_block_row(float *M, float *W, int pid) {
-    const int i = (pid >> 4) & 15, c = pid & 15;
+__device__ __forceinline__ void invert_block_row(float *M, float *W, int p) {
+    const int b = min((p >> 6) & 3, A_ROW - 1), i = (p >> 2) & 15, cq = p & 3;  // b < A_ROW for every p
     const int row = A_ROW * 16 + i;
-    float acc[A_ROW];
+    const bool active = p < A_ROW * 64;
+    if (active) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int b = 0; b < A_ROW; ++b) acc[b] = 0.f;
+        for (int m = 0; m < A_ROW; ++m) {
+            if (m < b) continue;
 #pragma unroll
-    for (int m = 0; m < A_ROW; ++m) {
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float av = M[midx(row, m * 16 + k)];
-#pragma unroll
-            for (int b = 0; b <= m; ++b) acc[b] = fmaf(av, M[midx(m * 16 + k, b * 16 + c)], acc[b]);
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(M + row * kLdM + m * 16 + 4 * k4);
+                const float *t = M + (m * 16 + 4 * k4) * kLdM + b * 16 + 4 * cq;
+                fma4(acc, a4.x, *reinterpret_cast<const float4 *>(t));
+                fma4(acc, a4.y, *reinterpret_cast<const float4 *>(t + kLdM));
+                fma4(acc, a4.z, *reinterpret_cast<const float4 *>(t + 2 * kLdM));
+                fma4(acc, a4.w, *reinterpret_cast<const float4 *>(t + 3 * kLdM));
+            }
         }
+        *reinterpret_cast<float4 *>(W + (b * 16 + i) * 16 + 4 * cq) = acc;
     }
-#pragma unroll
-    for (int b = 0; b < A_ROW; ++b) W[b * 256 + i * 16 + c] = acc[b];
     group_sync(kBarPrep);
+    if (active) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int b = 0; b < A_ROW; ++b) acc[b] = 0.f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        const float tv = M[midx(row, A_ROW * 16 + k)];
-#pragma unroll
-        for (int b = 0; b < A_ROW; ++b) acc[b] = fmaf(tv, W[b * 256 + k * 16 + c], acc[b]);
+        for (int k4 = 0; k4 < 4; ++k4) {
+            const float4 t4 = *reinterpret_cast<const float4 *>(M + row * kLdM + A_ROW * 16 + 4 * k4);
+            const float *w = W + (b * 16 + 4 * k4) * 16 + 4 * cq;
+            fma4(acc, t4.x, *reinterpret_cast<const float4 *>(w));
+            fma4(acc, t4.y, *reinterpret_cast<const float4 *>(w + 16));
+            fma4(acc, t4.z, *reinterpret_cast<const float4 *>(w + 32));
+            fma4(acc, t4.w, *reinterpret_cast<const float4 *>(w + 48));
+        }
+        *reinterpret_cast<float4 *>(M + row * kLdM + b * 16 + 4 * cq) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
-#pragma unroll
-    for (int b = 0; b < A_ROW; ++b) M[midx(row, b * 16 + c)] = -acc[b];
     group_sync(kBarPrep);
 }
 
@@ -613,10 +628,32 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
         const int p = pid & 127, hf = pid >> 7;
         bool failed = false;
         const uint32_t aIdGram = tc::idesc_f16_f32acc(128, 64);
+        // q, k, g, beta of a chunk into registers.
+        constexpr int kPer = 64 * (D / 8) / kGroup;  // 16-byte chunks per thread per tile
+        uint4 qv[kPer], kv[kPer];
+        float gv = 0.f, bv = 0.f;
+        auto load_chunk = [&](int cc) {
+            const int tk = t0 + cc * kChunk;
+            const int nn = min(kChunk, Lseq - cc * kChunk);
+            if (pid < 64) {
+                const size_t gi = static_cast<size_t>(tk + min(pid & 63, nn - 1)) * a.h_v + h;
+                gv = a.g[gi];
+                bv = a.beta[gi];
+            }
+#pragma unroll
+            for (int it = 0; it < kPer; ++it) {
+                const int e = pid + it * kGroup;
+                const int r = e / (D / 8), c8 = e % (D / 8);
+                const size_t row = static_cast<size_t>(tk + min(r, nn - 1));  // always a row of that chunk
+                qv[it] = __ldg(reinterpret_cast<const uint4 *>(a.q + row * ldq + kh * D + c8 * 8));
+                kv[it] = __ldg(reinterpret_cast<const uint4 *>(a.k + row * ldq + kh * D + c8 * 8));
+            }
+        };
         for (int c = 0; c < n_chunks; ++c) {
             const int s = c & 1;
             const int tok0 = t0 + c * kChunk;
             const int n = min(kChunk, Lseq - c * kChunk);
+            load_chunk(c);  // issued before the wait for the stage
             if (c >= 2) {
                 const bool ok = mbar_wait_bounded(freeb + s, ((c - 2) >> 1) & 1);
                 if (group_any(kBarPrep, !ok)) {
@@ -627,24 +664,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             // ---- q, k as fp16 operand tiles; g, beta ----------------------------------
             uint8_t *qk = sQK(s);
             {
-                float gv = 0.f, bv = 0.f;
-                const int t = pid & 63;
-                if (pid < 64) {
-                    const size_t gi = static_cast<size_t>(tok0 + min(t, n - 1)) * a.h_v + h;
-                    gv = a.g[gi];
-                    bv = a.beta[gi];
-                }
-                constexpr int kPer = 64 * (D / 8) / kGroup;  // 16-byte chunks per thread per tile
-                uint4 qv[kPer], kv[kPer];
-#pragma unroll
-                for (int it = 0; it < kPer; ++it) {
-                    const int e = pid + it * kGroup;
-                    const int r = e / (D / 8), cc = e % (D / 8);
-                    const size_t row = static_cast<size_t>(tok0 + min(r, n - 1));  // always a row of this chunk
-                    qv[it] = __ldg(reinterpret_cast<const uint4 *>(a.q + row * ldq + kh * D + cc * 8));
-                    kv[it] = __ldg(reinterpret_cast<const uint4 *>(a.k + row * ldq + kh * D + cc * 8));
-                }
-                if (c + 1 < n_chunks && pid < 128) {  // the next chunk's q, k rows into L2
+                if (c + 1 < n_chunks && pid < 128) {  // q, k rows of the next chunk into L2
                     const int rn = min(kChunk, Lseq - (c + 1) * kChunk);
                     const int r = pid & 63;
                     if (r < rn) {
@@ -657,14 +677,15 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
 #pragma unroll
                 for (int it = 0; it < kPer; ++it) {
                     const int e = pid + it * kGroup;
-                    const int r = e / (D / 8), cc = e % (D / 8);
+                    const int r = e / (D / 8), c8 = e % (D / 8);
                     const uint4 z = make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4 *>(qk + tc::sw128_chunk_offset(r, cc, 128)) =
+                    *reinterpret_cast<uint4 *>(qk + tc::sw128_chunk_offset(r, c8, 128)) =
                         r < n ? bf16x8_to_f16x8(qv[it]) : z;
-                    *reinterpret_cast<uint4 *>(qk + tc::sw128_chunk_offset(64 + r, cc, 128)) =
+                    *reinterpret_cast<uint4 *>(qk + tc::sw128_chunk_offset(64 + r, c8, 128)) =
                         r < n ? bf16x8_to_f16x8(kv[it]) : z;
                 }
                 if (pid < 64) {
+                    const int t = pid & 63;
                     sGraw[t] = t < n ? gv : 0.f;
                     sBeta[t] = t < n ? bv : 0.f;
                 }
@@ -715,7 +736,16 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             tc::fence_after_sync();
 
             // ---- P rows (lanes 0..63) and A rows (lanes 64..127), columns 32 hf.. ----
-            {
+            // Rows 0..31 x columns 32..63 are masked (warp-uniform): P gets zeros,
+            // the upper triangle of A is never read.
+            if (hf == 1 && (p & 32) == 0) {
+                if (p < 64) {
+                    const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int q = 4; q < 8; ++q)
+                        *reinterpret_cast<uint4 *>(sP(s) + tc::sw128_chunk_offset(p & 63, q, 64)) = z;
+                }
+            } else {
                 float x[32];
                 tmem_load_row<32>(my_lane + kColGram + 32 * hf, x);
                 const int r = p & 63;
@@ -735,7 +765,12 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 } else {
                     const float br = sBeta[r];
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) sM[midx(r, 32 * hf + q)] = (32 * hf + q < r) ? br * x[q] : 0.f;
+                    for (int q = 0; q < 32; q += 4) {
+                        const int q0 = 32 * hf + q;
+                        *reinterpret_cast<float4 *>(sM + r * kLdM + q0) =
+                            make_float4(q0 + 0 < r ? br * x[q + 0] : 0.f, q0 + 1 < r ? br * x[q + 1] : 0.f,
+                                        q0 + 2 < r ? br * x[q + 2] : 0.f, q0 + 3 < r ? br * x[q + 3] : 0.f);
+                    }
                 }
             }
             tc::fence_before_sync();
@@ -746,18 +781,19 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             if (pid < 64) {
                 invert_diag_solve(sM, pid, xd);
             } else {
-                // Ktil^T[i][t] = exp(G_C - G_t) k_t[i]: items (row i, 16 tokens)
-                for (int e = pid - 64; e < D * 4; e += kGroup - 64) {
-                    const int i = (e >> 2) & (D - 1), quarter = e & 3;
-                    float x[16];
+                // Ktil^T[i][t] = exp(G_C - G_t) k_t[i]: items (row i, 32 tokens); the
+                // lanes of a warp read consecutive i of one k row.
+                for (int e = pid - 64; e < D * 2; e += kGroup - 64) {
+                    const int i = e & (D - 1), half = (e / D) & 1;
+                    float x[32];
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const int t = quarter * 16 + u;
+                    for (int u = 0; u < 32; ++u) {
+                        const int t = half * 32 + u;
                         const uint16_t kb = *reinterpret_cast<const uint16_t *>(qk + tc::sw128_offset(64 + t, i, 128));
                         x[u] = sDec[t] * half_bits_to_float(kb);
                     }
-                    store_chunk8_f16(sKtT(s), D, i, 2 * quarter, x);
-                    store_chunk8_f16(sKtT(s), D, i, 2 * quarter + 1, x + 8);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) store_chunk8_f16(sKtT(s), D, i, 4 * half + q, x + 8 * q);
                 }
             }
             group_sync(kBarPrep);
@@ -772,9 +808,14 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 const int t = (pid >> 2) & 63, quarter = pid & 3;
                 float x[16];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
+                for (int u = 0; u < 16; u += 4) {
                     const int q = quarter * 16 + u;
-                    x[u] = (q <= t) ? sM[midx(t, q)] * sBeta[q] : 0.f;
+                    const float4 m4 = *reinterpret_cast<const float4 *>(sM + t * kLdM + q);
+                    const float4 b4 = *reinterpret_cast<const float4 *>(sBeta + q);
+                    x[u + 0] = (q + 0 <= t) ? m4.x * b4.x : 0.f;
+                    x[u + 1] = (q + 1 <= t) ? m4.y * b4.y : 0.f;
+                    x[u + 2] = (q + 2 <= t) ? m4.z * b4.z : 0.f;
+                    x[u + 3] = (q + 3 <= t) ? m4.w * b4.w : 0.f;
                 }
                 store_chunk8_f16(sTpp(s), 64, t, 2 * quarter, x);
                 store_chunk8_f16(sTpp(s), 64, t, 2 * quarter + 1, x + 8);
