@@ -296,12 +296,12 @@ def mixed_case(torch, gdn, dev, reps):
             "tokens_per_s": (nd + pre.total_tokens) / (ms * 1e-3)}
 
 
-def run_extra(torch, gdn, dev, wanted, peaks):
+def run_extra(torch, gdn, dev, wanted, peaks, prefix_seqlen=32768):
     extra = []
     if "prefill" in wanted:
         extra.append(prefill_case(torch, gdn, gi.prefill_qwen3next_gva(0), dev, reps=5))
     if "prefix" in wanted:
-        extra.append(prefill_case(torch, gdn, gi.prefix_cache_prefill(0), dev, reps=3, E=17))
+        extra.append(prefill_case(torch, gdn, gi.prefix_cache_prefill(0, seqlen=prefix_seqlen), dev, reps=3, E=17))
     if "mixed" in wanted:
         extra.append(mixed_case(torch, gdn, dev, reps=5))
     for x in extra:
@@ -413,6 +413,8 @@ def main():
     ap.add_argument("--workloads", default="decode,prefill,prefix,mixed",
                     help="comma list of decode (headline), prefill, prefix, mixed")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefix-seqlen", type=int, default=32768,
+                    help="tokens per sequence of the prefix-cache workload (smaller for profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -436,7 +438,7 @@ def main():
     if args.no_extra:
         wanted &= {"decode"}
     if "decode" not in wanted:
-        extra = run_extra(torch, gdn, dev, wanted, load_peaks())
+        extra = run_extra(torch, gdn, dev, wanted, load_peaks(), args.prefix_seqlen)
         if rank == 0:
             print(json.dumps({"metric": "GDN prefill tokens/s", "workloads": extra}), flush=True)
         return
@@ -473,7 +475,7 @@ def main():
         "clocks": clocks,
     }
     if wanted - {"decode"}:
-        line["workloads"] = run_extra(torch, gdn, dev, wanted, peaks)
+        line["workloads"] = run_extra(torch, gdn, dev, wanted, peaks, args.prefix_seqlen)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:

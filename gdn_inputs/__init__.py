@@ -184,5 +184,5 @@ def prefix_cache_prefill(seed: int = 0, n_seq: int = 4, seqlen: int = 32768) -> 
     """Prefix-cache prefill with state emission on the 1088-token block grid:
     4 sequences of 32768 tokens, H_k=16, H_v=32, d=128, E=17 chunks."""
     b = token_batch([seqlen] * n_seq, 16, 32, 128, seed, init_state=False)
-    return {"name": "prefix_cache_4x32768_hk16_hv32_d128_E17", "prefill": b,
+    return {"name": f"prefix_cache_{n_seq}x{seqlen}_hk16_hv32_d128_E17", "prefill": b,
             "emit_every_chunks": 17}
