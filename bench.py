@@ -281,19 +281,78 @@ def mixed_case(torch, gdn, dev, reps):
     def call():
         gdn.gdn_mixed_step(nd, q, k, v, g, beta, cu, cu_h, cache, slots[:nd], o, pre_dst_slot=slots[nd:])
 
-    call()
-    torch.cuda.synchronize()
-    ev = []
-    for _ in range(reps):
-        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        call()
-        z.record()
-        ev.append((a, z))
-    torch.cuda.synchronize()
-    ms = statistics.median(a.elapsed_time(z) for a, z in ev)
+    s_dec, s_pre = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def colaunch():
+        # decode rows and prefills on two streams at once (same kernels)
+        main = torch.cuda.current_stream()
+        s_dec.wait_stream(main)
+        s_pre.wait_stream(main)
+        with torch.cuda.stream(s_dec):
+            gdn.gdn_decode_packed(q[:nd], k[:nd], v[:nd], g[:nd], beta[:nd], cache, slots[:nd], o[:nd])
+        with torch.cuda.stream(s_pre):
+            gdn.gdn_prefill_varlen(q[nd:], k[nd:], v[nd:], g[nd:], beta[nd:], cu, cu_h, o[nd:], state=cache,
+                                   dst_slot=slots[nd:])
+        main.wait_stream(s_dec)
+        main.wait_stream(s_pre)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        ev = []
+        for _ in range(reps):
+            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            z.record()
+            ev.append((a, z))
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(z) for a, z in ev)
+
+    ms = timed(call)
+    ms2 = timed(colaunch)
     return {"workload": wl["name"], "decode_rows": nd, "prefill_seqlens": pre.seqlens, "ms": ms,
-            "tokens_per_s": (nd + pre.total_tokens) / (ms * 1e-3)}
+            "tokens_per_s": (nd + pre.total_tokens) / (ms * 1e-3), "colaunch_two_streams_ms": ms2}
+
+
+def decode_latency_case(torch, gdn, dev, rows_list=(1, 8, 64, 256), iters=200):
+    """Decode step latency per padded batch size: eager C-ABI calls from
+    Python versus replay of a CUDA graph holding one step (H=16, d=128)."""
+    cases = []
+    for rows in rows_list:
+        b = gi.token_batch([1] * rows, H, H, D, 5, init_state=True)
+        src, n_slots = gi.slots(rows, 5)
+        cache = torch.zeros((n_slots, H, D, D), dtype=torch.float32, device=dev)
+        cache[torch.from_numpy(src.astype(np.int64)).to(dev)] = \
+            torch.from_numpy(np.swapaxes(b.init_state, -1, -2).copy()).to(dev)
+        q, k, v = bf16(torch, b.q, dev), bf16(torch, b.k, dev), bf16(torch, b.v, dev)
+        g, beta = torch.from_numpy(b.g).to(dev), torch.from_numpy(b.beta).to(dev)
+        src_t = torch.from_numpy(src).to(dev)
+        o = torch.empty((rows, H, D), dtype=torch.bfloat16, device=dev)
+
+        def call():
+            gdn.gdn_decode_packed(q, k, v, g, beta, cache, src_t, o)
+
+        def per_step_us(fn):
+            for _ in range(5):
+                fn()
+            torch.cuda.synchronize()
+            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(iters):
+                fn()
+            z.record()
+            torch.cuda.synchronize()
+            return a.elapsed_time(z) * 1e3 / iters
+
+        eager = per_step_us(call)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            call()
+        replay = per_step_us(graph.replay)
+        cases.append({"rows": rows, "eager_us_per_step": eager, "graph_us_per_step": replay,
+                      "graph_rows_per_s": rows / (replay * 1e-6)})
+    return {"workload": "decode_latency_h16_d128", "cases": cases}
 
 
 def run_extra(torch, gdn, dev, wanted, peaks, prefix_seqlen=32768):
@@ -304,6 +363,8 @@ def run_extra(torch, gdn, dev, wanted, peaks, prefix_seqlen=32768):
         extra.append(prefill_case(torch, gdn, gi.prefix_cache_prefill(0, seqlen=prefix_seqlen), dev, reps=3, E=17))
     if "mixed" in wanted:
         extra.append(mixed_case(torch, gdn, dev, reps=5))
+    if "graph" in wanted:
+        extra.append(decode_latency_case(torch, gdn, dev))
     for x in extra:
         if "algorithmic_tflops" in x:
             x["roofline"] = {"bound": "tensor", "kernel": "prefill_chunk_tc_kernel<128>",
@@ -410,8 +471,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the prefill/mixed workloads")
-    ap.add_argument("--workloads", default="decode,prefill,prefix,mixed",
-                    help="comma list of decode (headline), prefill, prefix, mixed")
+    ap.add_argument("--workloads", default="decode,prefill,prefix,mixed,graph",
+                    help="comma list of decode (headline), prefill, prefix, mixed, graph (decode latency)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefix-seqlen", type=int, default=32768,
                     help="tokens per sequence of the prefix-cache workload (smaller for profiling captures)")

@@ -107,6 +107,40 @@ gdn_status_t gdn_decode_packed(const gdn_dims_t *dims, int32_t num_rows,
                                gdn_bf16 *o, int32_t *dev_status, void *stream);
 
 /*
+ * Multi-token decode: tokens_per_row consecutive tokens per cached row, as a
+ * speculative-decoding verifier feeds them.  The pages list speculative
+ * decoding as unsupported ("Enable batch-invariant mixed decode and prefill
+ * for Qwen GDN", section "Out of scope"; "GatedDeltaNet Automatic Prefix
+ * Caching", section "Purpose", outstanding tasks); this entry point is the
+ * plain reading: the recurrence of gdn_decode_packed applied token after
+ * token, with the state after each token optionally kept in its own slot so
+ * the caller can resume from the last accepted token.
+ *
+ *   num_rows, tokens_per_row  R rows of T >= 1 tokens; token t of row r is
+ *              entry r*T + t of every token-major tensor.
+ *   q, k       [R*T][h_k][d_k] bf16;  v, o [R*T][h_v][d_v] bf16
+ *   g, beta    [R*T][h_v] fp32
+ *   state      [num_slots][h_v][d_v][d_k] fp32 slot cache.
+ *   src_slot   [R] int32: state entering token 0; negative = padded row
+ *              (skipped, its o rows zeroed).
+ *   dst_slots  [R*T] int32 or NULL.  Non-NULL: after token t the state is
+ *              written to slot dst_slots[r*T + t] when that entry is >= 0
+ *              (an entry >= num_slots sets GDN_DEV_BAD_SLOT and is skipped).
+ *              NULL: the state after the last token is written back to
+ *              src_slot[r].  Slots written by one call must be distinct,
+ *              except that a row may write its own src slot.
+ * The state is read once per (row, head) and kept on chip across the T
+ * tokens; T tokens of one call equal T calls of gdn_decode_packed bit for
+ * bit.
+ */
+gdn_status_t gdn_decode_multi(const gdn_dims_t *dims, int32_t num_rows, int32_t tokens_per_row,
+                              const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                              const float *g, const float *beta,
+                              float *state, int64_t num_slots,
+                              const int32_t *src_slot, const int32_t *dst_slots,
+                              gdn_bf16 *o, int32_t *dev_status, void *stream);
+
+/*
  * Chunked varlen prefill on the 64-token chunk grid.
  * vLLM page "Enable batch-invariant mixed decode and prefill for Qwen GDN",
  * section "How" (fresh prefill rows go through chunk prefill), and
@@ -149,6 +183,41 @@ gdn_status_t gdn_prefill_varlen(const gdn_dims_t *dims, int32_t num_seqs,
                                 float *chunk_states, int32_t emit_every_chunks,
                                 int64_t chunk_states_capacity,
                                 int32_t *dev_status, void *stream);
+
+/*
+ * Chunked varlen prefill that writes its emitted states straight into the
+ * prefix-cache blocks of the state cache, instead of a flat stream.
+ * "GatedDeltaNet Automatic Prefix Caching", section "Purpose" (replay the
+ * chunk history into persistent cache blocks so later requests hit the
+ * prefix cache) and the review thread on its decode/prefill metadata
+ * (block_idx_first_scheduled_token, block_idx_last_computed_token,
+ * block_idx_last_scheduled_token); "Enable GDN batch-invariant prefix
+ * caching", section "Purpose" (blocks on the 64-token chunk grid).
+ *
+ * Arguments as gdn_prefill_varlen, except:
+ *   emit_every_chunks  E >= 1: chunks per cache block (block size 64 E).
+ *   block_table        device int32 [num_seqs][block_table_stride]: the
+ *                      sequence's cache slots by block index.
+ *   block_first        device int32 [num_seqs]: block index that this call's
+ *                      first token opens (the cached prefix length / 64 E,
+ *                      i.e. block_idx_first_scheduled_token).
+ * The state after token 64 E (k+1) of this call (full chunks only) goes to
+ * slot block_table[s][block_first[s] + k].  A negative entry skips the
+ * write; an index past the row or a slot >= num_slots sets
+ * GDN_DEV_BAD_SLOT and skips it.  The values written are those that
+ * gdn_prefill_varlen emits into its stream, bit for bit; o and the final
+ * state (dst_slot) are the same too.
+ */
+gdn_status_t gdn_prefill_varlen_apc(const gdn_dims_t *dims, int32_t num_seqs,
+                                    const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                                    const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                                    const float *g, const float *beta,
+                                    float *state, int64_t num_slots,
+                                    const int32_t *src_slot, const int32_t *dst_slot,
+                                    gdn_bf16 *o, int32_t emit_every_chunks,
+                                    const int32_t *block_table, int32_t block_table_stride,
+                                    const int32_t *block_first,
+                                    int32_t *dev_status, void *stream);
 
 /*
  * One mixed continuous-batching step: num_decodes cached decode rows at the

@@ -25,8 +25,8 @@ from . import _build
 
 __all__ = [
     "GdnError", "load_library", "library_path",
-    "gdn_decode_packed", "gdn_prefill_varlen", "gdn_mixed_step",
-    "gdn_prefill_num_emits", "gdn_prefill_emit_offsets", "gdn_align_block_size",
+    "gdn_decode_packed", "gdn_decode_multi", "gdn_prefill_varlen", "gdn_prefill_varlen_apc",
+    "gdn_mixed_step", "gdn_prefill_num_emits", "gdn_prefill_emit_offsets", "gdn_align_block_size",
     "gdn_floor_prefix_hit", "gdn_grid_emit_every_chunks", "gdn_status_string",
     "EXPORTED_SYMBOLS", "GDN_DEV_BAD_SLOT", "GDN_DEV_TIMEOUT",
 ]
@@ -35,8 +35,8 @@ GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA = 0, 1, 2, 3
 GDN_DEV_BAD_SLOT, GDN_DEV_TIMEOUT = 0x1, 0x2
 
 EXPORTED_SYMBOLS = (
-    "gdn_decode_packed", "gdn_prefill_varlen", "gdn_mixed_step",
-    "gdn_prefill_num_emits", "gdn_prefill_emit_offsets", "gdn_align_block_size",
+    "gdn_decode_packed", "gdn_decode_multi", "gdn_prefill_varlen", "gdn_prefill_varlen_apc",
+    "gdn_mixed_step", "gdn_prefill_num_emits", "gdn_prefill_emit_offsets", "gdn_align_block_size",
     "gdn_floor_prefix_hit", "gdn_grid_emit_every_chunks", "gdn_status_string",
 )
 
@@ -73,9 +73,15 @@ def load_library() -> ctypes.CDLL:
     lib.gdn_decode_packed.restype = ctypes.c_int
     lib.gdn_decode_packed.argtypes = [ctypes.POINTER(Dims), _I32, _P, _P, _P, _P, _P, _P, _I64,
                                       _P, _P, _P, _P, _P]
+    lib.gdn_decode_multi.restype = ctypes.c_int
+    lib.gdn_decode_multi.argtypes = [ctypes.POINTER(Dims), _I32, _I32, _P, _P, _P, _P, _P, _P, _I64,
+                                     _P, _P, _P, _P, _P]
     lib.gdn_prefill_varlen.restype = ctypes.c_int
     lib.gdn_prefill_varlen.argtypes = [ctypes.POINTER(Dims), _I32, _P, _P, _P, _P, _P, _P, _P,
                                        _P, _I64, _P, _P, _P, _P, _I32, _I64, _P, _P]
+    lib.gdn_prefill_varlen_apc.restype = ctypes.c_int
+    lib.gdn_prefill_varlen_apc.argtypes = [ctypes.POINTER(Dims), _I32, _P, _P, _P, _P, _P, _P, _P,
+                                           _P, _I64, _P, _P, _P, _I32, _P, _I32, _P, _P, _P]
     lib.gdn_mixed_step.restype = ctypes.c_int
     lib.gdn_mixed_step.argtypes = [ctypes.POINTER(Dims), _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
                                    _P, _I64, _P, _P, _P, _P, _P, _P, _I32, _I64, _P, _P]
@@ -174,6 +180,36 @@ def gdn_decode_packed(q, k, v, g, beta, state, src_slot, o, dst_slot=None, dev_s
            "gdn_decode_packed")
 
 
+def gdn_decode_multi(tokens_per_row: int, q, k, v, g, beta, state, src_slot, o, dst_slots=None,
+                     dev_status=None, scale: float = 1.0, stream=None) -> None:
+    """Multi-token decode: ``q.shape[0] // tokens_per_row`` rows of
+    ``tokens_per_row`` consecutive tokens each (see gdn.h)."""
+    lib = load_library()
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    q, k, v = _dev(q, "q", bf, 3), _dev(k, "k", bf, 3), _dev(v, "v", bf, 3)
+    g, beta = _dev(g, "g", f32, 2), _dev(beta, "beta", f32, 2)
+    state = _dev(state, "state", f32, 4)
+    src_slot = _dev(src_slot, "src_slot", i32, 1)
+    dst_slots = _dev(dst_slots, "dst_slots", i32, 1, optional=True)
+    o = _dev(o, "o", bf, 3)
+    dev_status = _dev(dev_status, "dev_status", i32, optional=True)
+    T = int(tokens_per_row)
+    ntok = q.shape[0]
+    if T < 1 or ntok % T:
+        raise ValueError("q.shape[0] must be a multiple of tokens_per_row >= 1")
+    rows = ntok // T
+    if not (k.shape == q.shape and v.shape[0] == ntok and o.shape == v.shape
+            and g.shape == (ntok, v.shape[1]) and beta.shape == g.shape
+            and src_slot.shape[0] == rows and (dst_slots is None or dst_slots.shape[0] == ntok)
+            and state.shape[1:] == (v.shape[1], v.shape[2], q.shape[2])):
+        raise ValueError("inconsistent multi-token decode shapes")
+    d = _dims(q, v, scale)
+    _check(lib.gdn_decode_multi(ctypes.byref(d), rows, T, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                _ptr(beta), _ptr(state), state.shape[0], _ptr(src_slot),
+                                _ptr(dst_slots), _ptr(o), _ptr(dev_status), _stream(stream)),
+           "gdn_decode_multi")
+
+
 def gdn_prefill_varlen(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, o, state=None,
                        src_slot=None, dst_slot=None, chunk_states=None, emit_every_chunks: int = 0,
                        dev_status=None, scale: float = 1.0, stream=None) -> None:
@@ -206,6 +242,40 @@ def gdn_prefill_varlen(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, o, state=N
                                   _ptr(dst_slot), _ptr(o), _ptr(chunk_states),
                                   int(emit_every_chunks), cap, _ptr(dev_status), _stream(stream)),
            "gdn_prefill_varlen")
+
+
+def gdn_prefill_varlen_apc(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, o, state, block_table,
+                           block_first, emit_every_chunks: int, src_slot=None, dst_slot=None,
+                           dev_status=None, scale: float = 1.0, stream=None) -> None:
+    """Chunked varlen prefill emitting into cache blocks: ``block_table``
+    int32 [num_seqs][max_blocks], ``block_first`` int32 [num_seqs] (see gdn.h)."""
+    lib = load_library()
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    q, k, v = _dev(q, "q", bf, 3), _dev(k, "k", bf, 3), _dev(v, "v", bf, 3)
+    g, beta = _dev(g, "g", f32, 2), _dev(beta, "beta", f32, 2)
+    o = _dev(o, "o", bf, 3)
+    cu_seqlens = _dev(cu_seqlens, "cu_seqlens", i32, 1)
+    state = _dev(state, "state", f32, 4)
+    block_table = _dev(block_table, "block_table", i32, 2)
+    block_first = _dev(block_first, "block_first", i32, 1)
+    src_slot = _dev(src_slot, "src_slot", i32, 1, optional=True)
+    dst_slot = _dev(dst_slot, "dst_slot", i32, 1, optional=True)
+    dev_status = _dev(dev_status, "dev_status", i32, optional=True)
+    keep, cu_h = _host_i32(cu_seqlens_host, "cu_seqlens_host")
+    n = cu_seqlens.shape[0] - 1
+    if len(keep) != n + 1 or block_table.shape[0] != n or block_first.shape[0] != n:
+        raise ValueError("cu_seqlens_host, block_table and block_first must cover num_seqs sequences")
+    T = q.shape[0]
+    if not (k.shape == q.shape and v.shape[0] == T and o.shape == v.shape
+            and g.shape == (T, v.shape[1]) and beta.shape == g.shape):
+        raise ValueError("inconsistent prefill shapes")
+    d = _dims(q, v, scale)
+    _check(lib.gdn_prefill_varlen_apc(ctypes.byref(d), n, _ptr(cu_seqlens), cu_h, _ptr(q), _ptr(k),
+                                      _ptr(v), _ptr(g), _ptr(beta), _ptr(state), state.shape[0],
+                                      _ptr(src_slot), _ptr(dst_slot), _ptr(o), int(emit_every_chunks),
+                                      _ptr(block_table), block_table.shape[1], _ptr(block_first),
+                                      _ptr(dev_status), _stream(stream)),
+           "gdn_prefill_varlen_apc")
 
 
 def gdn_mixed_step(num_decodes: int, q, k, v, g, beta, cu_seqlens_p, cu_seqlens_p_host, state,

@@ -72,15 +72,51 @@ gdn_status_t decode_impl(const gdn_dims_t *dims, int32_t num_rows, const gdn_bf1
     return gdn::launch_decode(a, dims->d_k, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+gdn_status_t decode_multi_impl(const gdn_dims_t *dims, int32_t num_rows, int32_t tokens_per_row,
+                               const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                               const float *g, const float *beta, float *state, int64_t num_slots,
+                               const int32_t *src_slot, const int32_t *dst_slots, gdn_bf16 *o,
+                               int32_t *dev_status, cudaStream_t stream) {
+    gdn_status_t why = GDN_OK;
+    if (!dims_ok(dims, &why)) return why;
+    if (num_rows < 0 || tokens_per_row < 1 || num_slots < 0) return GDN_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(num_rows) * tokens_per_row > INT_MAX) return GDN_ERR_UNSUPPORTED;
+    if (num_rows == 0) return GDN_OK;
+    if (!q || !k || !v || !g || !beta || !state || !src_slot || !o) return GDN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(state) || !aligned16(o))
+        return GDN_ERR_INVALID_ARG;
+    gdn::DecodeMultiArgs a;
+    a.num_rows = num_rows;
+    a.tokens_per_row = tokens_per_row;
+    a.h_k = dims->h_k;
+    a.h_v = dims->h_v;
+    a.scale = dims->scale;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.g = g;
+    a.beta = beta;
+    a.state = state;
+    a.num_slots = num_slots;
+    a.src_slot = src_slot;
+    a.dst_slots = dst_slots;
+    a.o = o;
+    a.dev_status = dev_status;
+    return gdn::launch_decode_multi(a, dims->d_k, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 gdn_status_t prefill_impl(const gdn_dims_t *dims, int32_t num_seqs, const int32_t *cu_seqlens,
                           const int32_t *cu_host, const gdn_bf16 *q, const gdn_bf16 *k,
                           const gdn_bf16 *v, const float *g, const float *beta, float *state,
                           int64_t num_slots, const int32_t *src_slot, const int32_t *dst_slot,
                           gdn_bf16 *o, float *chunk_states, int32_t E, int64_t capacity,
-                          int32_t *dev_status, cudaStream_t stream) {
+                          int32_t *dev_status, cudaStream_t stream,
+                          const int32_t *emit_table = nullptr, int32_t emit_table_stride = 0,
+                          const int32_t *emit_first = nullptr) {
     gdn_status_t why = GDN_OK;
     if (!dims_ok(dims, &why)) return why;
     if (num_seqs < 0 || num_slots < 0 || E < 0) return GDN_ERR_INVALID_ARG;
+    if (emit_table && (!emit_first || emit_table_stride < 1 || !state)) return GDN_ERR_INVALID_ARG;
     if (num_seqs == 0) return GDN_OK;
     if (!cu_seqlens || !cu_ok(cu_host, num_seqs)) return GDN_ERR_INVALID_ARG;
     const int64_t T = cu_host[num_seqs];
@@ -89,7 +125,7 @@ gdn_status_t prefill_impl(const gdn_dims_t *dims, int32_t num_seqs, const int32_
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(state) || !aligned16(o) ||
         !aligned16(chunk_states))
         return GDN_ERR_INVALID_ARG;
-    if (E > 0) {
+    if (E > 0 && !emit_table) {
         const int64_t need = num_emits(cu_host, num_seqs, E);
         if (need > 0 && (!chunk_states || capacity < need)) return GDN_ERR_INVALID_ARG;
     }
@@ -110,11 +146,14 @@ gdn_status_t prefill_impl(const gdn_dims_t *dims, int32_t num_seqs, const int32_
     a.src_slot = src_slot;
     a.dst_slot = dst_slot;
     a.o = o;
-    a.chunk_states = E > 0 ? chunk_states : nullptr;
+    a.chunk_states = (E > 0 && !emit_table) ? chunk_states : nullptr;
     a.emit_every_chunks = E;
     a.dev_status = dev_status;
     a.total_tokens = T;
-    a.chunk_capacity = E > 0 ? capacity : 0;
+    a.chunk_capacity = (E > 0 && !emit_table) ? capacity : 0;
+    a.emit_table = E > 0 ? emit_table : nullptr;
+    a.emit_first = E > 0 ? emit_first : nullptr;
+    a.emit_table_stride = emit_table_stride;
     return gdn::launch_prefill(a, dims->d_k, cu_host, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -131,6 +170,15 @@ gdn_status_t gdn_decode_packed(const gdn_dims_t *dims, int32_t num_rows, const g
                        dev_status, static_cast<cudaStream_t>(stream));
 }
 
+gdn_status_t gdn_decode_multi(const gdn_dims_t *dims, int32_t num_rows, int32_t tokens_per_row,
+                              const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                              const float *g, const float *beta, float *state, int64_t num_slots,
+                              const int32_t *src_slot, const int32_t *dst_slots, gdn_bf16 *o,
+                              int32_t *dev_status, void *stream) {
+    return decode_multi_impl(dims, num_rows, tokens_per_row, q, k, v, g, beta, state, num_slots,
+                             src_slot, dst_slots, o, dev_status, static_cast<cudaStream_t>(stream));
+}
+
 gdn_status_t gdn_prefill_varlen(const gdn_dims_t *dims, int32_t num_seqs,
                                 const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                                 const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
@@ -142,6 +190,23 @@ gdn_status_t gdn_prefill_varlen(const gdn_dims_t *dims, int32_t num_seqs,
     return prefill_impl(dims, num_seqs, cu_seqlens, cu_seqlens_host, q, k, v, g, beta, state,
                         num_slots, src_slot, dst_slot, o, chunk_states, emit_every_chunks,
                         chunk_states_capacity, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+gdn_status_t gdn_prefill_varlen_apc(const gdn_dims_t *dims, int32_t num_seqs,
+                                    const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                                    const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                                    const float *g, const float *beta, float *state,
+                                    int64_t num_slots, const int32_t *src_slot,
+                                    const int32_t *dst_slot, gdn_bf16 *o,
+                                    int32_t emit_every_chunks, const int32_t *block_table,
+                                    int32_t block_table_stride, const int32_t *block_first,
+                                    int32_t *dev_status, void *stream) {
+    if (emit_every_chunks < 1 || !block_table || !block_first || block_table_stride < 1 || !state)
+        return GDN_ERR_INVALID_ARG;
+    return prefill_impl(dims, num_seqs, cu_seqlens, cu_seqlens_host, q, k, v, g, beta, state,
+                        num_slots, src_slot, dst_slot, o, nullptr, emit_every_chunks, 0, dev_status,
+                        static_cast<cudaStream_t>(stream), block_table, block_table_stride,
+                        block_first);
 }
 
 gdn_status_t gdn_mixed_step(const gdn_dims_t *dims, int32_t num_decodes, int32_t num_prefills,

@@ -1,4 +1,5 @@
-// Packed recurrent decode: one token per cached row against its fp32 state.
+// Packed recurrent decode: one token per cached row against its fp32 state,
+// and the multi-token form for rows carrying several (speculative) tokens.
 //
 // vLLM page "Enable batch-invariant mixed decode and prefill for Qwen GDN",
 // section "How": cached rows always go through this packed recurrent decode,
@@ -84,6 +85,109 @@ decode_kernel(const DecodeArgs a) {
     }
 }
 
+// Multi-token decode (speculative tokens): the item's 16 state rows stay in
+// registers across the row's tokens; after token t the state is stored at
+// dst_slots[r * T + t] when that entry is >= 0 (a snapshot a verifier can
+// roll back to), or, with dst_slots == NULL, once after the last token back
+// to src_slot[r].  Every step is the same update_row as the packed decode, so
+// T tokens here equal T packed-decode calls bit for bit.
+template <int D>
+__global__ void __launch_bounds__(kDecodeThreads)
+decode_multi_kernel(const DecodeMultiArgs a) {
+    constexpr int V4 = D / 32;
+    constexpr int kItemsPerHead = D / kRowsPerItem;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane >> 3;
+    const int l8 = lane & 7;
+    const int T = a.tokens_per_row;
+    const int64_t n_items = static_cast<int64_t>(a.num_rows) * a.h_v * kItemsPerHead;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int group = a.h_v / a.h_k;
+
+    for (int64_t it = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+         it < n_items; it += nwarps) {
+        const int blk = static_cast<int>(it % kItemsPerHead);
+        const int64_t rh = it / kItemsPerHead;
+        const int h = static_cast<int>(rh % a.h_v);
+        const int r = static_cast<int>(rh / a.h_v);
+        const int row0 = blk * kRowsPerItem;
+        const int kh = h / group;
+
+        const int src = a.src_slot[r];
+        if (src < 0 || src >= a.num_slots) {
+            if (src >= 0) report(a.dev_status, GDN_DEV_BAD_SLOT);
+            for (int t = 0; t < T; ++t) {
+                uint16_t *orow = a.o + ((static_cast<size_t>(r) * T + t) * a.h_v + h) * D;
+                if (lane < kRowsPerItem) orow[row0 + lane] = 0;
+            }
+            continue;
+        }
+        const float *sp = a.state + (static_cast<size_t>(src) * a.h_v + h) * D * D;
+        float4 s[kGroupsPerItem][V4];
+#pragma unroll
+        for (int i = 0; i < kGroupsPerItem; ++i) {
+            const int j = row0 + i * kRowsPerGroup + sub;
+#pragma unroll
+            for (int m = 0; m < V4; ++m)
+                s[i][m] = __ldcg(reinterpret_cast<const float4 *>(sp + static_cast<size_t>(j) * D +
+                                                                  4 * (l8 + 8 * m)));
+        }
+        for (int t = 0; t < T; ++t) {
+            const size_t tok = static_cast<size_t>(r) * T + t;
+            float kk[V4 * 4], qq[V4 * 4];
+            load_bf16_slice<V4>(a.k + (tok * a.h_k + kh) * D, l8, kk);
+            load_bf16_slice<V4>(a.q + (tok * a.h_k + kh) * D, l8, qq);
+            const size_t gh = tok * a.h_v + h;
+            const float alpha = expf(a.g[gh]);
+            const float beta = a.beta[gh];
+            const float kq = octet_dot<V4>(kk, qq);
+            const uint16_t *vrow = a.v + gh * D;
+            uint16_t *orow = a.o + gh * D;
+            int dst = -1;
+            if (a.dst_slots) {
+                dst = a.dst_slots[tok];
+                if (dst >= a.num_slots) {
+                    report(a.dev_status, GDN_DEV_BAD_SLOT);
+                    dst = -1;
+                }
+            } else if (t == T - 1) {
+                dst = src;
+            }
+            float *dp = dst >= 0 ? a.state + (static_cast<size_t>(dst) * a.h_v + h) * D * D : nullptr;
+#pragma unroll
+            for (int i = 0; i < kGroupsPerItem; ++i) {
+                const int j = row0 + i * kRowsPerGroup + sub;
+                const float vj = bf16_bits_to_float(vrow[j]);
+                const float oj = update_row<V4>(s[i], kk, qq, alpha, beta, vj, kq, a.scale);
+                if (dp) {
+#pragma unroll
+                    for (int m = 0; m < V4; ++m)
+                        __stcg(reinterpret_cast<float4 *>(dp + static_cast<size_t>(j) * D + 4 * (l8 + 8 * m)),
+                               s[i][m]);
+                }
+                if (l8 == 0) orow[j] = float_to_bf16_bits(oj);
+            }
+        }
+    }
+}
+
+template <int D>
+cudaError_t launch_decode_multi_d(const DecodeMultiArgs &a, cudaStream_t stream) {
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_multi_kernel<D>, kDecodeThreads, 0);
+    if (e != cudaSuccess) return e;
+    const int64_t items = static_cast<int64_t>(a.num_rows) * a.h_v * (D / kRowsPerItem);
+    const int64_t need = (items + (kDecodeThreads / 32) - 1) / (kDecodeThreads / 32);
+    const int64_t cap = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
+    const int grid = static_cast<int>(need < cap ? need : cap);
+    decode_multi_kernel<D><<<grid, kDecodeThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t stream) {
     int dev = 0, sms = 0, per_sm = 0;
@@ -106,6 +210,11 @@ cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t stream) {
 cudaError_t launch_decode(const DecodeArgs &a, int d, cudaStream_t stream) {
     if (a.num_rows == 0) return cudaSuccess;
     return d == 128 ? launch_decode_d<128>(a, stream) : launch_decode_d<64>(a, stream);
+}
+
+cudaError_t launch_decode_multi(const DecodeMultiArgs &a, int d, cudaStream_t stream) {
+    if (a.num_rows == 0 || a.tokens_per_row == 0) return cudaSuccess;
+    return d == 128 ? launch_decode_multi_d<128>(a, stream) : launch_decode_multi_d<64>(a, stream);
 }
 
 }  // namespace gdn

@@ -23,6 +23,20 @@ struct DecodeArgs {
     int32_t *dev_status;
 };
 
+// Multi-token decode: tokens_per_row consecutive tokens per row.
+struct DecodeMultiArgs {
+    int32_t num_rows, tokens_per_row, h_k, h_v;
+    float scale;
+    const uint16_t *q, *k, *v;  // token t of row r at index r * tokens_per_row + t
+    const float *g, *beta;
+    float *state;
+    int64_t num_slots;
+    const int32_t *src_slot;   // [num_rows]
+    const int32_t *dst_slots;  // [num_rows * tokens_per_row] or null
+    uint16_t *o;
+    int32_t *dev_status;
+};
+
 struct PrefillArgs {
     int32_t num_seqs, h_k, h_v;
     float scale;
@@ -38,10 +52,17 @@ struct PrefillArgs {
     int32_t *dev_status;
     int64_t total_tokens;    // rows of q, k, v, g, beta, o
     int64_t chunk_capacity;  // entries of chunk_states
+    // Emission into cache blocks (instead of chunk_states) when emit_table is
+    // set: emission k of sequence s goes to slot
+    // emit_table[s * emit_table_stride + emit_first[s] + k].
+    const int32_t *emit_table;
+    const int32_t *emit_first;
+    int32_t emit_table_stride;
 };
 
 // Launchers (decode.cu, prefill.cu).  Arguments are validated by the caller.
 cudaError_t launch_decode(const DecodeArgs &a, int d, cudaStream_t stream);
+cudaError_t launch_decode_multi(const DecodeMultiArgs &a, int d, cudaStream_t stream);
 // cu_host: host mirror of a.cu_seqlens (sizes the launch and orders the chains).
 cudaError_t launch_prefill(const PrefillArgs &a, int d, const int32_t *cu_host, cudaStream_t stream);
 

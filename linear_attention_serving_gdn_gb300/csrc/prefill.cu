@@ -338,6 +338,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
     const int Lseq = a.cu_seqlens[seq + 1] - t0;
     const int E = a.emit_every_chunks;
     const int64_t eoff = (E > 0 && a.chunk_states) ? emit_offset(a.cu_seqlens, seq, E, part) : 0;
+    const int emit_first = a.emit_table ? a.emit_first[seq] : 0;
     const int src = a.src_slot ? a.src_slot[seq] : -1;
     const int dst = a.dst_slot ? a.dst_slot[seq] : -1;
     const size_t ldq = static_cast<size_t>(a.h_k) * D, ldv = static_cast<size_t>(a.h_v) * D;
@@ -583,10 +584,21 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             mbar_arrive(freeb + s);  // every MMA and read of this chunk's stage is done
             if (j < D) {
                 float *ep = nullptr;
-                if (E > 0 && a.chunk_states && n == kChunk && ((c + 1) % E) == 0) {
-                    const int64_t idx = eoff + (c + 1) / E - 1;
-                    if (idx >= 0 && idx < a.chunk_capacity)
-                        ep = a.chunk_states + ((static_cast<size_t>(idx) * a.h_v + h) * D + jm) * D;
+                if (E > 0 && n == kChunk && ((c + 1) % E) == 0) {
+                    if (a.emit_table) {  // emission k of this sequence -> its cache block's slot
+                        const int64_t col = static_cast<int64_t>(emit_first) + (c + 1) / E - 1;
+                        const int slot = (col >= 0 && col < a.emit_table_stride)
+                                             ? a.emit_table[static_cast<int64_t>(seq) * a.emit_table_stride + col]
+                                             : static_cast<int>(a.num_slots);
+                        if (slot >= 0 && slot < a.num_slots)
+                            ep = a.state + ((static_cast<size_t>(slot) * a.h_v + h) * D + jm) * D;
+                        else if (slot >= 0 && tid == 0)
+                            report(a.dev_status, GDN_DEV_BAD_SLOT);
+                    } else if (a.chunk_states) {
+                        const int64_t idx = eoff + (c + 1) / E - 1;
+                        if (idx >= 0 && idx < a.chunk_capacity)
+                            ep = a.chunk_states + ((static_cast<size_t>(idx) * a.h_v + h) * D + jm) * D;
+                    }
                 }
                 float *dp = (c == n_chunks - 1 && dst >= 0)
                                 ? a.state + ((static_cast<size_t>(dst) * a.h_v + h) * D + jm) * D

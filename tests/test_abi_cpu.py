@@ -92,6 +92,24 @@ def test_decode_rejects_bad_arguments_on_the_host(lib):
     assert _decode(lib, ok, rows=0) == 0                           # empty: no-op
 
 
+def _multi(lib, dims, rows=4, T=3, q=FAKE, src=FAKE, state=FAKE):
+    return lib.gdn_decode_multi(ctypes.byref(dims), rows, T, q, FAKE, FAKE, FAKE, FAKE, state, 8,
+                                src, None, FAKE, None, None)
+
+
+def test_decode_multi_rejects_bad_arguments_on_the_host(lib):
+    ok = _Dims(16, 16, 128, 128, 1.0)
+    assert _multi(lib, _Dims(16, 16, 96, 96, 1.0)) == 2
+    assert _multi(lib, ok, T=0) == 1                               # at least one token per row
+    assert _multi(lib, ok, T=-2) == 1
+    assert _multi(lib, ok, rows=-1) == 1
+    assert _multi(lib, ok, rows=1 << 20, T=1 << 12) == 2          # rows * T beyond int32
+    assert _multi(lib, ok, q=None) == 1
+    assert _multi(lib, ok, src=None) == 1
+    assert _multi(lib, ok, state=ctypes.c_void_p(0x10008)) == 1   # misaligned
+    assert _multi(lib, ok, rows=0) == 0                            # empty: no-op
+
+
 def _prefill(lib, cu_host, n, E=0, cap=0, cs=None, dims=None):
     dims = dims or _Dims(16, 32, 128, 128, 1.0)
     arr = (ctypes.c_int32 * len(cu_host))(*cu_host)
@@ -107,6 +125,23 @@ def test_prefill_rejects_bad_arguments_on_the_host(lib):
     assert _prefill(lib, [0, 2000], 1, E=-1) == 1
     assert _prefill(lib, [0, 10], 1, dims=_Dims(16, 32, 256, 256, 1.0)) == 2
     assert _prefill(lib, [0], 0) == 0                              # no sequences: no-op
+
+
+def _apc(lib, cu_host, n, E=17, table=FAKE, stride=4, first=FAKE, state=FAKE):
+    dims = _Dims(16, 32, 128, 128, 1.0)
+    arr = (ctypes.c_int32 * len(cu_host))(*cu_host)
+    return lib.gdn_prefill_varlen_apc(ctypes.byref(dims), n, FAKE, arr, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                      state, 8, None, None, FAKE, E, table, stride, first, None, None)
+
+
+def test_prefill_apc_rejects_bad_arguments_on_the_host(lib):
+    assert _apc(lib, [0, 2000], 1, E=0) == 1                       # a block size is required
+    assert _apc(lib, [0, 2000], 1, table=None) == 1
+    assert _apc(lib, [0, 2000], 1, first=None) == 1
+    assert _apc(lib, [0, 2000], 1, stride=0) == 1
+    assert _apc(lib, [0, 2000], 1, state=None) == 1
+    assert _apc(lib, [0, 10, 5], 2) == 1                           # non-monotone
+    assert _apc(lib, [0], 0) == 0                                  # no sequences: no-op
 
 
 def test_mixed_step_rejects_bad_arguments_on_the_host(lib):
