@@ -46,6 +46,8 @@
 // Every shared-memory index that depends on the thread index is masked to
 // its array's range, so no address can leave the allocation even for a
 // thread outside the branch that guards it.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
 #include "gdn_internal.cuh"
@@ -64,6 +66,7 @@ constexpr long long kWaitCycles = 2000000000LL;
 constexpr int kMaxOrder = 2048;
 
 struct PrefillLaunch {
+    CUtensorMap tm_q, tm_k;  // q, k as 2-D [T][h_k d] bf16, 64 x 64 boxes, 128-byte swizzle
     PrefillArgs a;
     int32_t n_order;
     int32_t order[kMaxOrder];  // launch rank -> sequence, longest first
@@ -94,8 +97,8 @@ struct Smem {
     static constexpr uint32_t kBeta = kG + 256;                // f32 [64]
     static constexpr uint32_t kGraw = kBeta + 256;             // f32 [64]
     static constexpr uint32_t kDec = kGraw + 256;              // f32 [64] exp(G_C - G_t)
-    static constexpr uint32_t kBars = kDec + 256;              // 6 mbarriers
-    static constexpr uint32_t kTmem = kBars + 48;              // TMEM base address
+    static constexpr uint32_t kBars = kDec + 256;              // 8 mbarriers
+    static constexpr uint32_t kTmem = kBars + 64;              // TMEM base address
     static constexpr uint32_t kFail = kTmem + 4;               // int
     static constexpr uint32_t kEoff = kFail + 4;               // long long [16]
     static constexpr uint32_t kBytes = kEoff + 128;
@@ -127,6 +130,20 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 w) {
     r.z = pack_half2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u));
     r.w = pack_half2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
     return r;
+}
+
+// TMA: one 2-D box of a tensor map into shared memory, completing on an
+// mbarrier that expects the box's bytes.
+__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            tc::smem_u32(smem_dst)),
+        "l"(map), "r"(x), "r"(y), "r"(tc::smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(bar)), "r"(bytes)
+                 : "memory");
 }
 
 __device__ __forceinline__ float half_bits_to_float(uint16_t h) {
@@ -325,7 +342,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
     float *sGraw = reinterpret_cast<float *>(sm + SM::kGraw);
     float *sDec = reinterpret_cast<float *>(sm + SM::kDec);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SM::kBars);
-    uint64_t *mma_bar = bars + 0, *gram_bar = bars + 1, *ready = bars + 2, *freeb = bars + 4;
+    uint64_t *mma_bar = bars + 0, *gram_bar = bars + 1, *ready = bars + 2, *freeb = bars + 4, *tma_bar = bars + 6;
     uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(sm + SM::kTmem);
     int *fail = reinterpret_cast<int *>(sm + SM::kFail);
     long long *part = reinterpret_cast<long long *>(sm + SM::kEoff);
@@ -366,6 +383,8 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
         tc::mbar_init(ready + 1, kGroup);
         tc::mbar_init(freeb + 0, kGroup);
         tc::mbar_init(freeb + 1, kGroup);
+        tc::mbar_init(tma_bar + 0, 1);
+        tc::mbar_init(tma_bar + 1, 1);
         *fail = 0;
     }
     if (D < 128) {  // rows >= D of the transposed operand tiles stay zero (d = 64 pads M to 128)
@@ -640,11 +659,14 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
         const int p = pid & 127, hf = pid >> 7;
         bool failed = false;
         const uint32_t aIdGram = tc::idesc_f16_f32acc(128, 64);
-        // q, k, g, beta of a chunk into registers.
+        // q, k of a chunk go straight into its stage's operand tile by TMA
+        // (bf16, 128-byte swizzle: the layout the MMA descriptors expect),
+        // issued one chunk ahead as soon as the stage is free; g, beta into
+        // registers.  The bf16 -> fp16 conversion then runs in place.
         constexpr int kPer = 64 * (D / 8) / kGroup;  // 16-byte chunks per thread per tile
-        uint4 qv[kPer], kv[kPer];
+        constexpr uint32_t kTmaBytes = 2u * (D / 64) * 64 * 128;
         float gv = 0.f, bv = 0.f;
-        auto load_chunk = [&](int cc) {
+        auto issue_chunk = [&](int cc) {
             const int tk = t0 + cc * kChunk;
             const int nn = min(kChunk, Lseq - cc * kChunk);
             if (pid < 64) {
@@ -652,49 +674,51 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 gv = a.g[gi];
                 bv = a.beta[gi];
             }
+            if (pid == 0) {
+                uint8_t *tile = sQK(cc & 1);
+                uint64_t *tb = tma_bar + (cc & 1);
+                mbar_expect_tx(tb, kTmaBytes);
 #pragma unroll
-            for (int it = 0; it < kPer; ++it) {
-                const int e = pid + it * kGroup;
-                const int r = e / (D / 8), c8 = e % (D / 8);
-                const size_t row = static_cast<size_t>(tk + min(r, nn - 1));  // always a row of that chunk
-                qv[it] = __ldg(reinterpret_cast<const uint4 *>(a.q + row * ldq + kh * D + c8 * 8));
-                kv[it] = __ldg(reinterpret_cast<const uint4 *>(a.k + row * ldq + kh * D + c8 * 8));
+                for (int kb = 0; kb < D / 64; ++kb) {
+                    tma_load_2d(tile + kb * 16384, &L.tm_q, kh * D + kb * 64, tk, tb);
+                    tma_load_2d(tile + kb * 16384 + 8192, &L.tm_k, kh * D + kb * 64, tk, tb);
+                }
             }
         };
+        if (n_chunks > 0) issue_chunk(0);
         for (int c = 0; c < n_chunks; ++c) {
             const int s = c & 1;
             const int tok0 = t0 + c * kChunk;
             const int n = min(kChunk, Lseq - c * kChunk);
-            load_chunk(c);  // issued before the wait for the stage
-            if (c >= 2) {
-                const bool ok = mbar_wait_bounded(freeb + s, ((c - 2) >> 1) & 1);
-                if (group_any(kBarPrep, !ok)) {
-                    failed = true;
-                    break;
-                }
-            }
-            // ---- q, k as fp16 operand tiles; g, beta ----------------------------------
+            // ---- q, k tiles (copied during the previous chunk) to fp16; g, beta ----------
             uint8_t *qk = sQK(s);
             {
-                if (c + 1 < n_chunks && pid < 128) {  // q, k rows of the next chunk into L2
-                    const int rn = min(kChunk, Lseq - (c + 1) * kChunk);
+                if (c + 2 < n_chunks && pid < 128) {  // q, k rows of chunk c + 2 into L2
+                    const int rn = min(kChunk, Lseq - (c + 2) * kChunk);
                     const int r = pid & 63;
                     if (r < rn) {
-                        const size_t row = static_cast<size_t>(tok0 + kChunk + r);
+                        const size_t row = static_cast<size_t>(tok0 + 2 * kChunk + r);
                         const uint16_t *src_row = (pid < 64 ? a.q : a.k) + row * ldq + kh * D;
                         asm volatile("prefetch.global.L2 [%0];" ::"l"(src_row) : "memory");
                         if (D > 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(src_row + 64) : "memory");
                     }
                 }
+                const bool okt = mbar_wait_bounded(tma_bar + s, (c >> 1) & 1);
+                if (group_any(kBarPrep, !okt)) {
+                    failed = true;
+                    break;
+                }
+                // rows past the sequence end (the next sequence's tokens) become zeros
 #pragma unroll
                 for (int it = 0; it < kPer; ++it) {
                     const int e = pid + it * kGroup;
                     const int r = e / (D / 8), c8 = e % (D / 8);
+                    uint4 *pq = reinterpret_cast<uint4 *>(qk + tc::sw128_chunk_offset(r, c8, 128));
+                    uint4 *pk = reinterpret_cast<uint4 *>(qk + tc::sw128_chunk_offset(64 + r, c8, 128));
                     const uint4 z = make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4 *>(qk + tc::sw128_chunk_offset(r, c8, 128)) =
-                        r < n ? bf16x8_to_f16x8(qv[it]) : z;
-                    *reinterpret_cast<uint4 *>(qk + tc::sw128_chunk_offset(64 + r, c8, 128)) =
-                        r < n ? bf16x8_to_f16x8(kv[it]) : z;
+                    const uint4 xq = *pq, xk = *pk;
+                    *pq = r < n ? bf16x8_to_f16x8(xq) : z;
+                    *pk = r < n ? bf16x8_to_f16x8(xk) : z;
                 }
                 if (pid < 64) {
                     const int t = pid & 63;
@@ -810,7 +834,17 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             }
             group_sync(kBarPrep);
             if (pid < 64) invert_diag_store(sM, pid, xd);
-            group_sync(kBarPrep);
+            // ---- the next chunk's q, k copies, once its stage is free --------------------
+            if (c + 1 < n_chunks) {
+                const bool ok = c + 1 < 2 || mbar_wait_bounded(freeb + (s ^ 1), ((c - 1) >> 1) & 1);
+                if (group_any(kBarPrep, !ok)) {
+                    failed = true;
+                    break;
+                }
+                issue_chunk(c + 1);
+            } else {
+                group_sync(kBarPrep);
+            }
             invert_block_row<1>(sM, sW, pid);
             invert_block_row<2>(sM, sW, pid);
             invert_block_row<3>(sM, sW, pid);
@@ -860,12 +894,44 @@ cudaError_t launch_d(const PrefillLaunch &L, cudaStream_t stream) {
 
 }  // namespace
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library); resolved once.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// rows x cols bf16, row-major with row stride cols; boxes of 64 rows x 64 cols.
+bool encode_rows(CUtensorMap *m, const uint16_t *base, uint64_t rows, uint64_t cols) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {cols, rows > 0 ? rows : 1};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_prefill(const PrefillArgs &a, int d, const int32_t *cu_host, cudaStream_t stream) {
     if (a.num_seqs == 0) return cudaSuccess;
     static_assert(sizeof(PrefillLaunch) < 32000, "kernel parameter size");
     // Longest sequences first, so the longest chains start in the first wave.
     PrefillLaunch L;
     L.a = a;
+    const uint64_t cols = static_cast<uint64_t>(a.h_k) * d;
+    if (a.total_tokens > 0 && (!encode_rows(&L.tm_q, a.q, a.total_tokens, cols) ||
+                               !encode_rows(&L.tm_k, a.k, a.total_tokens, cols)))
+        return cudaErrorNotSupported;
     L.n_order = a.num_seqs < kMaxOrder ? a.num_seqs : kMaxOrder;
     for (int i = 0; i < L.n_order; ++i) L.order[i] = i;
     for (int i = 1; i < L.n_order; ++i) {  // insertion sort by length, descending, stable
