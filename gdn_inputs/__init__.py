@@ -186,3 +186,36 @@ def prefix_cache_prefill(seed: int = 0, n_seq: int = 4, seqlen: int = 32768) -> 
     b = token_batch([seqlen] * n_seq, 16, 32, 128, seed, init_state=False)
     return {"name": f"prefix_cache_{n_seq}x{seqlen}_hk16_hv32_d128_E17", "prefill": b,
             "emit_every_chunks": 17}
+
+
+@dataclass
+class RawInputs:
+    """Raw per-token projections ahead of the layer's input preparation:
+    q, k un-normalised (bf16 bits), a and b (fp32, [T][h_v]) from which the
+    decay and the write strength are formed, and the per-head parameters
+    A_log and dt_bias (fp32, [h_v])."""
+    h_k: int
+    h_v: int
+    d: int
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    a: np.ndarray
+    b: np.ndarray
+    A_log: np.ndarray
+    dt_bias: np.ndarray
+
+
+def raw_inputs(n_tokens: int, h_k: int, h_v: int, d: int, seed: int) -> RawInputs:
+    """q, k ~ N(0, 1) times a per-row scale drawn log-uniform in [0.25, 4]
+    (so normalisation matters), v ~ N(0, 1), all rounded to bf16; a, b ~
+    N(0, 1); A_log ~ log U(0.02, 0.2); dt_bias ~ N(0, 0.5**2)."""
+    rng = np.random.default_rng(np.random.PCG64(seed + 271828))
+    q = _normal(rng, (n_tokens, h_k, d)) * np.exp2(rng.uniform(-2, 2, (n_tokens, h_k, 1))).astype(np.float32)
+    k = _normal(rng, (n_tokens, h_k, d)) * np.exp2(rng.uniform(-2, 2, (n_tokens, h_k, 1))).astype(np.float32)
+    v = _normal(rng, (n_tokens, h_v, d))
+    a = _normal(rng, (n_tokens, h_v))
+    b = _normal(rng, (n_tokens, h_v))
+    A_log = np.log(rng.uniform(0.02, 0.2, h_v)).astype(np.float32)
+    dt_bias = (0.5 * _normal(rng, (h_v,))).astype(np.float32)
+    return RawInputs(h_k, h_v, d, bf16_bits(q), bf16_bits(k), bf16_bits(v), a, b, A_log, dt_bias)
