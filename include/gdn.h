@@ -107,6 +107,45 @@ gdn_status_t gdn_decode_packed(const gdn_dims_t *dims, int32_t num_rows,
                                gdn_bf16 *o, int32_t *dev_status, void *stream);
 
 /*
+ * Input preparation ahead of the recurrence, from raw per-token projections.
+ * The pages give no formula for this step (they consume prepared inputs);
+ * the reading is the Gated DeltaNet layer's (Yang, Kautz, Hatamizadeh,
+ * ICLR 2025):
+ *     q = q_raw / sqrt(sum q_raw^2 + eps), k likewise   (per token and key head,
+ *                                                         rounded to bf16)
+ *     g = -exp(A_log[h]) * softplus(a + dt_bias[h]),  beta = sigmoid(b)
+ *
+ *   num_tokens       T >= 0 tokens.
+ *   q_raw, k_raw     [T][h_k][d_k] bf16;  q, k outputs, same shape (may alias
+ *                    the inputs).
+ *   a, b             [T][h_v] fp32;  g, beta outputs [T][h_v] fp32.
+ *   A_log, dt_bias   [h_v] fp32.
+ *   eps              >= 0, added to the sum of squares.
+ * The sum of squares and every later operation have one fixed order, shared
+ * with gdn_decode_packed_raw: this call followed by gdn_decode_packed gives
+ * the fused call's outputs and states bit for bit.
+ */
+gdn_status_t gdn_prep_inputs(const gdn_dims_t *dims, int64_t num_tokens,
+                             const gdn_bf16 *q_raw, const gdn_bf16 *k_raw,
+                             const float *a, const float *b,
+                             const float *A_log, const float *dt_bias, float eps,
+                             gdn_bf16 *q, gdn_bf16 *k, float *g, float *beta, void *stream);
+
+/*
+ * gdn_decode_packed with the input preparation of gdn_prep_inputs fused into
+ * the kernel: q_raw, k_raw are normalised in registers and g, beta are formed
+ * from a, b, A_log, dt_bias as they are loaded.  Other arguments as
+ * gdn_decode_packed.
+ */
+gdn_status_t gdn_decode_packed_raw(const gdn_dims_t *dims, int32_t num_rows,
+                                   const gdn_bf16 *q_raw, const gdn_bf16 *k_raw, const gdn_bf16 *v,
+                                   const float *a, const float *b,
+                                   const float *A_log, const float *dt_bias, float eps,
+                                   float *state, int64_t num_slots,
+                                   const int32_t *src_slot, const int32_t *dst_slot,
+                                   gdn_bf16 *o, int32_t *dev_status, void *stream);
+
+/*
  * Multi-token decode: tokens_per_row consecutive tokens per cached row, as a
  * speculative-decoding verifier feeds them.  The pages list speculative
  * decoding as unsupported ("Enable batch-invariant mixed decode and prefill

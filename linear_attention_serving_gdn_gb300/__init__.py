@@ -25,8 +25,8 @@ from . import _build
 
 __all__ = [
     "GdnError", "load_library", "library_path",
-    "gdn_decode_packed", "gdn_decode_multi", "gdn_prefill_varlen", "gdn_prefill_varlen_apc",
-    "gdn_mixed_step", "gdn_prefill_num_emits", "gdn_prefill_emit_offsets", "gdn_align_block_size",
+    "gdn_decode_packed", "gdn_decode_packed_raw", "gdn_prep_inputs", "gdn_decode_multi",
+    "gdn_prefill_varlen", "gdn_prefill_varlen_apc", "gdn_mixed_step", "gdn_prefill_num_emits", "gdn_prefill_emit_offsets", "gdn_align_block_size",
     "gdn_floor_prefix_hit", "gdn_grid_emit_every_chunks", "gdn_status_string",
     "EXPORTED_SYMBOLS", "GDN_DEV_BAD_SLOT", "GDN_DEV_TIMEOUT",
 ]
@@ -35,8 +35,8 @@ GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA = 0, 1, 2, 3
 GDN_DEV_BAD_SLOT, GDN_DEV_TIMEOUT = 0x1, 0x2
 
 EXPORTED_SYMBOLS = (
-    "gdn_decode_packed", "gdn_decode_multi", "gdn_prefill_varlen", "gdn_prefill_varlen_apc",
-    "gdn_mixed_step", "gdn_prefill_num_emits", "gdn_prefill_emit_offsets", "gdn_align_block_size",
+    "gdn_decode_packed", "gdn_decode_packed_raw", "gdn_prep_inputs", "gdn_decode_multi",
+    "gdn_prefill_varlen", "gdn_prefill_varlen_apc", "gdn_mixed_step", "gdn_prefill_num_emits", "gdn_prefill_emit_offsets", "gdn_align_block_size",
     "gdn_floor_prefix_hit", "gdn_grid_emit_every_chunks", "gdn_status_string",
 )
 
@@ -73,6 +73,12 @@ def load_library() -> ctypes.CDLL:
     lib.gdn_decode_packed.restype = ctypes.c_int
     lib.gdn_decode_packed.argtypes = [ctypes.POINTER(Dims), _I32, _P, _P, _P, _P, _P, _P, _I64,
                                       _P, _P, _P, _P, _P]
+    lib.gdn_decode_packed_raw.restype = ctypes.c_int
+    lib.gdn_decode_packed_raw.argtypes = [ctypes.POINTER(Dims), _I32, _P, _P, _P, _P, _P, _P, _P,
+                                          ctypes.c_float, _P, _I64, _P, _P, _P, _P, _P]
+    lib.gdn_prep_inputs.restype = ctypes.c_int
+    lib.gdn_prep_inputs.argtypes = [ctypes.POINTER(Dims), _I64, _P, _P, _P, _P, _P, _P, ctypes.c_float,
+                                    _P, _P, _P, _P, _P]
     lib.gdn_decode_multi.restype = ctypes.c_int
     lib.gdn_decode_multi.argtypes = [ctypes.POINTER(Dims), _I32, _I32, _P, _P, _P, _P, _P, _P, _I64,
                                      _P, _P, _P, _P, _P]
@@ -178,6 +184,56 @@ def gdn_decode_packed(q, k, v, g, beta, state, src_slot, o, dst_slot=None, dev_s
                                  _ptr(beta), _ptr(state), state.shape[0], _ptr(src_slot),
                                  _ptr(dst_slot), _ptr(o), _ptr(dev_status), _stream(stream)),
            "gdn_decode_packed")
+
+
+def gdn_prep_inputs(q_raw, k_raw, a, b, A_log, dt_bias, q, k, g, beta, eps: float = 1e-6,
+                    stream=None) -> None:
+    """Input preparation: normalised q, k (bf16) and g, beta (fp32) from raw
+    projections (see gdn.h).  q, k may alias q_raw, k_raw."""
+    lib = load_library()
+    bf, f32 = torch.bfloat16, torch.float32
+    q_raw, k_raw = _dev(q_raw, "q_raw", bf, 3), _dev(k_raw, "k_raw", bf, 3)
+    q, k = _dev(q, "q", bf, 3), _dev(k, "k", bf, 3)
+    a, b, g, beta = (_dev(x, n, f32, 2) for x, n in ((a, "a"), (b, "b"), (g, "g"), (beta, "beta")))
+    A_log, dt_bias = _dev(A_log, "A_log", f32, 1), _dev(dt_bias, "dt_bias", f32, 1)
+    T, h_v = a.shape
+    if not (k_raw.shape == q_raw.shape == q.shape == k.shape and q.shape[0] == T and b.shape == a.shape
+            and g.shape == a.shape and beta.shape == a.shape and A_log.shape == (h_v,)
+            and dt_bias.shape == (h_v,)):
+        raise ValueError("inconsistent input-preparation shapes")
+    d = Dims(q.shape[1], h_v, q.shape[2], q.shape[2], 1.0)
+    _check(lib.gdn_prep_inputs(ctypes.byref(d), T, _ptr(q_raw), _ptr(k_raw), _ptr(a), _ptr(b), _ptr(A_log),
+                               _ptr(dt_bias), float(eps), _ptr(q), _ptr(k), _ptr(g), _ptr(beta),
+                               _stream(stream)),
+           "gdn_prep_inputs")
+
+
+def gdn_decode_packed_raw(q_raw, k_raw, v, a, b, A_log, dt_bias, state, src_slot, o, dst_slot=None,
+                          dev_status=None, eps: float = 1e-6, scale: float = 1.0, stream=None) -> None:
+    """Packed decode with the input preparation fused in (see gdn.h)."""
+    lib = load_library()
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    q_raw, k_raw, v = _dev(q_raw, "q_raw", bf, 3), _dev(k_raw, "k_raw", bf, 3), _dev(v, "v", bf, 3)
+    a, b = _dev(a, "a", f32, 2), _dev(b, "b", f32, 2)
+    A_log, dt_bias = _dev(A_log, "A_log", f32, 1), _dev(dt_bias, "dt_bias", f32, 1)
+    state = _dev(state, "state", f32, 4)
+    src_slot = _dev(src_slot, "src_slot", i32, 1)
+    dst_slot = _dev(dst_slot, "dst_slot", i32, 1, optional=True)
+    o = _dev(o, "o", bf, 3)
+    dev_status = _dev(dev_status, "dev_status", i32, optional=True)
+    rows = q_raw.shape[0]
+    if not (k_raw.shape == q_raw.shape and v.shape[0] == rows and o.shape == v.shape
+            and a.shape == (rows, v.shape[1]) and b.shape == a.shape
+            and A_log.shape == (v.shape[1],) and dt_bias.shape == A_log.shape
+            and src_slot.shape[0] == rows and (dst_slot is None or dst_slot.shape[0] == rows)
+            and state.shape[1:] == (v.shape[1], v.shape[2], q_raw.shape[2])):
+        raise ValueError("inconsistent decode shapes")
+    d = _dims(q_raw, v, scale)
+    _check(lib.gdn_decode_packed_raw(ctypes.byref(d), rows, _ptr(q_raw), _ptr(k_raw), _ptr(v), _ptr(a),
+                                     _ptr(b), _ptr(A_log), _ptr(dt_bias), float(eps), _ptr(state),
+                                     state.shape[0], _ptr(src_slot), _ptr(dst_slot), _ptr(o),
+                                     _ptr(dev_status), _stream(stream)),
+           "gdn_decode_packed_raw")
 
 
 def gdn_decode_multi(tokens_per_row: int, q, k, v, g, beta, state, src_slot, o, dst_slots=None,

@@ -41,16 +41,23 @@ int64_t num_emits(const int32_t *cu, int32_t n, int32_t E) {
     return tot;
 }
 
+// Raw-input preparation parameters of the fused decode (all null: none).
+struct RawPrep {
+    const float *a = nullptr, *b = nullptr, *A_log = nullptr, *dt_bias = nullptr;
+    float eps = 0.f;
+};
+
 gdn_status_t decode_impl(const gdn_dims_t *dims, int32_t num_rows, const gdn_bf16 *q,
                          const gdn_bf16 *k, const gdn_bf16 *v, const float *g, const float *beta,
                          float *state, int64_t num_slots, const int32_t *src_slot,
                          const int32_t *dst_slot, gdn_bf16 *o, int32_t *dev_status,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, const RawPrep &raw = RawPrep()) {
     gdn_status_t why = GDN_OK;
     if (!dims_ok(dims, &why)) return why;
     if (num_rows < 0 || num_slots < 0) return GDN_ERR_INVALID_ARG;
     if (num_rows == 0) return GDN_OK;
-    if (!q || !k || !v || !g || !beta || !state || !src_slot || !o) return GDN_ERR_INVALID_ARG;
+    const bool have_gates = raw.a ? (raw.b && raw.A_log && raw.dt_bias && raw.eps >= 0.f) : (g && beta);
+    if (!q || !k || !v || !have_gates || !state || !src_slot || !o) return GDN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(state) || !aligned16(o))
         return GDN_ERR_INVALID_ARG;
     gdn::DecodeArgs a;
@@ -69,6 +76,11 @@ gdn_status_t decode_impl(const gdn_dims_t *dims, int32_t num_rows, const gdn_bf1
     a.dst_slot = dst_slot;
     a.o = o;
     a.dev_status = dev_status;
+    a.a_raw = raw.a;
+    a.b_raw = raw.b;
+    a.A_log = raw.A_log;
+    a.dt_bias = raw.dt_bias;
+    a.eps = raw.eps;
     return gdn::launch_decode(a, dims->d_k, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -168,6 +180,52 @@ gdn_status_t gdn_decode_packed(const gdn_dims_t *dims, int32_t num_rows, const g
                                int32_t *dev_status, void *stream) {
     return decode_impl(dims, num_rows, q, k, v, g, beta, state, num_slots, src_slot, dst_slot, o,
                        dev_status, static_cast<cudaStream_t>(stream));
+}
+
+gdn_status_t gdn_decode_packed_raw(const gdn_dims_t *dims, int32_t num_rows, const gdn_bf16 *q_raw,
+                                   const gdn_bf16 *k_raw, const gdn_bf16 *v, const float *a,
+                                   const float *b, const float *A_log, const float *dt_bias, float eps,
+                                   float *state, int64_t num_slots, const int32_t *src_slot,
+                                   const int32_t *dst_slot, gdn_bf16 *o, int32_t *dev_status,
+                                   void *stream) {
+    if (!a || !b || !A_log || !dt_bias || !(eps >= 0.f)) return GDN_ERR_INVALID_ARG;
+    RawPrep raw;
+    raw.a = a;
+    raw.b = b;
+    raw.A_log = A_log;
+    raw.dt_bias = dt_bias;
+    raw.eps = eps;
+    return decode_impl(dims, num_rows, q_raw, k_raw, v, nullptr, nullptr, state, num_slots, src_slot,
+                       dst_slot, o, dev_status, static_cast<cudaStream_t>(stream), raw);
+}
+
+gdn_status_t gdn_prep_inputs(const gdn_dims_t *dims, int64_t num_tokens, const gdn_bf16 *q_raw,
+                             const gdn_bf16 *k_raw, const float *a, const float *b, const float *A_log,
+                             const float *dt_bias, float eps, gdn_bf16 *q, gdn_bf16 *k, float *g,
+                             float *beta, void *stream) {
+    gdn_status_t why = GDN_OK;
+    if (!dims_ok(dims, &why)) return why;
+    if (num_tokens < 0 || !(eps >= 0.f)) return GDN_ERR_INVALID_ARG;
+    if (num_tokens == 0) return GDN_OK;
+    if (!q_raw || !k_raw || !a || !b || !A_log || !dt_bias || !q || !k || !g || !beta) return GDN_ERR_INVALID_ARG;
+    if (!aligned16(q_raw) || !aligned16(k_raw) || !aligned16(q) || !aligned16(k)) return GDN_ERR_INVALID_ARG;
+    gdn::PrepArgs p;
+    p.num_tokens = num_tokens;
+    p.h_k = dims->h_k;
+    p.h_v = dims->h_v;
+    p.q_raw = q_raw;
+    p.k_raw = k_raw;
+    p.a = a;
+    p.b = b;
+    p.A_log = A_log;
+    p.dt_bias = dt_bias;
+    p.eps = eps;
+    p.q = q;
+    p.k = k;
+    p.g = g;
+    p.beta = beta;
+    return gdn::launch_prep(p, dims->d_k, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK
+                                                                                             : GDN_ERR_CUDA;
 }
 
 gdn_status_t gdn_decode_multi(const gdn_dims_t *dims, int32_t num_rows, int32_t tokens_per_row,

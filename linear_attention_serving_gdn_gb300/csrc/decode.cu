@@ -21,7 +21,7 @@ constexpr int kRowsPerGroup = 4;  // rows of S^T per warp-wide access (lane octe
 constexpr int kGroupsPerItem = 4;
 constexpr int kRowsPerItem = kRowsPerGroup * kGroupsPerItem;  // 16
 
-template <int D>
+template <int D, bool kRaw>
 __global__ void __launch_bounds__(kDecodeThreads)
 decode_kernel(const DecodeArgs a) {
     constexpr int V4 = D / 32;                   // float4 per lane per row
@@ -66,8 +66,16 @@ decode_kernel(const DecodeArgs a) {
         load_bf16_slice<V4>(a.k + (static_cast<size_t>(r) * a.h_k + kh) * D, l8, kk);
         load_bf16_slice<V4>(a.q + (static_cast<size_t>(r) * a.h_k + kh) * D, l8, qq);
         const size_t gh = static_cast<size_t>(r) * a.h_v + h;
-        const float alpha = expf(a.g[gh]);
-        const float beta = a.beta[gh];
+        float g, beta;
+        if constexpr (kRaw) {  // fused input preparation
+            normalize_bf16<V4>(kk, a.eps);
+            normalize_bf16<V4>(qq, a.eps);
+            gate_inputs(a.a_raw[gh], a.b_raw[gh], a.A_log[h], a.dt_bias[h], g, beta);
+        } else {
+            g = a.g[gh];
+            beta = a.beta[gh];
+        }
+        const float alpha = expf(g);
         const float kq = octet_dot<V4>(kk, qq);
         const uint16_t *vrow = a.v + gh * D;
 
@@ -188,20 +196,20 @@ cudaError_t launch_decode_multi_d(const DecodeMultiArgs &a, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool kRaw>
 cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t stream) {
     int dev = 0, sms = 0, per_sm = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D>, kDecodeThreads, 0);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, kRaw>, kDecodeThreads, 0);
     if (e != cudaSuccess) return e;
     const int64_t items = static_cast<int64_t>(a.num_rows) * a.h_v * (D / kRowsPerItem);
     const int64_t need = (items + (kDecodeThreads / 32) - 1) / (kDecodeThreads / 32);
     const int64_t cap = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
     const int grid = static_cast<int>(need < cap ? need : cap);
-    decode_kernel<D><<<grid, kDecodeThreads, 0, stream>>>(a);
+    decode_kernel<D, kRaw><<<grid, kDecodeThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -209,7 +217,8 @@ cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t stream) {
 
 cudaError_t launch_decode(const DecodeArgs &a, int d, cudaStream_t stream) {
     if (a.num_rows == 0) return cudaSuccess;
-    return d == 128 ? launch_decode_d<128>(a, stream) : launch_decode_d<64>(a, stream);
+    if (a.a_raw) return d == 128 ? launch_decode_d<128, true>(a, stream) : launch_decode_d<64, true>(a, stream);
+    return d == 128 ? launch_decode_d<128, false>(a, stream) : launch_decode_d<64, false>(a, stream);
 }
 
 cudaError_t launch_decode_multi(const DecodeMultiArgs &a, int d, cudaStream_t stream) {

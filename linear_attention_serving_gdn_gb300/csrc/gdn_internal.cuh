@@ -21,6 +21,21 @@ struct DecodeArgs {
     const int32_t *src_slot, *dst_slot;
     uint16_t *o;
     int32_t *dev_status;
+    // Fused input preparation (when a_raw is set): q, k are raw and are
+    // normalised in the kernel; g, beta come from a_raw, b_raw, A_log, dt_bias.
+    const float *a_raw, *b_raw, *A_log, *dt_bias;
+    float eps;
+};
+
+// Standalone input preparation.
+struct PrepArgs {
+    int64_t num_tokens;
+    int32_t h_k, h_v;
+    const uint16_t *q_raw, *k_raw;
+    const float *a, *b, *A_log, *dt_bias;
+    float eps;
+    uint16_t *q, *k;
+    float *g, *beta;
 };
 
 // Multi-token decode: tokens_per_row consecutive tokens per row.
@@ -63,6 +78,7 @@ struct PrefillArgs {
 // Launchers (decode.cu, prefill.cu).  Arguments are validated by the caller.
 cudaError_t launch_decode(const DecodeArgs &a, int d, cudaStream_t stream);
 cudaError_t launch_decode_multi(const DecodeMultiArgs &a, int d, cudaStream_t stream);
+cudaError_t launch_prep(const PrepArgs &a, int d, cudaStream_t stream);
 // cu_host: host mirror of a.cu_seqlens (sizes the launch and orders the chains).
 cudaError_t launch_prefill(const PrefillArgs &a, int d, const int32_t *cu_host, cudaStream_t stream);
 

@@ -1,0 +1,78 @@
+// Input preparation of the layer ahead of the recurrence: q, k normalised
+// per (token, key head) and the decay / write strength formed from raw
+// projections (formulas and their fixed evaluation order in row_update.cuh).
+// The pages give no formula for this step; the reading is the Gated DeltaNet
+// layer's.  Rows are handled by lane octets in exactly the decode kernel's
+// layout, so this kernel followed by gdn_decode_packed equals the fused
+// gdn_decode_packed_raw bit for bit.  Memory-bound: one read and one write of
+// q, k, and a, b -> g, beta.
+#include "row_update.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kPrepThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
+    constexpr int V4 = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane >> 3, l8 = lane & 7;
+    const int64_t rows_per_tensor = a.num_tokens * a.h_k;
+    const int64_t rows = 2 * rows_per_tensor;  // q rows, then k rows
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    // Warp-uniform loop over groups of 4 rows (one per lane octet): every lane
+    // takes part in the octet reductions; octets past the end only skip I/O.
+    for (int64_t base = warp * 4; base < rows; base += nwarps * 4) {
+        const int64_t row = base + sub;
+        const bool live = row < rows;
+        const bool is_k = row >= rows_per_tensor;
+        const int64_t rr = is_k ? row - rows_per_tensor : row;
+        float x[V4 * 4];
+        if (live) {
+            load_bf16_slice<V4>((is_k ? a.k_raw : a.q_raw) + rr * D, l8, x);
+        } else {
+#pragma unroll
+            for (int e = 0; e < V4 * 4; ++e) x[e] = 0.f;
+        }
+        normalize_bf16<V4>(x, a.eps);
+        if (live) store_bf16_slice<V4>((is_k ? a.k : a.q) + rr * D, l8, x);
+    }
+    const int64_t n_gate = a.num_tokens * a.h_v;
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_gate;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int h = static_cast<int>(e % a.h_v);
+        float g, beta;
+        gate_inputs(a.a[e], a.b[e], a.A_log[h], a.dt_bias[h], g, beta);
+        a.g[e] = g;
+        a.beta[e] = beta;
+    }
+}
+
+template <int D>
+cudaError_t launch_prep_d(const PrepArgs &a, cudaStream_t stream) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t rows = 2 * a.num_tokens * a.h_k;
+    const int64_t need_rows = (rows + (kPrepThreads / 8) - 1) / (kPrepThreads / 8);
+    const int64_t need_gate = (a.num_tokens * a.h_v + kPrepThreads - 1) / kPrepThreads;
+    int64_t grid = need_rows > need_gate ? need_rows : need_gate;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    prep_kernel<D><<<static_cast<int>(grid), kPrepThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const PrepArgs &a, int d, cudaStream_t stream) {
+    if (a.num_tokens == 0) return cudaSuccess;
+    return d == 128 ? launch_prep_d<128>(a, stream) : launch_prep_d<64>(a, stream);
+}
+
+}  // namespace gdn

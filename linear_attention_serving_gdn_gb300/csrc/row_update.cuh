@@ -31,6 +31,45 @@ __device__ __forceinline__ void load_bf16_slice(const uint16_t *p, int l8, float
     }
 }
 
+template <int V4>
+__device__ __forceinline__ void store_bf16_slice(uint16_t *p, int l8, const float (&x)[V4 * 4]) {
+#pragma unroll
+    for (int m = 0; m < V4; ++m) {
+        uint2 w;
+        w.x = static_cast<uint32_t>(float_to_bf16_bits(x[4 * m + 0])) |
+              (static_cast<uint32_t>(float_to_bf16_bits(x[4 * m + 1])) << 16);
+        w.y = static_cast<uint32_t>(float_to_bf16_bits(x[4 * m + 2])) |
+              (static_cast<uint32_t>(float_to_bf16_bits(x[4 * m + 3])) << 16);
+        *reinterpret_cast<uint2 *>(p + 4 * (l8 + 8 * m)) = w;
+    }
+}
+
+// Input preparation of the layer (the pages give no formula; the reading is
+// the Gated DeltaNet layer's): per (token, key head)
+//     x_hat = x / sqrt(sum x^2 + eps), rounded to bf16,
+// and per (token, value head)
+//     g = -exp(A_log) softplus(a + dt_bias),  beta = sigmoid(b).
+// The sum of squares has one fixed order (each lane of the octet over its
+// slice, then the xor butterfly) and every operation is explicitly rounded,
+// so the standalone preparation kernel and the fused decode produce the
+// same bits.
+template <int V4>
+__device__ __forceinline__ void normalize_bf16(float (&x)[V4 * 4], float eps) {
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < V4 * 4; ++e) acc = __fmaf_rn(x[e], x[e], acc);
+    const float inv = rsqrtf(__fadd_rn(octet_sum(acc), eps));
+#pragma unroll
+    for (int e = 0; e < V4 * 4; ++e) x[e] = bf16_bits_to_float(float_to_bf16_bits(__fmul_rn(x[e], inv)));
+}
+
+__device__ __forceinline__ void gate_inputs(float a, float b, float A_log, float dt_bias, float &g, float &beta) {
+    const float x = __fadd_rn(a, dt_bias);
+    const float sp = x > 20.f ? x : log1pf(expf(x));
+    g = __fmul_rn(-expf(A_log), sp);
+    beta = __frcp_rn(__fadd_rn(1.f, expf(-b)));
+}
+
 // k . q over the full head dim; identical bits on all lanes of the octet.
 template <int V4>
 __device__ __forceinline__ float octet_dot(const float (&kk)[V4 * 4], const float (&qq)[V4 * 4]) {

@@ -110,6 +110,25 @@ def test_decode_multi_rejects_bad_arguments_on_the_host(lib):
     assert _multi(lib, ok, rows=0) == 0                            # empty: no-op
 
 
+def test_input_prep_entries_reject_bad_arguments_on_the_host(lib):
+    ok = _Dims(16, 16, 128, 128, 1.0)
+    prep = lambda T=8, eps=1e-6, q=FAKE, A=FAKE: lib.gdn_prep_inputs(
+        ctypes.byref(ok), T, q, FAKE, FAKE, FAKE, A, FAKE, ctypes.c_float(eps), FAKE, FAKE, FAKE, FAKE, None)
+    assert prep(T=-1) == 1
+    assert prep(eps=-1.0) == 1
+    assert prep(q=None) == 1
+    assert prep(A=None) == 1
+    assert prep(T=0) == 0
+    raw = lambda eps=1e-6, a=FAKE: lib.gdn_decode_packed_raw(
+        ctypes.byref(ok), 4, FAKE, FAKE, FAKE, a, FAKE, FAKE, FAKE, ctypes.c_float(eps), FAKE, 8, FAKE, None,
+        FAKE, None, None)
+    assert raw(a=None) == 1
+    assert raw(eps=float("nan")) == 1
+    assert lib.gdn_decode_packed_raw(ctypes.byref(_Dims(16, 16, 96, 96, 1.0)), 4, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                     FAKE, FAKE, ctypes.c_float(1e-6), FAKE, 8, FAKE, None, FAKE, None,
+                                     None) == 2
+
+
 def _prefill(lib, cu_host, n, E=0, cap=0, cs=None, dims=None):
     dims = dims or _Dims(16, 32, 128, 128, 1.0)
     arr = (ctypes.c_int32 * len(cu_host))(*cu_host)
