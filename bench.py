@@ -433,6 +433,16 @@ def cpu_baseline(target_s=10.0):
                       f"(H=16, d=128), fp64 token recurrence, OpenMP over (row, head) chains"}
 
 
+DECODE_METRIC = "GDN decode rows/s (packed recurrent decode, fp32 state)"
+
+
+def decode_config(n_slots, world=1):
+    return {"workload": "decode_r256_h16_d128", "rows": DECODE_ROWS, "heads": H, "d_k": D, "d_v": D,
+            "cache_slots": n_slots, "state_bytes": DECODE_ROWS * H * D * D * 4,
+            "l2_policy": "inputs larger than L2 (256 MiB of states read+written per step)",
+            "parallelism": f"replicas x{world}"}
+
+
 def reference_arm(args):
     import torch
     world, rank, _ = dist_setup(torch)
@@ -448,12 +458,11 @@ def reference_arm(args):
         times.append(d)
     tot = sum(times)
     value = rows * args.steps / tot
-    line = {"impl": "reference", "metric": "GDN decode rows/s", "value": value, "unit": "rows/s",
+    line = {"impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "rows/s",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "decode_r256_h16_d128 (each step: a 64-row sample)",
-                       "rows_per_step": rows, "heads": H, "d": D},
+            "config": decode_config(2 * DECODE_ROWS),
             "cpu_baseline": {"value": value, "unit": "rows/s", "cores": threads, "kind": "oracle",
                              "sample": f"{rows} of the 256 decode rows per step, 1 recurrent step"},
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -517,14 +526,11 @@ def main():
     bytes_per_launch = DECODE_BYTES_PER_ROW * DECODE_ROWS
     achieved = bytes_per_launch / (launch_ms * 1e-3) / 1e9
     line = {
-        "metric": "GDN decode rows/s (packed recurrent decode, fp32 state)",
+        "metric": DECODE_METRIC,
         "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32 state / bf16 activations", "data": "synthetic",
-        "config": {"workload": wl["name"], "rows": DECODE_ROWS, "heads": H, "d_k": D, "d_v": D,
-                   "cache_slots": wl["n_slots"], "state_bytes": DECODE_ROWS * H * D * D * 4,
-                   "l2_policy": "inputs larger than L2 (256 MiB of states read+written per step)",
-                   "parallelism": f"replicas x{world}"},
+        "config": decode_config(wl["n_slots"], world),
         "roofline": {"bound": "hbm", "kernel": "decode_kernel<128>", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "traffic": measured_traffic("decode_kernel<128>"),
