@@ -315,6 +315,79 @@ def mixed_case(torch, gdn, dev, reps):
             "tokens_per_s": (nd + pre.total_tokens) / (ms * 1e-3), "colaunch_two_streams_ms": ms2}
 
 
+def multi_decode_case(torch, gdn, dev, peaks, rows=256, T=4, reps=10):
+    """Multi-token decode, 256 rows x 4 tokens (H=16, d=128): with a state
+    snapshot after every token, and with only the final state written back.
+    Algorithmic bytes per row: state read once + written per snapshot, plus
+    q, k, v, o (bf16) and g, beta (fp32) per token."""
+    b = gi.token_batch([T] * rows, H, H, D, 6, init_state=True)
+    n_slots = rows * (T + 1)
+    perm = np.random.default_rng(6).permutation(n_slots).astype(np.int32)
+    src, dsts = perm[:rows], perm[rows:].reshape(rows, T)
+    cache = torch.zeros((n_slots, H, D, D), dtype=torch.float32, device=dev)
+    cache[torch.from_numpy(src.astype(np.int64)).to(dev)] = \
+        torch.from_numpy(np.swapaxes(b.init_state, -1, -2).copy()).to(dev)
+    q, k, v = bf16(torch, b.q, dev), bf16(torch, b.k, dev), bf16(torch, b.v, dev)
+    g, beta = torch.from_numpy(b.g).to(dev), torch.from_numpy(b.beta).to(dev)
+    src_t, dst_t = torch.from_numpy(src).to(dev), torch.from_numpy(dsts.reshape(-1)).to(dev)
+    o = torch.empty((rows * T, H, D), dtype=torch.bfloat16, device=dev)
+    state_b = H * D * D * 4
+    tok_b = H * D * 2 * 4 + H * 4 * 2
+    out = {"workload": f"decode_multi_r{rows}_t{T}_h16_d128", "rows": rows, "tokens_per_row": T}
+    for name, dst, writes in (("snapshots", dst_t, T), ("final_only", None, 1)):
+        def call():
+            gdn.gdn_decode_multi(T, q, k, v, g, beta, cache, src_t, o, dst_slots=dst)
+        call()
+        torch.cuda.synchronize()
+        ev = []
+        for _ in range(reps):
+            a0, z0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record()
+            call()
+            z0.record()
+            ev.append((a0, z0))
+        torch.cuda.synchronize()
+        ms = statistics.median(a0.elapsed_time(z0) for a0, z0 in ev)
+        byts = rows * ((1 + writes) * state_b + T * tok_b)
+        gbs = byts / (ms * 1e-3) / 1e9
+        out[name] = {"ms": ms, "tokens_per_s": rows * T / (ms * 1e-3), "bytes_per_launch": byts,
+                     "roofline": {"bound": "hbm", "kernel": "decode_multi_kernel<128>", "achieved": gbs,
+                                  "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"]}}
+    return out
+
+
+def prep_case(torch, gdn, dev, peaks, T=131072, h_k=16, h_v=32, reps=10):
+    """Input preparation over 131072 tokens (H_k=16, H_v=32, d=128): q, k
+    read and written in bf16, a, b read and g, beta written in fp32."""
+    raw = gi.raw_inputs(T, h_k, h_v, D, 9)
+    q_raw, k_raw = bf16(torch, raw.q, dev), bf16(torch, raw.k, dev)
+    a, b_ = torch.from_numpy(raw.a).to(dev), torch.from_numpy(raw.b).to(dev)
+    A_log, dt_bias = torch.from_numpy(raw.A_log).to(dev), torch.from_numpy(raw.dt_bias).to(dev)
+    q, k = torch.empty_like(q_raw), torch.empty_like(k_raw)
+    g, beta = torch.empty_like(a), torch.empty_like(a)
+
+    def call():
+        gdn.gdn_prep_inputs(q_raw, k_raw, a, b_, A_log, dt_bias, q, k, g, beta)
+
+    call()
+    torch.cuda.synchronize()
+    ev = []
+    for _ in range(reps):
+        a0, z0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        call()
+        z0.record()
+        ev.append((a0, z0))
+    torch.cuda.synchronize()
+    ms = statistics.median(a0.elapsed_time(z0) for a0, z0 in ev)
+    byts = T * (2 * 2 * h_k * D * 2 + 4 * h_v * 4)
+    gbs = byts / (ms * 1e-3) / 1e9
+    return {"workload": f"prep_inputs_t{T}_hk{h_k}_hv{h_v}_d128", "ms": ms, "tokens_per_s": T / (ms * 1e-3),
+            "bytes_per_launch": byts,
+            "roofline": {"bound": "hbm", "kernel": "prep_kernel<128>", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"]}}
+
+
 def decode_latency_case(torch, gdn, dev, rows_list=(1, 8, 64, 256), iters=200):
     """Decode step latency per padded batch size: eager C-ABI calls from
     Python versus replay of a CUDA graph holding one step (H=16, d=128)."""
@@ -365,6 +438,10 @@ def run_extra(torch, gdn, dev, wanted, peaks, prefix_seqlen=32768):
         extra.append(mixed_case(torch, gdn, dev, reps=5))
     if "graph" in wanted:
         extra.append(decode_latency_case(torch, gdn, dev))
+    if "multi" in wanted:
+        extra.append(multi_decode_case(torch, gdn, dev, peaks))
+    if "prep" in wanted:
+        extra.append(prep_case(torch, gdn, dev, peaks))
     for x in extra:
         if "algorithmic_tflops" in x:
             x["roofline"] = {"bound": "tensor", "kernel": "prefill_chunk_tc_kernel<128>",
@@ -480,8 +557,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the prefill/mixed workloads")
-    ap.add_argument("--workloads", default="decode,prefill,prefix,mixed,graph",
-                    help="comma list of decode (headline), prefill, prefix, mixed, graph (decode latency)")
+    ap.add_argument("--workloads", default="decode,prefill,prefix,mixed,graph,multi,prep",
+                    help="comma list of decode (headline), prefill, prefix, mixed, graph (decode latency), "
+                         "multi (multi-token decode), prep (input preparation)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefix-seqlen", type=int, default=32768,
                     help="tokens per sequence of the prefix-cache workload (smaller for profiling captures)")

@@ -100,7 +100,7 @@ decode_kernel(const DecodeArgs a) {
 // to src_slot[r].  Every step is the same update_row as the packed decode, so
 // T tokens here equal T packed-decode calls bit for bit.
 template <int D>
-__global__ void __launch_bounds__(kDecodeThreads)
+__global__ void __launch_bounds__(kDecodeThreads, 2)
 decode_multi_kernel(const DecodeMultiArgs a) {
     constexpr int V4 = D / 32;
     constexpr int kItemsPerHead = D / kRowsPerItem;
