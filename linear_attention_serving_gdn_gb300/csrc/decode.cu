@@ -58,8 +58,7 @@ decode_kernel(const DecodeArgs a) {
             const int j = row0 + i * kRowsPerGroup + sub;
 #pragma unroll
             for (int m = 0; m < V4; ++m)
-                s[i][m] = __ldcg(reinterpret_cast<const float4 *>(sp + static_cast<size_t>(j) * D +
-                                                                  4 * (l8 + 8 * m)));
+                s[i][m] = ld_state4(sp + static_cast<size_t>(j) * D + 4 * (l8 + 8 * m));
         }
         const int kh = h / group;
         float kk[V4 * 4], qq[V4 * 4];
@@ -137,8 +136,7 @@ decode_multi_kernel(const DecodeMultiArgs a) {
             const int j = row0 + i * kRowsPerGroup + sub;
 #pragma unroll
             for (int m = 0; m < V4; ++m)
-                s[i][m] = __ldcg(reinterpret_cast<const float4 *>(sp + static_cast<size_t>(j) * D +
-                                                                  4 * (l8 + 8 * m)));
+                s[i][m] = ld_state4(sp + static_cast<size_t>(j) * D + 4 * (l8 + 8 * m));
         }
         for (int t = 0; t < T; ++t) {
             const size_t tok = static_cast<size_t>(r) * T + t;

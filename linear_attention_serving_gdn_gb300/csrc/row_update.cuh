@@ -19,6 +19,16 @@
 
 namespace gdn {
 
+// 16-byte state load, L2-only caching, with a 256-byte L2 fetch hint (the
+// lane octet's next segment of the same row is then an L2 hit).
+__device__ __forceinline__ float4 ld_state4(const float *p) {
+    float4 v;
+    asm volatile("ld.global.cg.L2::256B.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 template <int V4>
 __device__ __forceinline__ void load_bf16_slice(const uint16_t *p, int l8, float (&x)[V4 * 4]) {
 #pragma unroll
