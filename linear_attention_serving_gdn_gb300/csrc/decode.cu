@@ -7,10 +7,13 @@
 //
 // The kernel is bound by HBM: each (row, value head) state S^T [d_v][d_k] fp32
 // (64 KiB at d = 128) is read once and written once; q, k, v, g, beta and o
-// add about 1.6 %.  Work is split into items of 16 state rows (8 KiB); a
+// add about 1.6 %.  Work is split into items of 8 state rows (4 KiB); a
 // persistent grid of warps walks the items with a grid stride, so each warp
-// keeps 16 KiB of float4 loads in flight per item and the grid fills every SM
-// regardless of the row count.  Arithmetic per state row is in row_update.cuh.
+// has its item's loads in flight at once and the grid fills every SM
+// regardless of the row count.  State stores are streaming (.cs): the block
+// is not read again within the launch.  Measured, 8-row items with
+// streaming stores move the most bytes per second (16-row items or .cg
+// stores are ~3 % slower).  Arithmetic per state row is in row_update.cuh.
 #include "row_update.cuh"
 
 namespace gdn {
@@ -18,8 +21,8 @@ namespace {
 
 constexpr int kDecodeThreads = 256;
 constexpr int kRowsPerGroup = 4;  // rows of S^T per warp-wide access (lane octets)
-constexpr int kGroupsPerItem = 4;
-constexpr int kRowsPerItem = kRowsPerGroup * kGroupsPerItem;  // 16
+constexpr int kGroupsPerItem = 2;
+constexpr int kRowsPerItem = kRowsPerGroup * kGroupsPerItem;  // 8
 
 template <int D, bool kRaw>
 __global__ void __launch_bounds__(kDecodeThreads)
@@ -85,12 +88,18 @@ decode_kernel(const DecodeArgs a) {
             const float oj = update_row<V4>(s[i], kk, qq, alpha, beta, vj, kq, a.scale);
 #pragma unroll
             for (int m = 0; m < V4; ++m)
-                __stcg(reinterpret_cast<float4 *>(dp + static_cast<size_t>(j) * D + 4 * (l8 + 8 * m)),
+                __stcs(reinterpret_cast<float4 *>(dp + static_cast<size_t>(j) * D + 4 * (l8 + 8 * m)),
                        s[i][m]);
             if (l8 == 0) orow[j] = float_to_bf16_bits(oj);
         }
     }
 }
+
+// Items of the multi-token form: 16 rows, since every token of the row adds
+// q, k, v loads and reductions to the item (measured: 8-row items are ~15 %
+// slower here, unlike the single-token decode).
+constexpr int kMultiGroups = 4;
+constexpr int kMultiRows = kRowsPerGroup * kMultiGroups;  // 16
 
 // Multi-token decode (speculative tokens): the item's 16 state rows stay in
 // registers across the row's tokens; after token t the state is stored at
@@ -102,7 +111,7 @@ template <int D>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 decode_multi_kernel(const DecodeMultiArgs a) {
     constexpr int V4 = D / 32;
-    constexpr int kItemsPerHead = D / kRowsPerItem;
+    constexpr int kItemsPerHead = D / kMultiRows;
     const int lane = threadIdx.x & 31;
     const int sub = lane >> 3;
     const int l8 = lane & 7;
@@ -117,7 +126,7 @@ decode_multi_kernel(const DecodeMultiArgs a) {
         const int64_t rh = it / kItemsPerHead;
         const int h = static_cast<int>(rh % a.h_v);
         const int r = static_cast<int>(rh / a.h_v);
-        const int row0 = blk * kRowsPerItem;
+        const int row0 = blk * kMultiRows;
         const int kh = h / group;
 
         const int src = a.src_slot[r];
@@ -125,14 +134,14 @@ decode_multi_kernel(const DecodeMultiArgs a) {
             if (src >= 0) report(a.dev_status, GDN_DEV_BAD_SLOT);
             for (int t = 0; t < T; ++t) {
                 uint16_t *orow = a.o + ((static_cast<size_t>(r) * T + t) * a.h_v + h) * D;
-                if (lane < kRowsPerItem) orow[row0 + lane] = 0;
+                if (lane < kMultiRows) orow[row0 + lane] = 0;
             }
             continue;
         }
         const float *sp = a.state + (static_cast<size_t>(src) * a.h_v + h) * D * D;
-        float4 s[kGroupsPerItem][V4];
+        float4 s[kMultiGroups][V4];
 #pragma unroll
-        for (int i = 0; i < kGroupsPerItem; ++i) {
+        for (int i = 0; i < kMultiGroups; ++i) {
             const int j = row0 + i * kRowsPerGroup + sub;
 #pragma unroll
             for (int m = 0; m < V4; ++m)
@@ -161,14 +170,14 @@ decode_multi_kernel(const DecodeMultiArgs a) {
             }
             float *dp = dst >= 0 ? a.state + (static_cast<size_t>(dst) * a.h_v + h) * D * D : nullptr;
 #pragma unroll
-            for (int i = 0; i < kGroupsPerItem; ++i) {
+            for (int i = 0; i < kMultiGroups; ++i) {
                 const int j = row0 + i * kRowsPerGroup + sub;
                 const float vj = bf16_bits_to_float(vrow[j]);
                 const float oj = update_row<V4>(s[i], kk, qq, alpha, beta, vj, kq, a.scale);
                 if (dp) {
 #pragma unroll
                     for (int m = 0; m < V4; ++m)
-                        __stcg(reinterpret_cast<float4 *>(dp + static_cast<size_t>(j) * D + 4 * (l8 + 8 * m)),
+                        __stcs(reinterpret_cast<float4 *>(dp + static_cast<size_t>(j) * D + 4 * (l8 + 8 * m)),
                                s[i][m]);
                 }
                 if (l8 == 0) orow[j] = float_to_bf16_bits(oj);
@@ -186,7 +195,7 @@ cudaError_t launch_decode_multi_d(const DecodeMultiArgs &a, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_multi_kernel<D>, kDecodeThreads, 0);
     if (e != cudaSuccess) return e;
-    const int64_t items = static_cast<int64_t>(a.num_rows) * a.h_v * (D / kRowsPerItem);
+    const int64_t items = static_cast<int64_t>(a.num_rows) * a.h_v * (D / kMultiRows);
     const int64_t need = (items + (kDecodeThreads / 32) - 1) / (kDecodeThreads / 32);
     const int64_t cap = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
     const int grid = static_cast<int>(need < cap ? need : cap);
