@@ -19,7 +19,8 @@
 namespace gdn {
 namespace {
 
-constexpr int kDecodeThreads = 256;
+constexpr int kDecodeThreads = 128;  // measured best: 128 > 64 > 256 > 512 threads per block
+constexpr int kMultiThreads = 256;
 constexpr int kRowsPerGroup = 4;  // rows of S^T per warp-wide access (lane octets)
 constexpr int kGroupsPerItem = 2;
 constexpr int kRowsPerItem = kRowsPerGroup * kGroupsPerItem;  // 8
@@ -108,7 +109,7 @@ constexpr int kMultiRows = kRowsPerGroup * kMultiGroups;  // 16
 // to src_slot[r].  Every step is the same update_row as the packed decode, so
 // T tokens here equal T packed-decode calls bit for bit.
 template <int D>
-__global__ void __launch_bounds__(kDecodeThreads, 2)
+__global__ void __launch_bounds__(kMultiThreads, 2)
 decode_multi_kernel(const DecodeMultiArgs a) {
     constexpr int V4 = D / 32;
     constexpr int kItemsPerHead = D / kMultiRows;
@@ -193,13 +194,13 @@ cudaError_t launch_decode_multi_d(const DecodeMultiArgs &a, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_multi_kernel<D>, kDecodeThreads, 0);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_multi_kernel<D>, kMultiThreads, 0);
     if (e != cudaSuccess) return e;
     const int64_t items = static_cast<int64_t>(a.num_rows) * a.h_v * (D / kMultiRows);
-    const int64_t need = (items + (kDecodeThreads / 32) - 1) / (kDecodeThreads / 32);
+    const int64_t need = (items + (kMultiThreads / 32) - 1) / (kMultiThreads / 32);
     const int64_t cap = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
     const int grid = static_cast<int>(need < cap ? need : cap);
-    decode_multi_kernel<D><<<grid, kDecodeThreads, 0, stream>>>(a);
+    decode_multi_kernel<D><<<grid, kMultiThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
