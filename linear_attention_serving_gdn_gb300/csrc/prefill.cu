@@ -266,10 +266,17 @@ __device__ __forceinline__ void invert_diag_solve(const float *M, int p, float (
     }
 }
 
-__device__ __forceinline__ void invert_diag_store(float *M, int p, const float (&x)[16]) {
+// Also writes the block's columns of T'' = T diag(beta) as fp16 into the
+// 64-row K-major operand tile Tpp (upper blocks of Tpp stay zero).
+__device__ __forceinline__ void invert_diag_store(float *M, int p, const float (&x)[16], uint8_t *Tpp,
+                                                  const float *beta) {
     const int c = p & 15, base = ((p >> 4) & 3) * 16;
+    const float bc = beta[base + c];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) M[(base + i) * kLdM + base + c] = x[i];
+    for (int i = 0; i < 16; ++i) {
+        M[(base + i) * kLdM + base + c] = x[i];
+        *reinterpret_cast<__half *>(Tpp + tc::sw128_offset(base + i, base + c, 64)) = __float2half_rn(x[i] * bc);
+    }
 }
 
 __device__ __forceinline__ void fma4(float4 &acc, float a, const float4 &t) {
@@ -283,8 +290,8 @@ __device__ __forceinline__ void fma4(float4 &acc, float a, const float4 &t) {
 // b < a.  Thread p < 64 a owns block b = p / 64, row i = (p / 4) % 16 and the
 // four columns 4 (p % 4) .. + 3 of T_ab (float4 accesses; b is uniform over a
 // warp).  A_ab is overwritten only after the block row's products.
-template <int A_ROW>
-__device__ __forceinline__ void invert_block_row(float *M, float *W, int p) {
+template <int A_ROW, bool kLast>
+__device__ __forceinline__ void invert_block_row(float *M, float *W, int p, uint8_t *Tpp, const float *beta) {
     const int b = min((p >> 6) & 3, A_ROW - 1), i = (p >> 2) & 15, cq = p & 3;  // b < A_ROW for every p
     const int row = A_ROW * 16 + i;
     const bool active = p < A_ROW * 64;
@@ -318,8 +325,14 @@ __device__ __forceinline__ void invert_block_row(float *M, float *W, int p) {
             fma4(acc, t4.w, *reinterpret_cast<const float4 *>(w + 48));
         }
         *reinterpret_cast<float4 *>(M + row * kLdM + b * 16 + 4 * cq) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        const int col = b * 16 + 4 * cq;  // T''[row][col..col+3] = T diag(beta), 8 bytes of one chunk
+        const float4 b4 = *reinterpret_cast<const float4 *>(beta + col);
+        uint2 h;
+        h.x = pack_half2(-acc.x * b4.x, -acc.y * b4.y);
+        h.y = pack_half2(-acc.z * b4.z, -acc.w * b4.w);
+        *reinterpret_cast<uint2 *>(Tpp + tc::sw128_offset(row, col, 64)) = h;
     }
-    group_sync(kBarPrep);
+    if (!kLast) group_sync(kBarPrep);  // the last row's barrier is the caller's
 }
 
 template <int D>
@@ -387,6 +400,8 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
         tc::mbar_init(tma_bar + 1, 1);
         *fail = 0;
     }
+    for (int e = tid; e < 2 * 8192 / 16; e += kThreads)  // upper blocks of T'' stay zero
+        reinterpret_cast<uint4 *>(sm + SM::kTpp0)[e] = make_uint4(0, 0, 0, 0);
     if (D < 128) {  // rows >= D of the transposed operand tiles stay zero (d = 64 pads M to 128)
         for (int e = tid; e < 128 * D * 2 / 16; e += kThreads)
             reinterpret_cast<uint4 *>(sS0T)[e] = make_uint4(0, 0, 0, 0);
@@ -738,14 +753,14 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                     if (l >= o) incl += y;
                 }
                 const float excl = incl - pair;
-                sG[2 * l] = excl + g0;
-                sG[2 * l + 1] = excl + g0 + g1;
-            }
-            group_sync(kBarPrep);
-            if (pid < 64) {
-                const int t = pid & 63;
-                sGam(s)[t] = expf(sG[t]);
-                sDec[t] = expf(sG[63] - sG[t]);
+                const float G0 = excl + g0, G1 = excl + g0 + g1;
+                const float Gc = __shfl_sync(0xffffffffu, G1, 31);  // G_63, the chunk total
+                sG[2 * l] = G0;
+                sG[2 * l + 1] = G1;
+                sGam(s)[2 * l] = expf(G0);
+                sGam(s)[2 * l + 1] = expf(G1);
+                sDec[2 * l] = expf(Gc - G0);
+                sDec[2 * l + 1] = expf(Gc - G1);
             }
             tc::fence_proxy_async_smem();
             tc::fence_before_sync();
@@ -833,7 +848,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 }
             }
             group_sync(kBarPrep);
-            if (pid < 64) invert_diag_store(sM, pid, xd);
+            if (pid < 64) invert_diag_store(sM, pid, xd, sTpp(s), sBeta);
             // ---- the next chunk's q, k copies, once its stage is free --------------------
             if (c + 1 < n_chunks) {
                 const bool ok = c + 1 < 2 || mbar_wait_bounded(freeb + (s ^ 1), ((c - 1) >> 1) & 1);
@@ -845,27 +860,10 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             } else {
                 group_sync(kBarPrep);
             }
-            invert_block_row<1>(sM, sW, pid);
-            invert_block_row<2>(sM, sW, pid);
-            invert_block_row<3>(sM, sW, pid);
-
-            // ---- T'' = T diag(beta): items (row t, 16 columns) ------------------------
-            {
-                const int t = (pid >> 2) & 63, quarter = pid & 3;
-                float x[16];
-#pragma unroll
-                for (int u = 0; u < 16; u += 4) {
-                    const int q = quarter * 16 + u;
-                    const float4 m4 = *reinterpret_cast<const float4 *>(sM + t * kLdM + q);
-                    const float4 b4 = *reinterpret_cast<const float4 *>(sBeta + q);
-                    x[u + 0] = (q + 0 <= t) ? m4.x * b4.x : 0.f;
-                    x[u + 1] = (q + 1 <= t) ? m4.y * b4.y : 0.f;
-                    x[u + 2] = (q + 2 <= t) ? m4.z * b4.z : 0.f;
-                    x[u + 3] = (q + 3 <= t) ? m4.w * b4.w : 0.f;
-                }
-                store_chunk8_f16(sTpp(s), 64, t, 2 * quarter, x);
-                store_chunk8_f16(sTpp(s), 64, t, 2 * quarter + 1, x + 8);
-            }
+            // T'' = T diag(beta) is written as fp16 by the inverse itself.
+            invert_block_row<1, false>(sM, sW, pid, sTpp(s), sBeta);
+            invert_block_row<2, false>(sM, sW, pid, sTpp(s), sBeta);
+            invert_block_row<3, true>(sM, sW, pid, sTpp(s), sBeta);
             tc::fence_proxy_async_smem();
             mbar_arrive(ready + s);
             group_sync(kBarPrep);  // scratch reuse by the next chunk
