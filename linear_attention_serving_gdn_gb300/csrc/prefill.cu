@@ -707,6 +707,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             const int n = min(kChunk, Lseq - c * kChunk);
             // ---- q, k tiles (copied during the previous chunk) to fp16; g, beta ----------
             uint8_t *qk = sQK(s);
+            bool okt;
             {
                 if (c + 2 < n_chunks && pid < 128) {  // q, k rows of chunk c + 2 into L2
                     const int rn = min(kChunk, Lseq - (c + 2) * kChunk);
@@ -718,14 +719,10 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                         if (D > 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(src_row + 64) : "memory");
                     }
                 }
-                const bool okt = mbar_wait_bounded(tma_bar + s, (c >> 1) & 1);
-                if (group_any(kBarPrep, !okt)) {
-                    failed = true;
-                    break;
-                }
+                okt = mbar_wait_bounded(tma_bar + s, (c >> 1) & 1);
                 // rows past the sequence end (the next sequence's tokens) become zeros
 #pragma unroll
-                for (int it = 0; it < kPer; ++it) {
+                for (int it = 0; it < kPer && okt; ++it) {
                     const int e = pid + it * kGroup;
                     const int r = e / (D / 8), c8 = e % (D / 8);
                     uint4 *pq = reinterpret_cast<uint4 *>(qk + tc::sw128_chunk_offset(r, c8, 128));
@@ -741,7 +738,10 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                     sBeta[t] = t < n ? bv : 0.f;
                 }
             }
-            group_sync(kBarPrep);
+            if (group_any(kBarPrep, !okt)) {  // a copy that never landed: stop (bounded)
+                failed = true;
+                break;
+            }
             if (pid < 32) {  // inclusive prefix sum of g over the chunk, fixed order
                 const int l = pid & 31;
                 const float g0 = sGraw[2 * l], g1 = sGraw[2 * l + 1];
@@ -778,18 +778,17 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 tc::mma_commit(gram_bar);
             }
             __syncwarp();
-            const bool okg = mbar_wait_bounded(gram_bar, c & 1);
-            if (group_any(kBarPrep, !okg)) {
-                failed = true;
-                mbar_wait_bounded(gram_bar, c & 1);  // let an issued Gram finish before TMEM is freed
-                break;
-            }
+            // Each warp reads the Gram only once every lane saw it complete; a
+            // failure is agreed on at the barrier after P and A.
+            const bool okg = __all_sync(0xffffffffu, mbar_wait_bounded(gram_bar, c & 1));
             tc::fence_after_sync();
 
             // ---- P rows (lanes 0..63) and A rows (lanes 64..127), columns 32 hf.. ----
             // Rows 0..31 x columns 32..63 are masked (warp-uniform): P gets zeros,
             // the upper triangle of A is never read.
-            if (hf == 1 && (p & 32) == 0) {
+            if (!okg) {
+                // nothing: the barrier below ends the loop
+            } else if (hf == 1 && (p & 32) == 0) {
                 if (p < 64) {
                     const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
@@ -825,7 +824,11 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 }
             }
             tc::fence_before_sync();
-            group_sync(kBarPrep);
+            if (group_any(kBarPrep, !okg)) {
+                failed = true;
+                mbar_wait_bounded(gram_bar, c & 1);  // let an issued Gram finish before TMEM is freed
+                break;
+            }
 
             // ---- T = (I + A)^-1 (diagonal blocks) || Ktil^T --------------------------
             float xd[16];
