@@ -850,8 +850,13 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                     for (int q = 0; q < 4; ++q) store_chunk8_f16(sKtT(s), D, i, 4 * half + q, x + 8 * q);
                 }
             }
-            group_sync(kBarPrep);
-            if (pid < 64) invert_diag_store(sM, pid, xd, sTpp(s), sBeta);
+            // A diagonal block is solved and stored by the 16 lanes of one half
+            // warp (warps 8 and 9): a warp barrier orders its reads before the
+            // store; the group barrier below orders the store before the rows.
+            if (pid < 64) {
+                __syncwarp();
+                invert_diag_store(sM, pid, xd, sTpp(s), sBeta);
+            }
             // ---- the next chunk's q, k copies, once its stage is free --------------------
             if (c + 1 < n_chunks) {
                 const bool ok = c + 1 < 2 || mbar_wait_bounded(freeb + (s ^ 1), ((c - 1) >> 1) & 1);
