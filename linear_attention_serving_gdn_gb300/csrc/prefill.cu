@@ -732,15 +732,28 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                     *pq = r < n ? bf16x8_to_f16x8(xq) : z;
                     *pk = r < n ? bf16x8_to_f16x8(xk) : z;
                 }
+                tc::fence_proxy_async_smem();  // the converted tile is read by the Gram MMA
                 if (pid < 64) {
                     const int t = pid & 63;
                     sGraw[t] = t < n ? gv : 0.f;
                     sBeta[t] = t < n ? bv : 0.f;
                 }
             }
+            tc::fence_before_sync();
             if (group_any(kBarPrep, !okt)) {  // a copy that never landed: stop (bounded)
                 failed = true;
                 break;
+            }
+            // ---- Gram [Q;K] K^T (issued by warp 9 while warp 8 runs the prefix sum) --
+            if (pid == 32) {
+                tc::fence_after_sync();
+                const uint64_t dQK = tc::desc_k_sw128(tc::smem_u32(qk));
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4;
+                    tc::mma_f16(tbase + kColGram, dQK + off, dQK + off + (64 * 128 >> 4), aIdGram, kk > 0);
+                }
+                tc::mma_commit(gram_bar);
             }
             if (pid < 32) {  // inclusive prefix sum of g over the chunk, fixed order
                 const int l = pid & 31;
@@ -762,21 +775,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 sDec[2 * l] = expf(Gc - G0);
                 sDec[2 * l + 1] = expf(Gc - G1);
             }
-            tc::fence_proxy_async_smem();
-            tc::fence_before_sync();
-            group_sync(kBarPrep);
-
-            // ---- Gram [Q;K] K^T --------------------------------------------------------
-            if (pid == 0) {
-                tc::fence_after_sync();
-                const uint64_t dQK = tc::desc_k_sw128(tc::smem_u32(qk));
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = ((kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4;
-                    tc::mma_f16(tbase + kColGram, dQK + off, dQK + off + (64 * 128 >> 4), aIdGram, kk > 0);
-                }
-                tc::mma_commit(gram_bar);
-            }
+            group_sync(kBarPrep);  // g cumsum, gamma, dec visible
             __syncwarp();
             // Each warp reads the Gram only once every lane saw it complete; a
             // failure is agreed on at the barrier after P and A.
