@@ -484,7 +484,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 *reinterpret_cast<uint4 *>(a.o + static_cast<size_t>(tok_out + t) * ldv + static_cast<size_t>(h) * D +
                                            cc * 8) = *reinterpret_cast<const uint4 *>(sOst + t * D + cc * 8);
             }
-            group_sync(kBarChain);
+            // the staging tile is next written by C2, after the S1 barrier
         };
 
         for (int c = 0; c < n_chunks; ++c) {
@@ -579,14 +579,11 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             tc::fence_before_sync();
 
             // ---- C4: U^T to fp16; D5 += U^T Ktil, D6 = U^T P^T --------------------
-            const bool ok2 = mbar_wait_bounded(mma_bar, mma_phase);
+            // (a failed wait is agreed on at the barrier that follows the phase)
+            const bool ok2 = __all_sync(0xffffffffu, mbar_wait_bounded(mma_bar, mma_phase));
             mma_phase ^= 1u;
-            if (group_any(kBarChain, !ok2)) {
-                failed = true;
-                break;
-            }
             tc::fence_after_sync();
-            if (j < D) {
+            if (ok2 && j < D) {
                 float u[32];
                 tmem_load_row<32>(d1_lane + 64 + 32 * hf, u);
 #pragma unroll
@@ -594,7 +591,10 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             }
             tc::fence_proxy_async_smem();
             tc::fence_before_sync();
-            group_sync(kBarChain);
+            if (group_any(kBarChain, !ok2)) {
+                failed = true;
+                break;
+            }
             if (tid == 0) {
                 tc::fence_after_sync();
                 const uint64_t dKt = tc::desc_k_sw128(tc::smem_u32(sKtT(s)));
@@ -608,15 +608,11 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             __syncwarp();
 
             // ---- C6: new state -> S0^T tile, emission, final state -----------------
-            const bool ok3 = mbar_wait_bounded(mma_bar, mma_phase);
+            const bool ok3 = __all_sync(0xffffffffu, mbar_wait_bounded(mma_bar, mma_phase));
             mma_phase ^= 1u;
-            if (group_any(kBarChain, !ok3)) {
-                failed = true;
-                break;
-            }
             tc::fence_after_sync();
-            mbar_arrive(freeb + s);  // every MMA and read of this chunk's stage is done
-            if (j < D) {
+            if (ok3) mbar_arrive(freeb + s);  // every MMA and read of this chunk's stage is done
+            if (ok3 && j < D) {
                 float *ep = nullptr;
                 if (E > 0 && n == kChunk && ((c + 1) % E) == 0) {
                     if (a.emit_table) {  // emission k of this sequence -> its cache block's slot
@@ -653,7 +649,10 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             }
             tc::fence_proxy_async_smem();
             tc::fence_before_sync();
-            group_sync(kBarChain);
+            if (group_any(kBarChain, !ok3)) {
+                failed = true;
+                break;
+            }
             prev_n = n;
             prev_tok0 = tok0;
         }
