@@ -506,15 +506,12 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             }
 
             // ---- wait for the chunk's operands ---------------------------------
-            const bool ok_ready = mbar_wait_bounded(ready + s, (c >> 1) & 1);
-            if (group_any(kBarChain, !ok_ready)) {
-                failed = true;
-                break;
-            }
+            // (a failed wait is agreed on at the S1 barrier below)
+            const bool ok_ready = __all_sync(0xffffffffu, mbar_wait_bounded(ready + s, (c >> 1) & 1));
             tc::fence_after_sync();
 
             // ---- S1: D1 = S0^T [Q;K]^T --------------------------------------------
-            if (tid == 0) {
+            if (tid == 0 && ok_ready) {
                 const uint64_t dQK = tc::desc_k_sw128(tc::smem_u32(sQK(s)));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -524,7 +521,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 tc::mma_commit(mma_bar);
             }
             __syncwarp();
-            if (tid < 64) sGamC(s)[tid & 63] = sGam(s)[tid & 63];  // kept for the output of this chunk
+            if (tid < 64 && ok_ready) sGamC(s)[tid & 63] = sGam(s)[tid & 63];  // kept for the output of this chunk
             // values -> staging tile (the U^T tile is free until C4 of this chunk)
 #pragma unroll
             for (int it = 0; it < kPerV; ++it) {
@@ -539,7 +536,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             // ---- C2: V'^T = V^T - (K S0)^T diag(gamma) --------------------------
             const bool ok1 = mbar_wait_bounded(mma_bar, mma_phase);
             mma_phase ^= 1u;
-            if (group_any(kBarChain, !ok1)) {
+            if (group_any(kBarChain, !ok1 || !ok_ready)) {
                 failed = true;
                 break;
             }
