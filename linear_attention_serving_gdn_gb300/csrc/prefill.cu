@@ -92,8 +92,8 @@ struct Smem {
     static constexpr uint32_t kGam1 = kGam0 + 256;
     static constexpr uint32_t kGamC = kGam1 + 256;             // f32 [2][64] chain group's copies
     static constexpr uint32_t kM = kGamC + 512;                // f32 [64][kLdM] A, then T
-    static constexpr uint32_t kW = kM + 64 * 68 * 4;           // f32 [3][16][16] block products
-    static constexpr uint32_t kG = kW + 3072;                  // f32 [64] cumulative log decay
+    static constexpr uint32_t kW = kM + 64 * 68 * 4;           // f32 [4][16][16] block products
+    static constexpr uint32_t kG = kW + 4096;                  // f32 [64] cumulative log decay
     static constexpr uint32_t kBeta = kG + 256;                // f32 [64]
     static constexpr uint32_t kGraw = kBeta + 256;             // f32 [64]
     static constexpr uint32_t kDec = kGraw + 256;              // f32 [64] exp(G_C - G_t)
@@ -333,6 +333,95 @@ __device__ __forceinline__ void invert_block_row(float *M, float *W, int p, uint
         *reinterpret_cast<uint2 *>(Tpp + tc::sw128_offset(row, col, 64)) = h;
     }
     if (!kLast) group_sync(kBarPrep);  // the last row's barrier is the caller's
+}
+
+// Part 2, as two doubling levels instead of block rows (the same 16 block
+// products in four phases instead of six): with T_aa the inverted diagonal
+// blocks,
+//   level 1 (pairs of 16-blocks):  T_10 = -T_11 (A_10 T_00),  T_32 = -T_33 (A_32 T_22);
+//   level 2 (rows 32..63 x columns 0..31):  X = A_B T_top,  T_B = -T_bottom X,
+//   T_top = [[T_00, 0], [T_10, T_11]],  T_bottom = [[T_22, 0], [T_32, T_33]],
+//   i.e. X_a0 = A_a0 T_00 + A_a1 T_10, X_a1 = A_a1 T_11 (a = 2, 3),
+//        T_2b = -T_22 X_2b,  T_3b = -(T_32 X_2b + T_33 X_3b).
+// Each output 16x16 block is computed by 64 threads (row i = (p/4) % 16,
+// columns 4 (p%4) .. + 3, float4 accesses); block indices are compile-time
+// per 64-thread task.  Results go to M and, scaled by beta, as fp16 to the
+// T'' tile.  The caller provides the barrier after the last phase.
+template <int LDX, int LDY>
+__device__ __forceinline__ void block_mac(float4 &acc, const float *X, const float *Y, int i, int cq) {
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+        const float4 x4 = *reinterpret_cast<const float4 *>(X + i * LDX + 4 * k4);
+        const float *y = Y + (4 * k4) * LDY + 4 * cq;
+        fma4(acc, x4.x, *reinterpret_cast<const float4 *>(y));
+        fma4(acc, x4.y, *reinterpret_cast<const float4 *>(y + LDY));
+        fma4(acc, x4.z, *reinterpret_cast<const float4 *>(y + 2 * LDY));
+        fma4(acc, x4.w, *reinterpret_cast<const float4 *>(y + 3 * LDY));
+    }
+}
+
+template <int A, int B>
+__device__ __forceinline__ void store_t_block(float *M, uint8_t *Tpp, const float *beta, int i, int cq,
+                                              const float4 &acc) {
+    const int row = A * 16 + i, col = B * 16 + 4 * cq;
+    *reinterpret_cast<float4 *>(M + row * kLdM + col) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    const float4 b4 = *reinterpret_cast<const float4 *>(beta + col);
+    uint2 hv;
+    hv.x = pack_half2(-acc.x * b4.x, -acc.y * b4.y);
+    hv.y = pack_half2(-acc.z * b4.z, -acc.w * b4.w);
+    *reinterpret_cast<uint2 *>(Tpp + tc::sw128_offset(row, col, 64)) = hv;
+}
+
+#define GDN_MB(a, b) (M + ((a) * 16) * kLdM + (b) * 16)
+template <int A>  // level 1, first half: W[A == 3] = A_{A,A-1} T_{A-1,A-1}
+__device__ __forceinline__ void l1_y(float *M, float *W, int i, int cq) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    block_mac<kLdM, kLdM>(acc, GDN_MB(A, A - 1), GDN_MB(A - 1, A - 1), i, cq);
+    *reinterpret_cast<float4 *>(W + (A == 3 ? 256 : 0) + i * 16 + 4 * cq) = acc;
+}
+template <int A>  // level 1, second half: T_{A,A-1} = -T_AA W
+__device__ __forceinline__ void l1_t(float *M, float *W, int i, int cq, uint8_t *Tpp, const float *beta) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    block_mac<kLdM, 16>(acc, GDN_MB(A, A), W + (A == 3 ? 256 : 0), i, cq);
+    store_t_block<A, A - 1>(M, Tpp, beta, i, cq, acc);
+}
+template <int A, int B>  // level 2, X_AB into W block 2 (A - 2) + B
+__device__ __forceinline__ void l2_x(float *M, float *W, int i, int cq) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (B == 0) block_mac<kLdM, kLdM>(acc, GDN_MB(A, 0), GDN_MB(0, 0), i, cq);
+    block_mac<kLdM, kLdM>(acc, GDN_MB(A, 1), GDN_MB(1, B), i, cq);
+    *reinterpret_cast<float4 *>(W + (2 * (A - 2) + B) * 256 + i * 16 + 4 * cq) = acc;
+}
+template <int A, int B>  // level 2, T_AB = -(T_A2 X_2B + [A == 3] T_33 X_3B)
+__device__ __forceinline__ void l2_t(float *M, float *W, int i, int cq, uint8_t *Tpp, const float *beta) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    block_mac<kLdM, 16>(acc, GDN_MB(A, 2), W + B * 256, i, cq);
+    if (A == 3) block_mac<kLdM, 16>(acc, GDN_MB(3, 3), W + (2 + B) * 256, i, cq);
+    store_t_block<A, B>(M, Tpp, beta, i, cq, acc);
+}
+#undef GDN_MB
+
+__device__ __forceinline__ void invert_offdiag(float *M, float *W, int p, uint8_t *Tpp, const float *beta) {
+    const int task = (p >> 6) & 3, i = (p >> 2) & 15, cq = p & 3;  // task uniform over 2 warps
+    if (task == 0) l1_y<1>(M, W, i, cq);
+    else if (task == 1) l1_y<3>(M, W, i, cq);
+    group_sync(kBarPrep);
+    if (task == 0) l1_t<1>(M, W, i, cq, Tpp, beta);
+    else if (task == 1) l1_t<3>(M, W, i, cq, Tpp, beta);
+    group_sync(kBarPrep);
+    switch (task) {
+        case 0: l2_x<2, 0>(M, W, i, cq); break;
+        case 1: l2_x<2, 1>(M, W, i, cq); break;
+        case 2: l2_x<3, 0>(M, W, i, cq); break;
+        default: l2_x<3, 1>(M, W, i, cq); break;
+    }
+    group_sync(kBarPrep);
+    switch (task) {
+        case 0: l2_t<2, 0>(M, W, i, cq, Tpp, beta); break;
+        case 1: l2_t<2, 1>(M, W, i, cq, Tpp, beta); break;
+        case 2: l2_t<3, 0>(M, W, i, cq, Tpp, beta); break;
+        default: l2_t<3, 1>(M, W, i, cq, Tpp, beta); break;
+    }
 }
 
 template <int D>
@@ -864,9 +953,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 group_sync(kBarPrep);
             }
             // T'' = T diag(beta) is written as fp16 by the inverse itself.
-            invert_block_row<1, false>(sM, sW, pid, sTpp(s), sBeta);
-            invert_block_row<2, false>(sM, sW, pid, sTpp(s), sBeta);
-            invert_block_row<3, true>(sM, sW, pid, sTpp(s), sBeta);
+            invert_offdiag(sM, sW, pid, sTpp(s), sBeta);
             tc::fence_proxy_async_smem();
             mbar_arrive(ready + s);
             group_sync(kBarPrep);  // scratch reuse by the next chunk
