@@ -343,9 +343,10 @@ __device__ __forceinline__ void invert_block_row(float *M, float *W, int p, uint
 //   T_top = [[T_00, 0], [T_10, T_11]],  T_bottom = [[T_22, 0], [T_32, T_33]],
 //   i.e. X_a0 = A_a0 T_00 + A_a1 T_10, X_a1 = A_a1 T_11 (a = 2, 3),
 //        T_2b = -T_22 X_2b,  T_3b = -(T_32 X_2b + T_33 X_3b).
-// Each output 16x16 block is computed by 64 threads (row i = (p/4) % 16,
-// columns 4 (p%4) .. + 3, float4 accesses); block indices are compile-time
-// per 64-thread task.  Results go to M and, scaled by beta, as fp16 to the
+// Level 1 runs in the two warps that solved the diagonal blocks (warp
+// barriers only); each level-2 output 16x16 block is computed by 64 threads
+// (row i = (p/4) % 16, columns 4 (p%4) .. + 3, float4 accesses) with
+// compile-time block indices per task.  Results go to M and, scaled by beta, as fp16 to the
 // T'' tile.  The caller provides the barrier after the last phase.
 template <int LDX, int LDY>
 __device__ __forceinline__ void block_mac(float4 &acc, const float *X, const float *Y, int i, int cq) {
@@ -373,18 +374,30 @@ __device__ __forceinline__ void store_t_block(float *M, uint8_t *Tpp, const floa
 }
 
 #define GDN_MB(a, b) (M + ((a) * 16) * kLdM + (b) * 16)
-template <int A>  // level 1, first half: W[A == 3] = A_{A,A-1} T_{A-1,A-1}
-__device__ __forceinline__ void l1_y(float *M, float *W, int i, int cq) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    block_mac<kLdM, kLdM>(acc, GDN_MB(A, A - 1), GDN_MB(A - 1, A - 1), i, cq);
-    *reinterpret_cast<float4 *>(W + (A == 3 ? 256 : 0) + i * 16 + 4 * cq) = acc;
+// Level 1 by one warp (the warp that solved diagonal blocks A-1 and A):
+// lane = (row i = lane / 2, columns 8 (lane % 2) .. + 7), two float4 each;
+// Y_{A,A-1} = A_{A,A-1} T_{A-1,A-1} into W block (A == 3), then
+// T_{A,A-1} = -T_AA Y, with warp barriers only.
+template <int A>
+__device__ __forceinline__ void level1_warp(float *M, float *W, int lane, uint8_t *Tpp, const float *beta) {
+    const int i = (lane >> 1) & 15, h = lane & 1;
+    float *Wy = W + (A == 3 ? 256 : 0);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        block_mac<kLdM, kLdM>(acc, M + (A * 16) * kLdM + (A - 1) * 16, M + ((A - 1) * 16) * kLdM + (A - 1) * 16, i,
+                              2 * h + u);
+        *reinterpret_cast<float4 *>(Wy + i * 16 + 4 * (2 * h + u)) = acc;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        block_mac<kLdM, 16>(acc, M + (A * 16) * kLdM + A * 16, Wy, i, 2 * h + u);
+        store_t_block<A, A - 1>(M, Tpp, beta, i, 2 * h + u, acc);
+    }
 }
-template <int A>  // level 1, second half: T_{A,A-1} = -T_AA W
-__device__ __forceinline__ void l1_t(float *M, float *W, int i, int cq, uint8_t *Tpp, const float *beta) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    block_mac<kLdM, 16>(acc, GDN_MB(A, A), W + (A == 3 ? 256 : 0), i, cq);
-    store_t_block<A, A - 1>(M, Tpp, beta, i, cq, acc);
-}
+
 template <int A, int B>  // level 2, X_AB into W block 2 (A - 2) + B
 __device__ __forceinline__ void l2_x(float *M, float *W, int i, int cq) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -401,14 +414,9 @@ __device__ __forceinline__ void l2_t(float *M, float *W, int i, int cq, uint8_t 
 }
 #undef GDN_MB
 
+// Level 2 (level 1 was done per warp right after the diagonal blocks).
 __device__ __forceinline__ void invert_offdiag(float *M, float *W, int p, uint8_t *Tpp, const float *beta) {
     const int task = (p >> 6) & 3, i = (p >> 2) & 15, cq = p & 3;  // task uniform over 2 warps
-    if (task == 0) l1_y<1>(M, W, i, cq);
-    else if (task == 1) l1_y<3>(M, W, i, cq);
-    group_sync(kBarPrep);
-    if (task == 0) l1_t<1>(M, W, i, cq, Tpp, beta);
-    else if (task == 1) l1_t<3>(M, W, i, cq, Tpp, beta);
-    group_sync(kBarPrep);
     switch (task) {
         case 0: l2_x<2, 0>(M, W, i, cq); break;
         case 1: l2_x<2, 1>(M, W, i, cq); break;
@@ -936,10 +944,14 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             }
             // A diagonal block is solved and stored by the 16 lanes of one half
             // warp (warps 8 and 9): a warp barrier orders its reads before the
-            // store; the group barrier below orders the store before the rows.
+            // store, and the same warp then builds level 1 of the off-diagonal
+            // part; the group barrier below orders both before level 2.
             if (pid < 64) {
                 __syncwarp();
                 invert_diag_store(sM, pid, xd, sTpp(s), sBeta);
+                __syncwarp();  // warp 8 holds blocks 0, 1 and warp 9 blocks 2, 3: level 1 per warp
+                if (pid < 32) level1_warp<1>(sM, sW, pid & 31, sTpp(s), sBeta);
+                else level1_warp<3>(sM, sW, pid & 31, sTpp(s), sBeta);
             }
             // ---- the next chunk's q, k copies, once its stage is free --------------------
             if (c + 1 < n_chunks) {
