@@ -36,8 +36,9 @@
 //     S1 -> V' -> S3 -> U -> S5/S6 -> new state, plus the output of the
 //     previous chunk while S1 runs;
 //   prep group (warps 8-15, lanes split the same way): the chunk-local
-//     operands of the next chunk
-//     (fp16 Q/K tiles, decays, Gram, P, A, T = (I + A)^-1, T'') into a
+//     operands of the next chunk -- Q/K tiles (TMA, one chunk ahead, fp16 in
+//     place), decays, Gram, P, A, T = (I + A)^-1 (diagonal 16x16 blocks by
+//     substitution, then two doubling levels), T'' and Ktil -- into a
 //     double-buffered stage, handed over through mbarriers.
 // A chunk's arithmetic depends only on its own inputs and the fp32 state
 // entering it, so results do not depend on the batch, and restarting from an
@@ -286,57 +287,8 @@ __device__ __forceinline__ void fma4(float4 &acc, float a, const float4 &t) {
     acc.w = fmaf(a, t.w, acc.w);
 }
 
-// Part 2: block rows a = 1..3, T_ab = -T_aa sum_{b<=m<a} A_am T_mb for every
-// b < a.  Thread p < 64 a owns block b = p / 64, row i = (p / 4) % 16 and the
-// four columns 4 (p % 4) .. + 3 of T_ab (float4 accesses; b is uniform over a
-// warp).  A_ab is overwritten only after the block row's products.
-template <int A_ROW, bool kLast>
-__device__ __forceinline__ void invert_block_row(float *M, float *W, int p, uint8_t *Tpp, const float *beta) {
-    const int b = min((p >> 6) & 3, A_ROW - 1), i = (p >> 2) & 15, cq = p & 3;  // b < A_ROW for every p
-    const int row = A_ROW * 16 + i;
-    const bool active = p < A_ROW * 64;
-    if (active) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int m = 0; m < A_ROW; ++m) {
-            if (m < b) continue;
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(M + row * kLdM + m * 16 + 4 * k4);
-                const float *t = M + (m * 16 + 4 * k4) * kLdM + b * 16 + 4 * cq;
-                fma4(acc, a4.x, *reinterpret_cast<const float4 *>(t));
-                fma4(acc, a4.y, *reinterpret_cast<const float4 *>(t + kLdM));
-                fma4(acc, a4.z, *reinterpret_cast<const float4 *>(t + 2 * kLdM));
-                fma4(acc, a4.w, *reinterpret_cast<const float4 *>(t + 3 * kLdM));
-            }
-        }
-        *reinterpret_cast<float4 *>(W + (b * 16 + i) * 16 + 4 * cq) = acc;
-    }
-    group_sync(kBarPrep);
-    if (active) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-            const float4 t4 = *reinterpret_cast<const float4 *>(M + row * kLdM + A_ROW * 16 + 4 * k4);
-            const float *w = W + (b * 16 + 4 * k4) * 16 + 4 * cq;
-            fma4(acc, t4.x, *reinterpret_cast<const float4 *>(w));
-            fma4(acc, t4.y, *reinterpret_cast<const float4 *>(w + 16));
-            fma4(acc, t4.z, *reinterpret_cast<const float4 *>(w + 32));
-            fma4(acc, t4.w, *reinterpret_cast<const float4 *>(w + 48));
-        }
-        *reinterpret_cast<float4 *>(M + row * kLdM + b * 16 + 4 * cq) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-        const int col = b * 16 + 4 * cq;  // T''[row][col..col+3] = T diag(beta), 8 bytes of one chunk
-        const float4 b4 = *reinterpret_cast<const float4 *>(beta + col);
-        uint2 h;
-        h.x = pack_half2(-acc.x * b4.x, -acc.y * b4.y);
-        h.y = pack_half2(-acc.z * b4.z, -acc.w * b4.w);
-        *reinterpret_cast<uint2 *>(Tpp + tc::sw128_offset(row, col, 64)) = h;
-    }
-    if (!kLast) group_sync(kBarPrep);  // the last row's barrier is the caller's
-}
-
-// Part 2, as two doubling levels instead of block rows (the same 16 block
-// products in four phases instead of six): with T_aa the inverted diagonal
+// Part 2, the off-diagonal blocks, as two doubling levels (16 block
+// products in four phases): with T_aa the inverted diagonal
 // blocks,
 //   level 1 (pairs of 16-blocks):  T_10 = -T_11 (A_10 T_00),  T_32 = -T_33 (A_32 T_22);
 //   level 2 (rows 32..63 x columns 0..31):  X = A_B T_top,  T_B = -T_bottom X,
