@@ -23,7 +23,9 @@
 // Products are computed transposed so that TMEM lane j is value column j:
 //     D1 = S0^T [Q;K]^T  (M = d_v, N = 128 tokens, K = d_k), double-buffered
 //     D3 = V'^T T''^T    (T'' = T diag(beta); reuses the K half of D1)
-//     D5 = gamma_C S0^T + U^T Ktil     (the fp32 state, accumulated in TMEM)
+//     D5 = gamma_C S0^T + (diag(dec) U)^T K,  dec_t = exp(G_C - G_t)
+//          (the fp32 state, accumulated in TMEM; K is read MN-major straight
+//          from its TMA tile, so Ktil is never formed)
 //     D6 = U^T P^T
 // and the Gram [Q;K] K^T (M = 128 tokens, N = 64, K = d_k).  Operands are
 // fp16 (inputs convert exactly from bf16 except below 2^-14); accumulation
@@ -36,10 +38,11 @@
 //     S1 -> V' -> S3 -> U -> S5/S6 -> new state, plus the output of the
 //     previous chunk while S1 runs;
 //   prep group (warps 8-15, lanes split the same way): the chunk-local
-//     operands of the next chunk -- Q/K tiles (TMA, one chunk ahead, fp16 in
-//     place), decays, Gram, P, A, T = (I + A)^-1 (diagonal 16x16 blocks by
-//     substitution, then two doubling levels), T'' and Ktil -- into a
-//     double-buffered stage, handed over through mbarriers.
+//     operands of the next chunk -- Q/K tiles (TMA into a ring of three
+//     slots, issued a whole chunk ahead, fp16 in place), decays, Gram, P, A,
+//     T = (I + A)^-1 (diagonal 16x16 blocks by substitution, then two
+//     doubling levels) and T'' -- into a double-buffered stage, handed over
+//     through mbarriers.
 // A chunk's arithmetic depends only on its own inputs and the fp32 state
 // entering it, so results do not depend on the batch, and restarting from an
 // emitted state reproduces the uninterrupted run bit for bit.
@@ -77,16 +80,13 @@ template <int D>
 struct Smem {
     // Tensor-core operand tiles (K-major, 128-byte swizzle, 1024-aligned).
     static constexpr uint32_t kQKBytes = 128 * D * 2;          // fp16 [128 rows: q then k][D]
-    static constexpr uint32_t kQK0 = 0;
-    static constexpr uint32_t kQK1 = kQK0 + kQKBytes;
-    static constexpr uint32_t kTpp0 = kQK1 + kQKBytes;         // fp16 [64 rows t][64]  T''
+    static constexpr uint32_t kQK0 = 0;                          // ring of three slots
+    static constexpr uint32_t kTpp0 = kQK0 + 3 * kQKBytes;     // fp16 [64 rows t][64]  T''
     static constexpr uint32_t kTpp1 = kTpp0 + 8192;
     static constexpr uint32_t kP0 = kTpp1 + 8192;              // fp16 [64 rows t][64]  P
     static constexpr uint32_t kP1 = kP0 + 8192;
-    static constexpr uint32_t kKtT0 = kP1 + 8192;              // fp16 [D rows i][64]   Ktil^T
-    static constexpr uint32_t kKtT1 = kKtT0 + D * 128;
-    static constexpr uint32_t kS0T = kKtT1 + D * 128;          // fp16 [128 rows j][D]  S0^T
-    static constexpr uint32_t kVpT = kS0T + 128 * D * 2;       // fp16 [128 rows j][64] V'^T
+    static constexpr uint32_t kS0T = kP1 + 8192;               // fp16 [128 rows j][D]  S0^T
+    static constexpr uint32_t kVpT = kS0T + 128 * D * 2;       // fp16 [128 rows j][64] V'^T, then (diag(dec) U)^T
     static constexpr uint32_t kUT = kVpT + 16384;              // fp16 [128 rows j][64] U^T
     // Plain buffers.
     static constexpr uint32_t kGam0 = kUT + 16384;             // f32 [64] exp(G_t), stage 0
@@ -97,16 +97,15 @@ struct Smem {
     static constexpr uint32_t kG = kW + 4096;                  // f32 [64] cumulative log decay
     static constexpr uint32_t kBeta = kG + 256;                // f32 [64]
     static constexpr uint32_t kGraw = kBeta + 256;             // f32 [64]
-    static constexpr uint32_t kDec = kGraw + 256;              // f32 [64] exp(G_C - G_t)
-    static constexpr uint32_t kBars = kDec + 256;              // 8 mbarriers
-    static constexpr uint32_t kTmem = kBars + 64;              // TMEM base address
+    static constexpr uint32_t kDec = kGraw + 256;              // f32 [2][64] exp(G_C - G_t), per stage
+    static constexpr uint32_t kBars = kDec + 512;              // 9 mbarriers
+    static constexpr uint32_t kTmem = kBars + 128;             // TMEM base address
     static constexpr uint32_t kFail = kTmem + 4;               // int
     static constexpr uint32_t kEoff = kFail + 4;               // long long [16]
     static constexpr uint32_t kBytes = kEoff + 128;
     static constexpr uint32_t kAlloc = kBytes + 1024;          // + alignment slack
-    static_assert(kS0T % 1024 == 0 && kVpT % 1024 == 0 && kUT % 1024 == 0 && kKtT0 % 1024 == 0, "");
-    static_assert(kKtT1 % 1024 == 0 && kBars % 8 == 0, "");
-    static_assert(kTpp0 % 1024 == 0 && kP0 % 1024 == 0 && kQK1 % 1024 == 0, "");
+    static_assert(kS0T % 1024 == 0 && kVpT % 1024 == 0 && kUT % 1024 == 0 && kBars % 8 == 0, "");
+    static_assert(kTpp0 % 1024 == 0 && kP0 % 1024 == 0 && kQKBytes % 1024 == 0, "");
     static_assert(kM % 16 == 0 && kW % 16 == 0, "float4 access to the scratch");
     static_assert(kAlloc <= 232448, "shared memory budget");
 };
@@ -145,10 +144,6 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(bar)), "r"(bytes)
                  : "memory");
-}
-
-__device__ __forceinline__ float half_bits_to_float(uint16_t h) {
-    return __half2float(*reinterpret_cast<__half *>(&h));
 }
 
 // Writes columns [c0, c0 + 32) of row r (fp32 bit patterns) as fp16 into a
@@ -395,15 +390,15 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
     auto sQK = [&](int st) { return sm + SM::kQK0 + st * SM::kQKBytes; };
     auto sTpp = [&](int st) { return sm + SM::kTpp0 + st * 8192; };
     auto sP = [&](int st) { return sm + SM::kP0 + st * 8192; };
-    auto sKtT = [&](int st) { return sm + SM::kKtT0 + st * (D * 128); };
     auto sGam = [&](int st) { return reinterpret_cast<float *>(sm + SM::kGam0 + st * 256); };
     auto sGamC = [&](int st) { return reinterpret_cast<float *>(sm + SM::kGamC + st * 256); };
     uint8_t *sS0T = sm + SM::kS0T, *sVpT = sm + SM::kVpT, *sUT = sm + SM::kUT;
     float *sM = reinterpret_cast<float *>(sm + SM::kM), *sW = reinterpret_cast<float *>(sm + SM::kW);
     float *sG = reinterpret_cast<float *>(sm + SM::kG), *sBeta = reinterpret_cast<float *>(sm + SM::kBeta);
     float *sGraw = reinterpret_cast<float *>(sm + SM::kGraw);
-    float *sDec = reinterpret_cast<float *>(sm + SM::kDec);
+    auto sDec = [&](int st) { return reinterpret_cast<float *>(sm + SM::kDec + st * 256); };
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SM::kBars);
+    // ready / freeb per stage (chunk parity); tma_bar per Q/K slot (chunk mod 3).
     uint64_t *mma_bar = bars + 0, *gram_bar = bars + 1, *ready = bars + 2, *freeb = bars + 4, *tma_bar = bars + 6;
     uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(sm + SM::kTmem);
     int *fail = reinterpret_cast<int *>(sm + SM::kFail);
@@ -447,6 +442,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
         tc::mbar_init(freeb + 1, kGroup);
         tc::mbar_init(tma_bar + 0, 1);
         tc::mbar_init(tma_bar + 1, 1);
+        tc::mbar_init(tma_bar + 2, 1);
         *fail = 0;
     }
     for (int e = tid; e < 2 * 8192 / 16; e += kThreads)  // upper blocks of T'' stay zero
@@ -505,7 +501,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
         const uint64_t dVpT = tc::desc_k_sw128(tc::smem_u32(sVpT));
         const uint64_t dUT = tc::desc_k_sw128(tc::smem_u32(sUT));
         constexpr uint32_t kIdN128 = tc::idesc_f16_f32acc(128, 128), kIdN64 = tc::idesc_f16_f32acc(128, 64);
-        constexpr uint32_t kIdND = tc::idesc_f16_f32acc(128, D);
+        constexpr uint32_t kIdNDbmn = tc::idesc_f16_f32acc_bmn(128, D);  // B (the K tile) MN-major
         uint32_t mma_phase = 0;
         bool failed = false;
         int prev_n = 0, prev_tok0 = 0;
@@ -537,7 +533,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
         };
 
         for (int c = 0; c < n_chunks; ++c) {
-            const int s = c & 1;
+            const int s = c & 1, qs = c % 3;
             const int tok0 = t0 + c * kChunk;
             const int n = min(kChunk, Lseq - c * kChunk);
             const uint32_t d1 = tbase + kColD1 + 128 * s;
@@ -561,7 +557,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
 
             // ---- S1: D1 = S0^T [Q;K]^T --------------------------------------------
             if (tid == 0 && ok_ready) {
-                const uint64_t dQK = tc::desc_k_sw128(tc::smem_u32(sQK(s)));
+                const uint64_t dQK = tc::desc_k_sw128(tc::smem_u32(sQK(qs)));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4;
@@ -624,8 +620,9 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             }
             tc::fence_before_sync();
 
-            // ---- C4: U^T to fp16; D5 += U^T Ktil, D6 = U^T P^T --------------------
-            // (a failed wait is agreed on at the barrier that follows the phase)
+            // ---- C4: U^T and (diag(dec) U)^T to fp16; D5 += (diag(dec) U)^T K, D6 = U^T P^T
+            // (a failed wait is agreed on at the barrier that follows the phase;
+            // the V'^T tile is free once S3 has completed)
             const bool ok2 = __all_sync(0xffffffffu, mbar_wait_bounded(mma_bar, mma_phase));
             mma_phase ^= 1u;
             tc::fence_after_sync();
@@ -634,6 +631,11 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 tmem_load_row<32>(d1_lane + 64 + 32 * hf, u);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) store_chunk8_f16(sUT, 128, jm, 4 * hf + q, u + 8 * q);
+                const float *dec = sDec(s) + 32 * hf;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) u[i] *= dec[i];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) store_chunk8_f16(sVpT, 128, jm, 4 * hf + q, u + 8 * q);
             }
             tc::fence_proxy_async_smem();
             tc::fence_before_sync();
@@ -643,10 +645,13 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             }
             if (tid == 0) {
                 tc::fence_after_sync();
-                const uint64_t dKt = tc::desc_k_sw128(tc::smem_u32(sKtT(s)));
+                // K rows of the Q/K slot as B (N = key index i, K = token t), MN-major:
+                // 64-column boxes 16 KB apart, a 16-token K step is 2048 B.
+                const uint64_t dK = tc::desc_mn_sw128(tc::smem_u32(sQK(qs) + 8192), 16384);
                 const uint64_t dPs = tc::desc_k_sw128(tc::smem_u32(sP(s)));
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) tc::mma_f16(tbase + kColD5, dUT + kk * 2, dKt + kk * 2, kIdND, 1);
+                for (int kk = 0; kk < 4; ++kk)
+                    tc::mma_f16(tbase + kColD5, dVpT + kk * 2, dK + kk * (2048 >> 4), kIdNDbmn, 1);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) tc::mma_f16(tbase + kColD6, dUT + kk * 2, dPs + kk * 2, kIdN64, kk > 0);
                 tc::mma_commit(mma_bar);
@@ -657,7 +662,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
             const bool ok3 = __all_sync(0xffffffffu, mbar_wait_bounded(mma_bar, mma_phase));
             mma_phase ^= 1u;
             tc::fence_after_sync();
-            if (ok3) mbar_arrive(freeb + s);  // every MMA and read of this chunk's stage is done
+            if (ok3) mbar_arrive(freeb + s);  // every MMA and read of this chunk's stage and Q/K slot is done
             if (ok3 && j < D) {
                 float *ep = nullptr;
                 if (E > 0 && n == kChunk && ((c + 1) % E) == 0) {
@@ -719,10 +724,10 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
         const int p = pid & 127, hf = pid >> 7;
         bool failed = false;
         const uint32_t aIdGram = tc::idesc_f16_f32acc(128, 64);
-        // q, k of a chunk go straight into its stage's operand tile by TMA
-        // (bf16, 128-byte swizzle: the layout the MMA descriptors expect),
-        // issued one chunk ahead as soon as the stage is free; g, beta into
-        // registers.  The bf16 -> fp16 conversion then runs in place.
+        // q, k of a chunk go straight into its Q/K slot by TMA (bf16, 128-byte
+        // swizzle: the layout the MMA descriptors expect), issued at the start
+        // of the previous chunk's preparation; g, beta into registers at the
+        // same time.  The bf16 -> fp16 conversion then runs in place.
         constexpr int kPer = 64 * (D / 8) / kGroup;  // 16-byte chunks per thread per tile
         constexpr uint32_t kTmaBytes = 2u * (D / 64) * 64 * 128;
         float gv = 0.f, bv = 0.f;
@@ -735,8 +740,9 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 bv = a.beta[gi];
             }
             if (pid == 0) {
-                uint8_t *tile = sQK(cc & 1);
-                uint64_t *tb = tma_bar + (cc & 1);
+                const int slot = cc % 3;
+                uint8_t *tile = sQK(slot);
+                uint64_t *tb = tma_bar + slot;
                 mbar_expect_tx(tb, kTmaBytes);
 #pragma unroll
                 for (int kb = 0; kb < D / 64; ++kb) {
@@ -747,13 +753,25 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
         };
         if (n_chunks > 0) issue_chunk(0);
         for (int c = 0; c < n_chunks; ++c) {
-            const int s = c & 1;
+            const int s = c & 1, qs = c % 3;
             const int tok0 = t0 + c * kChunk;
             const int n = min(kChunk, Lseq - c * kChunk);
-            // ---- q, k tiles (copied during the previous chunk) to fp16; g, beta ----------
-            uint8_t *qk = sQK(s);
+            // ---- next chunk's copies; q, k tiles (copied during the previous chunk) to fp16
+            uint8_t *qk = sQK(qs);
             bool okt;
             {
+                if (pid < 64) {  // g, beta of this chunk, loaded one chunk ahead
+                    const int t = pid & 63;
+                    sGraw[t] = t < n ? gv : 0.f;
+                    sBeta[t] = t < n ? bv : 0.f;
+                }
+                // The next chunk's Q/K slot and this chunk's stage were both last
+                // used by chunk c - 2: one wait, by the issuing thread, covers
+                // both (the group barrier after the conversion orders every write
+                // of the stage after it).
+                bool okf = true;
+                if (pid == 0 && c >= 2) okf = mbar_wait_bounded(freeb + s, ((c - 2) >> 1) & 1);
+                if (c + 1 < n_chunks && okf) issue_chunk(c + 1);
                 if (c + 2 < n_chunks && pid < 128) {  // q, k rows of chunk c + 2 into L2
                     const int rn = min(kChunk, Lseq - (c + 2) * kChunk);
                     const int r = pid & 63;
@@ -764,7 +782,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                         if (D > 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(src_row + 64) : "memory");
                     }
                 }
-                okt = mbar_wait_bounded(tma_bar + s, (c >> 1) & 1);
+                okt = okf && mbar_wait_bounded(tma_bar + qs, (c / 3) & 1);
                 // rows past the sequence end (the next sequence's tokens) become zeros
 #pragma unroll
                 for (int it = 0; it < kPer && okt; ++it) {
@@ -778,11 +796,6 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                     *pk = r < n ? bf16x8_to_f16x8(xk) : z;
                 }
                 tc::fence_proxy_async_smem();  // the converted tile is read by the Gram MMA
-                if (pid < 64) {
-                    const int t = pid & 63;
-                    sGraw[t] = t < n ? gv : 0.f;
-                    sBeta[t] = t < n ? bv : 0.f;
-                }
             }
             tc::fence_before_sync();
             if (group_any(kBarPrep, !okt)) {  // a copy that never landed: stop (bounded)
@@ -817,8 +830,8 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 sG[2 * l + 1] = G1;
                 sGam(s)[2 * l] = expf(G0);
                 sGam(s)[2 * l + 1] = expf(G1);
-                sDec[2 * l] = expf(Gc - G0);
-                sDec[2 * l + 1] = expf(Gc - G1);
+                sDec(s)[2 * l] = expf(Gc - G0);
+                sDec(s)[2 * l + 1] = expf(Gc - G1);
             }
             group_sync(kBarPrep);  // g cumsum, gamma, dec visible
             __syncwarp();
@@ -874,26 +887,9 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 break;
             }
 
-            // ---- T = (I + A)^-1 (diagonal blocks) || Ktil^T --------------------------
+            // ---- T = (I + A)^-1: diagonal blocks, then level 1 ---------------------------
             float xd[16];
-            if (pid < 64) {
-                invert_diag_solve(sM, pid, xd);
-            } else {
-                // Ktil^T[i][t] = exp(G_C - G_t) k_t[i]: items (row i, 32 tokens); the
-                // lanes of a warp read consecutive i of one k row.
-                for (int e = pid - 64; e < D * 2; e += kGroup - 64) {
-                    const int i = e & (D - 1), half = (e / D) & 1;
-                    float x[32];
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) {
-                        const int t = half * 32 + u;
-                        const uint16_t kb = *reinterpret_cast<const uint16_t *>(qk + tc::sw128_offset(64 + t, i, 128));
-                        x[u] = sDec[t] * half_bits_to_float(kb);
-                    }
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) store_chunk8_f16(sKtT(s), D, i, 4 * half + q, x + 8 * q);
-                }
-            }
+            if (pid < 64) invert_diag_solve(sM, pid, xd);
             // A diagonal block is solved and stored by the 16 lanes of one half
             // warp (warps 8 and 9): a warp barrier orders its reads before the
             // store, and the same warp then builds level 1 of the off-diagonal
@@ -905,17 +901,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 if (pid < 32) level1_warp<1>(sM, sW, pid & 31, sTpp(s), sBeta);
                 else level1_warp<3>(sM, sW, pid & 31, sTpp(s), sBeta);
             }
-            // ---- the next chunk's q, k copies, once its stage is free --------------------
-            if (c + 1 < n_chunks) {
-                const bool ok = c + 1 < 2 || mbar_wait_bounded(freeb + (s ^ 1), ((c - 1) >> 1) & 1);
-                if (group_any(kBarPrep, !ok)) {
-                    failed = true;
-                    break;
-                }
-                issue_chunk(c + 1);
-            } else {
-                group_sync(kBarPrep);
-            }
+            group_sync(kBarPrep);  // diagonal blocks and level 1 visible to level 2
             // T'' = T diag(beta) is written as fp16 by the inverse itself.
             invert_offdiag(sM, sW, pid, sTpp(s), sBeta);
             tc::fence_proxy_async_smem();

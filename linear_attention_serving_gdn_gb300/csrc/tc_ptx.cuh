@@ -1,8 +1,8 @@
 // Thin inline-PTX wrappers for the sm_100-family tensor-core path used by the
 // chunked prefill: mbarriers, TMEM allocation, tcgen05.mma (kind::f16),
 // tcgen05.commit, tcgen05.ld / tcgen05.st and the shared-memory matrix
-// descriptors of the canonical K-major 128-byte-swizzled layout.  Written from
-// the PTX ISA description of these instructions.
+// descriptors of the canonical K-major and MN-major 128-byte-swizzled
+// layouts.  Written from the PTX ISA description of these instructions.
 #pragma once
 
 #include <stdint.h>
@@ -97,6 +97,12 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32acc(int M, int N) {
            | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
 }
 
+// The same with B given MN-major (N contiguous in shared memory): the
+// "transpose B" bit of the kind::f16 instruction descriptor.
+__host__ __device__ constexpr uint32_t idesc_f16_f32acc_bmn(int M, int N) {
+    return idesc_f16_f32acc(M, N) | (1u << 16);
+}
+
 // Shared-memory descriptor of a K-major operand in the 128-byte-swizzle
 // canonical layout: each row holds 64 fp16 (128 B) of the K dimension, rows
 // are 128 B apart, 8-row groups 1024 B apart (the stride byte offset), and
@@ -110,6 +116,25 @@ __device__ __forceinline__ uint64_t desc_k_sw128(uint32_t smem_addr) {
     d |= static_cast<uint64_t>(1024 >> 4) << 32;              // stride byte offset
     d |= static_cast<uint64_t>(1) << 46;                      // descriptor version
     d |= static_cast<uint64_t>(2) << 61;                      // 128-byte swizzle
+    return d;
+}
+
+// Shared-memory descriptor of an MN-major operand in the 128-byte-swizzle
+// canonical layout: a 128-byte row holds 64 fp16 consecutive along M (or N)
+// at one k, rows k .. k + 7 form one 1024-byte swizzle atom (16-byte chunk c
+// of row k stored at chunk c ^ (k % 8)), 8-row groups along K are 1024 B
+// apart (the stride byte offset) and the next 64 elements along M/N start
+// mn_stride bytes further (the leading byte offset).  This is the layout a
+// 128-byte-swizzled TMA box of 64-element rows lands in, read with the box
+// rows as the K dimension.  The base must be 1024-byte aligned; a K step of
+// 16 elements advances the start address by 2048 B.
+__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t smem_addr, uint32_t mn_stride) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);     // start address
+    d |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;  // leading byte offset
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;                 // stride byte offset
+    d |= static_cast<uint64_t>(1) << 46;                         // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;                         // 128-byte swizzle
     return d;
 }
 
