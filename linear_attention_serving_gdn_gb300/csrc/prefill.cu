@@ -39,8 +39,9 @@
 //     previous chunk while S1 runs;
 //   prep group (warps 8-15, lanes split the same way): the chunk-local
 //     operands of the next chunk -- Q/K tiles (TMA into a ring of three
-//     slots, issued a whole chunk ahead, fp16 in place), decays, Gram, P, A,
-//     T = (I + A)^-1 (diagonal 16x16 blocks by substitution, then two
+//     slots, issued a whole chunk ahead and converted to fp16 in place
+//     while the previous chunk's diagonal blocks are solved), decays, Gram,
+//     P, A, T = (I + A)^-1 (diagonal 16x16 blocks by substitution, then two
 //     doubling levels) and T'' -- into a double-buffered stage, handed over
 //     through mbarriers.
 // A chunk's arithmetic depends only on its own inputs and the fp32 state
@@ -519,8 +520,14 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 tmem_load_row<32>(my_lane + kColD6 + 32 * hf, pu);
                 const float *gam = sGamC(buf) + 32 * hf;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    sOst[(32 * hf + i) * D + jm] = float_to_bf16_bits(a.scale * fmaf(gam[i], qs[i], pu[i]));
+                for (int i4 = 0; i4 < 32; i4 += 4) {
+                    const float4 g4 = *reinterpret_cast<const float4 *>(gam + i4);
+                    const float gg[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        sOst[(32 * hf + i4 + u) * D + jm] =
+                            float_to_bf16_bits(a.scale * fmaf(gg[u], qs[i4 + u], pu[i4 + u]));
+                }
             }
             tc::fence_before_sync();
             group_sync(kBarChain);
@@ -591,8 +598,15 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 tmem_load_row<32>(d1_lane + 64 + 32 * hf, ks);
                 const float *gam = sGam(s) + 32 * hf;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    ks[i] = __uint_as_float(static_cast<uint32_t>(sVst[(32 * hf + i) * D + jm]) << 16) - gam[i] * ks[i];
+                for (int i4 = 0; i4 < 32; i4 += 4) {
+                    const float4 g4 = *reinterpret_cast<const float4 *>(gam + i4);
+                    const float gg[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int i = i4 + u;
+                        ks[i] = __uint_as_float(static_cast<uint32_t>(sVst[(32 * hf + i) * D + jm]) << 16) - gg[u] * ks[i];
+                    }
+                }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) store_chunk8_f16(sVpT, 128, jm, 4 * hf + q, ks + 8 * q);
             }
@@ -633,7 +647,13 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 for (int q = 0; q < 4; ++q) store_chunk8_f16(sUT, 128, jm, 4 * hf + q, u + 8 * q);
                 const float *dec = sDec(s) + 32 * hf;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) u[i] *= dec[i];
+                for (int i4 = 0; i4 < 32; i4 += 4) {
+                    const float4 d4 = *reinterpret_cast<const float4 *>(dec + i4);
+                    u[i4] *= d4.x;
+                    u[i4 + 1] *= d4.y;
+                    u[i4 + 2] *= d4.z;
+                    u[i4 + 3] *= d4.w;
+                }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) store_chunk8_f16(sVpT, 128, jm, 4 * hf + q, u + 8 * q);
             }
@@ -727,11 +747,11 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
         // q, k of a chunk go straight into its Q/K slot by TMA (bf16, 128-byte
         // swizzle: the layout the MMA descriptors expect), issued at the start
         // of the previous chunk's preparation; g, beta into registers at the
-        // same time.  The bf16 -> fp16 conversion then runs in place.
-        constexpr int kPer = 64 * (D / 8) / kGroup;  // 16-byte chunks per thread per tile
+        // same time.  The bf16 -> fp16 conversion runs in place, during the
+        // previous chunk's diagonal solve, by the warps that solve nothing.
         constexpr uint32_t kTmaBytes = 2u * (D / 64) * 64 * 128;
         float gv = 0.f, bv = 0.f;
-        auto issue_chunk = [&](int cc) {
+        auto load_gb = [&](int cc) {
             const int tk = t0 + cc * kChunk;
             const int nn = min(kChunk, Lseq - cc * kChunk);
             if (pid < 64) {
@@ -739,6 +759,9 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 gv = a.g[gi];
                 bv = a.beta[gi];
             }
+        };
+        auto issue_tma = [&](int cc) {
+            const int tk = t0 + cc * kChunk;
             if (pid == 0) {
                 const int slot = cc % 3;
                 uint8_t *tile = sQK(slot);
@@ -751,12 +774,38 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 }
             }
         };
-        if (n_chunks > 0) issue_chunk(0);
-        for (int c = 0; c < n_chunks; ++c) {
+        // Waits for chunk cc's copies and converts its slot to fp16 in place
+        // (16-byte items first_e, first_e + step, ...); rows past the sequence
+        // end (the next sequence's tokens) become zeros.
+        auto convert = [&](int cc, int first_e, int step) -> bool {
+            const int slot = cc % 3;
+            const int nn = min(kChunk, Lseq - cc * kChunk);
+            uint8_t *tile = sQK(slot);
+            if (!mbar_wait_bounded(tma_bar + slot, (cc / 3) & 1)) return false;
+            for (int e = first_e; e < 64 * (D / 8); e += step) {
+                const int r = e / (D / 8), c8 = e % (D / 8);
+                uint4 *pq = reinterpret_cast<uint4 *>(tile + tc::sw128_chunk_offset(r, c8, 128));
+                uint4 *pk = reinterpret_cast<uint4 *>(tile + tc::sw128_chunk_offset(64 + r, c8, 128));
+                const uint4 z = make_uint4(0, 0, 0, 0);
+                const uint4 xq = *pq, xk = *pk;
+                *pq = r < nn ? bf16x8_to_f16x8(xq) : z;
+                *pk = r < nn ? bf16x8_to_f16x8(xk) : z;
+            }
+            tc::fence_proxy_async_smem();  // the converted tile is read by the tensor cores
+            return true;
+        };
+        if (n_chunks > 0) {
+            issue_tma(0);
+            if (n_chunks > 1) issue_tma(1);
+            load_gb(0);
+            if (!convert(0, pid, kGroup)) failed = true;
+        }
+        if (group_any(kBarPrep, failed)) failed = true;
+        for (int c = 0; c < n_chunks && !failed; ++c) {
             const int s = c & 1, qs = c % 3;
             const int tok0 = t0 + c * kChunk;
             const int n = min(kChunk, Lseq - c * kChunk);
-            // ---- next chunk's copies; q, k tiles (copied during the previous chunk) to fp16
+            // ---- next chunk's copies (each chunk's tile is converted one chunk ahead)
             uint8_t *qk = sQK(qs);
             bool okt;
             {
@@ -767,11 +816,12 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 }
                 // The next chunk's Q/K slot and this chunk's stage were both last
                 // used by chunk c - 2: one wait, by the issuing thread, covers
-                // both (the group barrier after the conversion orders every write
-                // of the stage after it).
+                // both (the group barrier below orders every write of the stage
+                // after it).  Chunk 1's copies were issued with chunk 0's.
                 bool okf = true;
                 if (pid == 0 && c >= 2) okf = mbar_wait_bounded(freeb + s, ((c - 2) >> 1) & 1);
-                if (c + 1 < n_chunks && okf) issue_chunk(c + 1);
+                if (c >= 1 && c + 1 < n_chunks && okf) issue_tma(c + 1);
+                if (c + 1 < n_chunks) load_gb(c + 1);
                 if (c + 2 < n_chunks && pid < 128) {  // q, k rows of chunk c + 2 into L2
                     const int rn = min(kChunk, Lseq - (c + 2) * kChunk);
                     const int r = pid & 63;
@@ -782,23 +832,10 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                         if (D > 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(src_row + 64) : "memory");
                     }
                 }
-                okt = okf && mbar_wait_bounded(tma_bar + qs, (c / 3) & 1);
-                // rows past the sequence end (the next sequence's tokens) become zeros
-#pragma unroll
-                for (int it = 0; it < kPer && okt; ++it) {
-                    const int e = pid + it * kGroup;
-                    const int r = e / (D / 8), c8 = e % (D / 8);
-                    uint4 *pq = reinterpret_cast<uint4 *>(qk + tc::sw128_chunk_offset(r, c8, 128));
-                    uint4 *pk = reinterpret_cast<uint4 *>(qk + tc::sw128_chunk_offset(64 + r, c8, 128));
-                    const uint4 z = make_uint4(0, 0, 0, 0);
-                    const uint4 xq = *pq, xk = *pk;
-                    *pq = r < n ? bf16x8_to_f16x8(xq) : z;
-                    *pk = r < n ? bf16x8_to_f16x8(xk) : z;
-                }
-                tc::fence_proxy_async_smem();  // the converted tile is read by the Gram MMA
+                okt = okf;
             }
             tc::fence_before_sync();
-            if (group_any(kBarPrep, !okt)) {  // a copy that never landed: stop (bounded)
+            if (group_any(kBarPrep, !okt)) {  // chunk c - 2 never finished: stop (bounded)
                 failed = true;
                 break;
             }
@@ -887,21 +924,27 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 break;
             }
 
-            // ---- T = (I + A)^-1: diagonal blocks, then level 1 ---------------------------
-            float xd[16];
-            if (pid < 64) invert_diag_solve(sM, pid, xd);
+            // ---- T = (I + A)^-1: diagonal blocks, then level 1 || next chunk's Q/K to fp16
             // A diagonal block is solved and stored by the 16 lanes of one half
             // warp (warps 8 and 9): a warp barrier orders its reads before the
             // store, and the same warp then builds level 1 of the off-diagonal
             // part; the group barrier below orders both before level 2.
+            bool okn = true;
             if (pid < 64) {
+                float xd[16];
+                invert_diag_solve(sM, pid, xd);
                 __syncwarp();
                 invert_diag_store(sM, pid, xd, sTpp(s), sBeta);
                 __syncwarp();  // warp 8 holds blocks 0, 1 and warp 9 blocks 2, 3: level 1 per warp
                 if (pid < 32) level1_warp<1>(sM, sW, pid & 31, sTpp(s), sBeta);
                 else level1_warp<3>(sM, sW, pid & 31, sTpp(s), sBeta);
+            } else if (c + 1 < n_chunks) {
+                okn = convert(c + 1, pid - 64, kGroup - 64);
             }
-            group_sync(kBarPrep);  // diagonal blocks and level 1 visible to level 2
+            if (group_any(kBarPrep, !okn)) {  // diagonal blocks and level 1 visible to level 2
+                failed = true;
+                break;
+            }
             // T'' = T diag(beta) is written as fp16 by the inverse itself.
             invert_offdiag(sM, sW, pid, sTpp(s), sBeta);
             tc::fence_proxy_async_smem();
