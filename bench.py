@@ -564,8 +564,10 @@ def decode_config(n_slots, world=1):
 
 
 def reference_arm(args):
-    import torch
-    world, rank, _ = dist_setup(torch)
+    # The oracle runs on the host cores of rank 0 only; no process group or
+    # GPU is needed, so the other ranks of a torchrun launch exit at once.
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     rows = 64
@@ -579,10 +581,10 @@ def reference_arm(args):
     tot = sum(times)
     value = rows * args.steps / tot
     line = {"impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "rows/s",
-            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": decode_config(2 * DECODE_ROWS),
+            "config": decode_config(2 * DECODE_ROWS, world),
             "cpu_baseline": {"value": value, "unit": "rows/s", "cores": threads, "kind": "oracle",
                              "sample": f"{rows} of the 256 decode rows per step, 1 recurrent step"},
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
