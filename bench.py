@@ -487,10 +487,10 @@ def run_extra(torch, gdn, dev, wanted, peaks, prefix_seqlen=32768):
         extra.append(prep_case(torch, gdn, dev, peaks))
     for x in extra:
         if "algorithmic_tflops" in x:
-            x["roofline"] = {"bound": "tensor", "kernel": "prefill_chunk_tc_kernel<128>",
+            x["roofline"] = {"bound": "tensor", "kernel": "prefill_chain_kernel<128>",
                              "achieved": x["algorithmic_tflops"], "peak": peaks["bf16_tflops"],
                              "unit": "TFLOP/s", "frac": x["algorithmic_tflops"] / peaks["bf16_tflops"],
-                             "traffic": measured_traffic("prefill_chunk_tc_kernel<128>", x["workload"]),
+                             "traffic": measured_traffic("prefill_chain_kernel<128>", x["workload"]),
                              "peak_source": peaks["source"] + " (dense bf16 burst; fp16 runs at the same rate)"}
     return extra
 
@@ -500,7 +500,7 @@ def kernel_source_hash(kernel: str) -> str:
     import hashlib
     csrc = os.path.join(ROOT, "linear_attention_serving_gdn_gb300", "csrc")
     files = {"decode_kernel<128>": ["decode.cu", "row_update.cuh", "gdn_internal.cuh"],
-             "prefill_chunk_tc_kernel<128>": ["prefill.cu", "tc_ptx.cuh", "gdn_internal.cuh"]}[kernel]
+             "prefill_chain_kernel<128>": ["prefill.cu", "tc_ptx.cuh", "gdn_internal.cuh"]}[kernel]
     h = hashlib.sha256()
     for f in files:
         h.update(open(os.path.join(csrc, f), "rb").read())

@@ -45,6 +45,15 @@
  *     GDN_DEV_* bit into *dev_status when dev_status is not NULL; kernels
  *     never trap.
  *   - Only d_k == d_v in {64, 128} is supported; h_v % h_k == 0.
+ *   - Slots: within one call, the set of slots a call writes (destination
+ *     slots, snapshot slots, cache-block slots) must be disjoint from the
+ *     slots that OTHER rows or sequences of the same call read, and no slot
+ *     may be written twice; a row or sequence may write the slot it reads
+ *     (in place).  Rows run concurrently, so an aliased slot would make the
+ *     result depend on scheduling.  A state shift along slots (row r writes
+ *     the slot row r+1 reads) must be split into calls that each satisfy
+ *     this rule.  When the decode and prefill halves of a step are launched
+ *     on two streams at once, their slot sets must be disjoint too.
  */
 #ifndef GDN_H_
 #define GDN_H_
@@ -62,10 +71,14 @@ typedef enum {
     GDN_OK = 0,
     GDN_ERR_INVALID_ARG = 1, /* null pointer, bad size, non-monotone cu_seqlens, ... */
     GDN_ERR_UNSUPPORTED = 2, /* head dims or shapes this build does not implement */
-    GDN_ERR_CUDA = 3         /* a CUDA runtime call or launch failed */
+    GDN_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    GDN_ERR_WORKSPACE = 4,   /* workspace smaller than gdn_prefill_workspace_bytes() or misaligned */
+    GDN_ERR_TIMEOUT = 5      /* from gdn_status_from_device(): a bounded wait expired in a kernel */
 } gdn_status_t;
 
-/* Bits ORed into *dev_status by kernels. */
+/* Bits ORed into *dev_status by kernels.  Kernels run asynchronously, so
+ * these reach the host only when the caller reads the word back;
+ * gdn_status_from_device() maps it to a gdn_status_t. */
 #define GDN_DEV_BAD_SLOT 0x1 /* a slot index was >= num_slots; the row/sequence was skipped */
 #define GDN_DEV_TIMEOUT 0x2  /* a bounded wait expired inside a kernel; its outputs are invalid */
 
@@ -207,7 +220,16 @@ gdn_status_t gdn_decode_multi(const gdn_dims_t *dims, int32_t num_rows, int32_t 
  *                     emit_offset(s) = sum_{s' < s} floor(L_s' / (64 E)).
  *                     E = 17 puts states on the 1088-token block grid.
  *   chunk_states_capacity  entries available in chunk_states; must be at
- *                     least gdn_prefill_num_emits(...).
+ *                     least gdn_prefill_num_emits(...).  1 <= E <= 2^24.
+ *                     Each sequence's first entry emit_offset(s) is computed
+ *                     on the device from cu_seqlens (no caller-built cu_emit
+ *                     array); gdn_prefill_emit_offsets() returns the same
+ *                     values on the host.
+ *   workspace, workspace_bytes  caller-owned device scratch of at least
+ *                     gdn_prefill_workspace_bytes(dims, num_seqs, T) bytes,
+ *                     256-byte aligned (NULL with 0 bytes when that is 0).
+ *                     A smaller or misaligned workspace returns
+ *                     GDN_ERR_WORKSPACE before any launch.
  * Resuming a sequence from the state emitted after token 64*E*j with its
  * tokens [64*E*j, L) reproduces the uninterrupted outputs and final state
  * bit for bit; so does running a sequence alone or inside any batch.
@@ -221,7 +243,16 @@ gdn_status_t gdn_prefill_varlen(const gdn_dims_t *dims, int32_t num_seqs,
                                 gdn_bf16 *o,
                                 float *chunk_states, int32_t emit_every_chunks,
                                 int64_t chunk_states_capacity,
+                                void *workspace, size_t workspace_bytes,
                                 int32_t *dev_status, void *stream);
+
+/*
+ * Device scratch that gdn_prefill_varlen, gdn_prefill_varlen_apc and the
+ * prefill half of gdn_mixed_step need for num_seqs sequences of total_tokens
+ * tokens (0 when the call needs none).  Host-only; returns (size_t)-1 for
+ * bad dims or negative sizes.
+ */
+size_t gdn_prefill_workspace_bytes(const gdn_dims_t *dims, int32_t num_seqs, int64_t total_tokens);
 
 /*
  * Chunked varlen prefill that writes its emitted states straight into the
@@ -256,6 +287,7 @@ gdn_status_t gdn_prefill_varlen_apc(const gdn_dims_t *dims, int32_t num_seqs,
                                     gdn_bf16 *o, int32_t emit_every_chunks,
                                     const int32_t *block_table, int32_t block_table_stride,
                                     const int32_t *block_first,
+                                    void *workspace, size_t workspace_bytes,
                                     int32_t *dev_status, void *stream);
 
 /*
@@ -269,7 +301,9 @@ gdn_status_t gdn_prefill_varlen_apc(const gdn_dims_t *dims, int32_t num_seqs,
  *   rows num_decodes + [cu_seqlens_p[s], cu_seqlens_p[s+1]).
  *   dec_src_slot/dec_dst_slot: as gdn_decode_packed (num_decodes entries).
  *   pre_src_slot/pre_dst_slot: as gdn_prefill_varlen (num_prefills entries).
- *   Remaining arguments as gdn_prefill_varlen; o covers all rows.
+ *   Remaining arguments as gdn_prefill_varlen; o covers all rows.  Both
+ *   halves are validated before either is launched: a bad argument in the
+ *   prefill half launches no decode work either.
  * The decode rows run on the same kernel and arithmetic as
  * gdn_decode_packed, so their outputs and states are bitwise identical to a
  * decode-only call, whatever prefills share the step.
@@ -284,6 +318,7 @@ gdn_status_t gdn_mixed_step(const gdn_dims_t *dims, int32_t num_decodes, int32_t
                             gdn_bf16 *o,
                             float *chunk_states, int32_t emit_every_chunks,
                             int64_t chunk_states_capacity,
+                            void *workspace, size_t workspace_bytes,
                             int32_t *dev_status, void *stream);
 
 /* ---- host-only helpers (no device work) ------------------------------- */
@@ -311,6 +346,12 @@ int64_t gdn_floor_prefix_hit(int64_t hit_tokens, int64_t prompt_tokens, int32_t 
 
 /* Emission stride, in chunks, of the grid above (1088 / 64 = 17). */
 int32_t gdn_grid_emit_every_chunks(int32_t block_size);
+
+/* Status of a completed call from the device status word it wrote (read
+ * back by the caller after the stream is done): GDN_ERR_TIMEOUT when
+ * GDN_DEV_TIMEOUT is set, GDN_ERR_INVALID_ARG when only GDN_DEV_BAD_SLOT is
+ * set, GDN_OK for 0. */
+gdn_status_t gdn_status_from_device(int32_t dev_status_word);
 
 const char *gdn_status_string(gdn_status_t status);
 

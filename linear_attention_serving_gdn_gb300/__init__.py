@@ -28,16 +28,19 @@ __all__ = [
     "gdn_decode_packed", "gdn_decode_packed_raw", "gdn_prep_inputs", "gdn_decode_multi",
     "gdn_prefill_varlen", "gdn_prefill_varlen_apc", "gdn_mixed_step", "gdn_prefill_num_emits", "gdn_prefill_emit_offsets", "gdn_align_block_size",
     "gdn_floor_prefix_hit", "gdn_grid_emit_every_chunks", "gdn_status_string",
+    "gdn_prefill_workspace_bytes", "gdn_status_from_device",
     "EXPORTED_SYMBOLS", "GDN_DEV_BAD_SLOT", "GDN_DEV_TIMEOUT",
 ]
 
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA = 0, 1, 2, 3
+GDN_ERR_WORKSPACE, GDN_ERR_TIMEOUT = 4, 5
 GDN_DEV_BAD_SLOT, GDN_DEV_TIMEOUT = 0x1, 0x2
 
 EXPORTED_SYMBOLS = (
     "gdn_decode_packed", "gdn_decode_packed_raw", "gdn_prep_inputs", "gdn_decode_multi",
     "gdn_prefill_varlen", "gdn_prefill_varlen_apc", "gdn_mixed_step", "gdn_prefill_num_emits", "gdn_prefill_emit_offsets", "gdn_align_block_size",
     "gdn_floor_prefix_hit", "gdn_grid_emit_every_chunks", "gdn_status_string",
+    "gdn_prefill_workspace_bytes", "gdn_status_from_device",
 )
 
 
@@ -55,6 +58,7 @@ class Dims(ctypes.Structure):
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
 _lib = None
 
 
@@ -84,13 +88,17 @@ def load_library() -> ctypes.CDLL:
                                      _P, _P, _P, _P, _P]
     lib.gdn_prefill_varlen.restype = ctypes.c_int
     lib.gdn_prefill_varlen.argtypes = [ctypes.POINTER(Dims), _I32, _P, _P, _P, _P, _P, _P, _P,
-                                       _P, _I64, _P, _P, _P, _P, _I32, _I64, _P, _P]
+                                       _P, _I64, _P, _P, _P, _P, _I32, _I64, _P, _SZ, _P, _P]
     lib.gdn_prefill_varlen_apc.restype = ctypes.c_int
     lib.gdn_prefill_varlen_apc.argtypes = [ctypes.POINTER(Dims), _I32, _P, _P, _P, _P, _P, _P, _P,
-                                           _P, _I64, _P, _P, _P, _I32, _P, _I32, _P, _P, _P]
+                                           _P, _I64, _P, _P, _P, _I32, _P, _I32, _P, _P, _SZ, _P, _P]
     lib.gdn_mixed_step.restype = ctypes.c_int
     lib.gdn_mixed_step.argtypes = [ctypes.POINTER(Dims), _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
-                                   _P, _I64, _P, _P, _P, _P, _P, _P, _I32, _I64, _P, _P]
+                                   _P, _I64, _P, _P, _P, _P, _P, _P, _I32, _I64, _P, _SZ, _P, _P]
+    lib.gdn_prefill_workspace_bytes.restype = _SZ
+    lib.gdn_prefill_workspace_bytes.argtypes = [ctypes.POINTER(Dims), _I32, _I64]
+    lib.gdn_status_from_device.restype = ctypes.c_int
+    lib.gdn_status_from_device.argtypes = [_I32]
     lib.gdn_prefill_num_emits.restype = _I64
     lib.gdn_prefill_num_emits.argtypes = [_P, _I32, _I32]
     lib.gdn_prefill_emit_offsets.restype = ctypes.c_int
@@ -146,6 +154,17 @@ def _host_i32(x, name):
         return x, ctypes.c_void_p(x.data_ptr())
     arr = (ctypes.c_int32 * len(x))(*[int(v) for v in x])
     return arr, ctypes.cast(arr, ctypes.c_void_p)
+
+
+def _workspace(ws, dims, num_seqs, total_tokens):
+    """(pointer, bytes) of a caller workspace; checks it against the library's need."""
+    need = load_library().gdn_prefill_workspace_bytes(ctypes.byref(dims), int(num_seqs), int(total_tokens))
+    if ws is None:
+        if need:
+            raise ValueError(f"this prefill needs a {need}-byte workspace (gdn_prefill_workspace_bytes)")
+        return None, 0
+    ws = _dev(ws, "workspace", torch.uint8)
+    return _ptr(ws), ws.numel()
 
 
 def _check(status, fn):
@@ -268,9 +287,11 @@ def gdn_decode_multi(tokens_per_row: int, q, k, v, g, beta, state, src_slot, o, 
 
 def gdn_prefill_varlen(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, o, state=None,
                        src_slot=None, dst_slot=None, chunk_states=None, emit_every_chunks: int = 0,
-                       dev_status=None, scale: float = 1.0, stream=None) -> None:
+                       dev_status=None, scale: float = 1.0, stream=None, workspace=None) -> None:
     """Chunked varlen prefill (see gdn.h).  ``cu_seqlens_host`` is a host
-    sequence (list or CPU tensor) with the same values as ``cu_seqlens``."""
+    sequence (list or CPU tensor) with the same values as ``cu_seqlens``;
+    ``workspace`` an optional uint8 device tensor (see
+    ``gdn_prefill_workspace_bytes``)."""
     lib = load_library()
     bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
     q, k, v = _dev(q, "q", bf, 3), _dev(k, "k", bf, 3), _dev(v, "v", bf, 3)
@@ -292,17 +313,19 @@ def gdn_prefill_varlen(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, o, state=N
         raise ValueError("inconsistent prefill shapes")
     d = _dims(q, v, scale)
     cap = 0 if chunk_states is None else chunk_states.shape[0]
+    ws, ws_bytes = _workspace(workspace, d, n, T)
     _check(lib.gdn_prefill_varlen(ctypes.byref(d), n, _ptr(cu_seqlens), cu_h, _ptr(q), _ptr(k),
                                   _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
                                   0 if state is None else state.shape[0], _ptr(src_slot),
                                   _ptr(dst_slot), _ptr(o), _ptr(chunk_states),
-                                  int(emit_every_chunks), cap, _ptr(dev_status), _stream(stream)),
+                                  int(emit_every_chunks), cap, ws, ws_bytes, _ptr(dev_status),
+                                  _stream(stream)),
            "gdn_prefill_varlen")
 
 
 def gdn_prefill_varlen_apc(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, o, state, block_table,
                            block_first, emit_every_chunks: int, src_slot=None, dst_slot=None,
-                           dev_status=None, scale: float = 1.0, stream=None) -> None:
+                           dev_status=None, scale: float = 1.0, stream=None, workspace=None) -> None:
     """Chunked varlen prefill emitting into cache blocks: ``block_table``
     int32 [num_seqs][max_blocks], ``block_first`` int32 [num_seqs] (see gdn.h)."""
     lib = load_library()
@@ -326,18 +349,19 @@ def gdn_prefill_varlen_apc(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, o, sta
             and g.shape == (T, v.shape[1]) and beta.shape == g.shape):
         raise ValueError("inconsistent prefill shapes")
     d = _dims(q, v, scale)
+    ws, ws_bytes = _workspace(workspace, d, n, T)
     _check(lib.gdn_prefill_varlen_apc(ctypes.byref(d), n, _ptr(cu_seqlens), cu_h, _ptr(q), _ptr(k),
                                       _ptr(v), _ptr(g), _ptr(beta), _ptr(state), state.shape[0],
                                       _ptr(src_slot), _ptr(dst_slot), _ptr(o), int(emit_every_chunks),
                                       _ptr(block_table), block_table.shape[1], _ptr(block_first),
-                                      _ptr(dev_status), _stream(stream)),
+                                      ws, ws_bytes, _ptr(dev_status), _stream(stream)),
            "gdn_prefill_varlen_apc")
 
 
 def gdn_mixed_step(num_decodes: int, q, k, v, g, beta, cu_seqlens_p, cu_seqlens_p_host, state,
                    dec_src_slot, o, dec_dst_slot=None, pre_src_slot=None, pre_dst_slot=None,
                    chunk_states=None, emit_every_chunks: int = 0, dev_status=None,
-                   scale: float = 1.0, stream=None) -> None:
+                   scale: float = 1.0, stream=None, workspace=None) -> None:
     """Mixed step: decode rows [0, num_decodes) then prefill sequences."""
     lib = load_library()
     bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
@@ -364,11 +388,13 @@ def gdn_mixed_step(num_decodes: int, q, k, v, g, beta, cu_seqlens_p, cu_seqlens_
         raise ValueError("token count does not match num_decodes + cu_seqlens_p_host[-1]")
     d = _dims(q, v, scale)
     cap = 0 if chunk_states is None else chunk_states.shape[0]
+    ws, ws_bytes = _workspace(workspace, d, n_p, T - int(num_decodes))
     _check(lib.gdn_mixed_step(ctypes.byref(d), int(num_decodes), n_p, _ptr(cu_seqlens_p), cu_h,
                               _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
                               state.shape[0], _ptr(dec_src_slot), _ptr(dec_dst_slot),
                               _ptr(pre_src_slot), _ptr(pre_dst_slot), _ptr(o), _ptr(chunk_states),
-                              int(emit_every_chunks), cap, _ptr(dev_status), _stream(stream)),
+                              int(emit_every_chunks), cap, ws, ws_bytes, _ptr(dev_status),
+                              _stream(stream)),
            "gdn_mixed_step")
 
 
@@ -403,6 +429,20 @@ def gdn_floor_prefix_hit(hit_tokens: int, prompt_tokens: int, block_size: int) -
 
 def gdn_grid_emit_every_chunks(block_size: int) -> int:
     return int(load_library().gdn_grid_emit_every_chunks(int(block_size)))
+
+
+def gdn_prefill_workspace_bytes(h_k: int, h_v: int, d: int, num_seqs: int, total_tokens: int) -> int:
+    """Device scratch (bytes) a prefill of ``num_seqs`` sequences needs."""
+    dims = Dims(int(h_k), int(h_v), int(d), int(d), 1.0)
+    n = load_library().gdn_prefill_workspace_bytes(ctypes.byref(dims), int(num_seqs), int(total_tokens))
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("invalid prefill dims or sizes")
+    return int(n)
+
+
+def gdn_status_from_device(word: int) -> int:
+    """Status of a finished call from the device status word it wrote."""
+    return int(load_library().gdn_status_from_device(int(word)))
 
 
 def gdn_status_string(status: int) -> str:

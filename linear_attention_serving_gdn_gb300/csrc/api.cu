@@ -4,6 +4,23 @@
 
 #include "gdn_internal.cuh"
 
+namespace gdn {
+
+bool current_device(int *dev, int *sms) {
+    static int cache[kMaxDevices] = {};
+    if (cudaGetDevice(dev) != cudaSuccess) return false;
+    if (*dev >= 0 && *dev < kMaxDevices && __atomic_load_n(&cache[*dev], __ATOMIC_ACQUIRE) > 0) {
+        *sms = cache[*dev];
+        return true;
+    }
+    if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess || *sms < 1)
+        return false;
+    if (*dev >= 0 && *dev < kMaxDevices) __atomic_store_n(&cache[*dev], *sms, __ATOMIC_RELEASE);
+    return true;
+}
+
+}  // namespace gdn
+
 namespace {
 
 using gdn::kChunk;
@@ -47,11 +64,12 @@ struct RawPrep {
     float eps = 0.f;
 };
 
-gdn_status_t decode_impl(const gdn_dims_t *dims, int32_t num_rows, const gdn_bf16 *q,
-                         const gdn_bf16 *k, const gdn_bf16 *v, const float *g, const float *beta,
-                         float *state, int64_t num_slots, const int32_t *src_slot,
-                         const int32_t *dst_slot, gdn_bf16 *o, int32_t *dev_status,
-                         cudaStream_t stream, const RawPrep &raw = RawPrep()) {
+// Validates a decode call and fills its kernel arguments; launches nothing.
+gdn_status_t decode_check(const gdn_dims_t *dims, int32_t num_rows, const gdn_bf16 *q,
+                          const gdn_bf16 *k, const gdn_bf16 *v, const float *g, const float *beta,
+                          float *state, int64_t num_slots, const int32_t *src_slot,
+                          const int32_t *dst_slot, gdn_bf16 *o, int32_t *dev_status,
+                          gdn::DecodeArgs *out, const RawPrep &raw = RawPrep()) {
     gdn_status_t why = GDN_OK;
     if (!dims_ok(dims, &why)) return why;
     if (num_rows < 0 || num_slots < 0) return GDN_ERR_INVALID_ARG;
@@ -60,7 +78,7 @@ gdn_status_t decode_impl(const gdn_dims_t *dims, int32_t num_rows, const gdn_bf1
     if (!q || !k || !v || !have_gates || !state || !src_slot || !o) return GDN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(state) || !aligned16(o))
         return GDN_ERR_INVALID_ARG;
-    gdn::DecodeArgs a;
+    gdn::DecodeArgs &a = *out;
     a.num_rows = num_rows;
     a.h_k = dims->h_k;
     a.h_v = dims->h_v;
@@ -81,6 +99,18 @@ gdn_status_t decode_impl(const gdn_dims_t *dims, int32_t num_rows, const gdn_bf1
     a.A_log = raw.A_log;
     a.dt_bias = raw.dt_bias;
     a.eps = raw.eps;
+    return GDN_OK;
+}
+
+gdn_status_t decode_impl(const gdn_dims_t *dims, int32_t num_rows, const gdn_bf16 *q,
+                         const gdn_bf16 *k, const gdn_bf16 *v, const float *g, const float *beta,
+                         float *state, int64_t num_slots, const int32_t *src_slot,
+                         const int32_t *dst_slot, gdn_bf16 *o, int32_t *dev_status,
+                         cudaStream_t stream, const RawPrep &raw = RawPrep()) {
+    gdn::DecodeArgs a{};
+    const gdn_status_t s = decode_check(dims, num_rows, q, k, v, g, beta, state, num_slots, src_slot,
+                                        dst_slot, o, dev_status, &a, raw);
+    if (s != GDN_OK || num_rows == 0) return s;
     return gdn::launch_decode(a, dims->d_k, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -117,17 +147,31 @@ gdn_status_t decode_multi_impl(const gdn_dims_t *dims, int32_t num_rows, int32_t
     return gdn::launch_decode_multi(a, dims->d_k, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-gdn_status_t prefill_impl(const gdn_dims_t *dims, int32_t num_seqs, const int32_t *cu_seqlens,
-                          const int32_t *cu_host, const gdn_bf16 *q, const gdn_bf16 *k,
-                          const gdn_bf16 *v, const float *g, const float *beta, float *state,
-                          int64_t num_slots, const int32_t *src_slot, const int32_t *dst_slot,
-                          gdn_bf16 *o, float *chunk_states, int32_t E, int64_t capacity,
-                          int32_t *dev_status, cudaStream_t stream,
-                          const int32_t *emit_table = nullptr, int32_t emit_table_stride = 0,
-                          const int32_t *emit_first = nullptr) {
+// Largest emission stride: 64 E stays far inside int32 on the device.
+constexpr int32_t kMaxEmitEvery = 1 << 24;
+
+size_t workspace_need(const gdn_dims_t *, int32_t, int64_t) { return 0; }
+
+gdn_status_t workspace_ok(const gdn_dims_t *dims, int32_t num_seqs, int64_t T, const void *ws,
+                          size_t ws_bytes) {
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GDN_ERR_WORKSPACE;
+    const size_t need = workspace_need(dims, num_seqs, T);
+    if (need > 0 && (!ws || ws_bytes < need)) return GDN_ERR_WORKSPACE;
+    return GDN_OK;
+}
+
+// Validates a prefill call and fills its kernel arguments; launches nothing.
+gdn_status_t prefill_check(const gdn_dims_t *dims, int32_t num_seqs, const int32_t *cu_seqlens,
+                           const int32_t *cu_host, const gdn_bf16 *q, const gdn_bf16 *k,
+                           const gdn_bf16 *v, const float *g, const float *beta, float *state,
+                           int64_t num_slots, const int32_t *src_slot, const int32_t *dst_slot,
+                           gdn_bf16 *o, float *chunk_states, int32_t E, int64_t capacity,
+                           const void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                           gdn::PrefillArgs *out, const int32_t *emit_table = nullptr,
+                           int32_t emit_table_stride = 0, const int32_t *emit_first = nullptr) {
     gdn_status_t why = GDN_OK;
     if (!dims_ok(dims, &why)) return why;
-    if (num_seqs < 0 || num_slots < 0 || E < 0) return GDN_ERR_INVALID_ARG;
+    if (num_seqs < 0 || num_slots < 0 || E < 0 || E > kMaxEmitEvery) return GDN_ERR_INVALID_ARG;
     if (emit_table && (!emit_first || emit_table_stride < 1 || !state)) return GDN_ERR_INVALID_ARG;
     if (num_seqs == 0) return GDN_OK;
     if (!cu_seqlens || !cu_ok(cu_host, num_seqs)) return GDN_ERR_INVALID_ARG;
@@ -142,7 +186,9 @@ gdn_status_t prefill_impl(const gdn_dims_t *dims, int32_t num_seqs, const int32_
         if (need > 0 && (!chunk_states || capacity < need)) return GDN_ERR_INVALID_ARG;
     }
     if (static_cast<int64_t>(num_seqs) * dims->h_v > INT_MAX) return GDN_ERR_UNSUPPORTED;
-    gdn::PrefillArgs a;
+    const gdn_status_t ws = workspace_ok(dims, num_seqs, T, workspace, workspace_bytes);
+    if (ws != GDN_OK) return ws;
+    gdn::PrefillArgs &a = *out;
     a.num_seqs = num_seqs;
     a.h_k = dims->h_k;
     a.h_v = dims->h_v;
@@ -166,6 +212,23 @@ gdn_status_t prefill_impl(const gdn_dims_t *dims, int32_t num_seqs, const int32_
     a.emit_table = E > 0 ? emit_table : nullptr;
     a.emit_first = E > 0 ? emit_first : nullptr;
     a.emit_table_stride = emit_table_stride;
+    return GDN_OK;
+}
+
+gdn_status_t prefill_impl(const gdn_dims_t *dims, int32_t num_seqs, const int32_t *cu_seqlens,
+                          const int32_t *cu_host, const gdn_bf16 *q, const gdn_bf16 *k,
+                          const gdn_bf16 *v, const float *g, const float *beta, float *state,
+                          int64_t num_slots, const int32_t *src_slot, const int32_t *dst_slot,
+                          gdn_bf16 *o, float *chunk_states, int32_t E, int64_t capacity,
+                          const void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                          cudaStream_t stream, const int32_t *emit_table = nullptr,
+                          int32_t emit_table_stride = 0, const int32_t *emit_first = nullptr) {
+    gdn::PrefillArgs a{};
+    const gdn_status_t s = prefill_check(dims, num_seqs, cu_seqlens, cu_host, q, k, v, g, beta, state,
+                                         num_slots, src_slot, dst_slot, o, chunk_states, E, capacity,
+                                         workspace, workspace_bytes, dev_status, &a, emit_table,
+                                         emit_table_stride, emit_first);
+    if (s != GDN_OK || num_seqs == 0) return s;
     return gdn::launch_prefill(a, dims->d_k, cu_host, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -244,10 +307,18 @@ gdn_status_t gdn_prefill_varlen(const gdn_dims_t *dims, int32_t num_seqs,
                                 int64_t num_slots, const int32_t *src_slot,
                                 const int32_t *dst_slot, gdn_bf16 *o, float *chunk_states,
                                 int32_t emit_every_chunks, int64_t chunk_states_capacity,
-                                int32_t *dev_status, void *stream) {
+                                void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                void *stream) {
     return prefill_impl(dims, num_seqs, cu_seqlens, cu_seqlens_host, q, k, v, g, beta, state,
                         num_slots, src_slot, dst_slot, o, chunk_states, emit_every_chunks,
-                        chunk_states_capacity, dev_status, static_cast<cudaStream_t>(stream));
+                        chunk_states_capacity, workspace, workspace_bytes, dev_status,
+                        static_cast<cudaStream_t>(stream));
+}
+
+size_t gdn_prefill_workspace_bytes(const gdn_dims_t *dims, int32_t num_seqs, int64_t total_tokens) {
+    gdn_status_t why = GDN_OK;
+    if (!dims_ok(dims, &why) || num_seqs < 0 || total_tokens < 0) return static_cast<size_t>(-1);
+    return workspace_need(dims, num_seqs, total_tokens);
 }
 
 gdn_status_t gdn_prefill_varlen_apc(const gdn_dims_t *dims, int32_t num_seqs,
@@ -258,13 +329,14 @@ gdn_status_t gdn_prefill_varlen_apc(const gdn_dims_t *dims, int32_t num_seqs,
                                     const int32_t *dst_slot, gdn_bf16 *o,
                                     int32_t emit_every_chunks, const int32_t *block_table,
                                     int32_t block_table_stride, const int32_t *block_first,
-                                    int32_t *dev_status, void *stream) {
+                                    void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                    void *stream) {
     if (emit_every_chunks < 1 || !block_table || !block_first || block_table_stride < 1 || !state)
         return GDN_ERR_INVALID_ARG;
     return prefill_impl(dims, num_seqs, cu_seqlens, cu_seqlens_host, q, k, v, g, beta, state,
-                        num_slots, src_slot, dst_slot, o, nullptr, emit_every_chunks, 0, dev_status,
-                        static_cast<cudaStream_t>(stream), block_table, block_table_stride,
-                        block_first);
+                        num_slots, src_slot, dst_slot, o, nullptr, emit_every_chunks, 0, workspace,
+                        workspace_bytes, dev_status, static_cast<cudaStream_t>(stream), block_table,
+                        block_table_stride, block_first);
 }
 
 gdn_status_t gdn_mixed_step(const gdn_dims_t *dims, int32_t num_decodes, int32_t num_prefills,
@@ -274,12 +346,14 @@ gdn_status_t gdn_mixed_step(const gdn_dims_t *dims, int32_t num_decodes, int32_t
                             const int32_t *dec_src_slot, const int32_t *dec_dst_slot,
                             const int32_t *pre_src_slot, const int32_t *pre_dst_slot,
                             gdn_bf16 *o, float *chunk_states, int32_t emit_every_chunks,
-                            int64_t chunk_states_capacity, int32_t *dev_status, void *stream) {
+                            int64_t chunk_states_capacity, void *workspace, size_t workspace_bytes,
+                            int32_t *dev_status, void *stream) {
     gdn_status_t why = GDN_OK;
     if (!dims_ok(dims, &why)) return why;
     if (num_decodes < 0 || num_prefills < 0) return GDN_ERR_INVALID_ARG;
     if (num_prefills > 0 && !cu_ok(cu_seqlens_p_host, num_prefills)) return GDN_ERR_INVALID_ARG;
     if (num_decodes > 0 && (!dec_src_slot || !state)) return GDN_ERR_INVALID_ARG;
+    if (num_prefills > 0 && !cu_seqlens_p) return GDN_ERR_INVALID_ARG;
     // The prefill part starts num_decodes rows into every token-major tensor;
     // rows are 16-byte multiples for the supported head dims.
     const size_t hk = static_cast<size_t>(dims->h_k) * dims->d_k;
@@ -288,24 +362,21 @@ gdn_status_t gdn_mixed_step(const gdn_dims_t *dims, int32_t num_decodes, int32_t
     auto off16 = [&](const gdn_bf16 *p, size_t row) { return p ? p + nd * row : nullptr; };
     auto offf = [&](const float *p) { return p ? p + nd * dims->h_v : nullptr; };
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // Validate both halves before launching either.
-    if (num_prefills > 0) {
-        const int64_t T = cu_seqlens_p_host[num_prefills];
-        if (T > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
-        if (!cu_seqlens_p || emit_every_chunks < 0) return GDN_ERR_INVALID_ARG;
-        if (emit_every_chunks > 0) {
-            const int64_t need = num_emits(cu_seqlens_p_host, num_prefills, emit_every_chunks);
-            if (need > 0 && (!chunk_states || chunk_states_capacity < need)) return GDN_ERR_INVALID_ARG;
-        }
-    }
-    if (num_decodes > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
-    gdn_status_t s = decode_impl(dims, num_decodes, q, k, v, g, beta, state, num_slots,
-                                 dec_src_slot, dec_dst_slot, o, dev_status, st);
+    // Both halves are validated completely before either is launched.
+    gdn::DecodeArgs da{};
+    gdn_status_t s = decode_check(dims, num_decodes, q, k, v, g, beta, state, num_slots, dec_src_slot,
+                                  dec_dst_slot, o, dev_status, &da);
     if (s != GDN_OK) return s;
-    return prefill_impl(dims, num_prefills, cu_seqlens_p, cu_seqlens_p_host, off16(q, hk),
-                        off16(k, hk), off16(v, hv), offf(g), offf(beta), state, num_slots,
-                        pre_src_slot, pre_dst_slot, o ? o + nd * hv : nullptr, chunk_states,
-                        emit_every_chunks, chunk_states_capacity, dev_status, st);
+    gdn::PrefillArgs pa{};
+    s = prefill_check(dims, num_prefills, cu_seqlens_p, cu_seqlens_p_host, off16(q, hk), off16(k, hk),
+                      off16(v, hv), offf(g), offf(beta), state, num_slots, pre_src_slot, pre_dst_slot,
+                      o ? o + nd * hv : nullptr, chunk_states, emit_every_chunks, chunk_states_capacity,
+                      workspace, workspace_bytes, dev_status, &pa);
+    if (s != GDN_OK) return s;
+    if (num_decodes > 0 && gdn::launch_decode(da, dims->d_k, st) != cudaSuccess) return GDN_ERR_CUDA;
+    if (num_prefills > 0 && gdn::launch_prefill(pa, dims->d_k, cu_seqlens_p_host, st) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    return GDN_OK;
 }
 
 int64_t gdn_prefill_num_emits(const int32_t *cu_seqlens_host, int32_t num_seqs,
@@ -344,12 +415,20 @@ int64_t gdn_floor_prefix_hit(int64_t hit_tokens, int64_t prompt_tokens, int32_t 
     return hit_tokens / b * b;
 }
 
+gdn_status_t gdn_status_from_device(int32_t word) {
+    if (word & GDN_DEV_TIMEOUT) return GDN_ERR_TIMEOUT;
+    if (word != 0) return GDN_ERR_INVALID_ARG;
+    return GDN_OK;
+}
+
 const char *gdn_status_string(gdn_status_t status) {
     switch (status) {
         case GDN_OK: return "GDN_OK";
         case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: invalid argument";
         case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: unsupported shape";
         case GDN_ERR_CUDA: return "GDN_ERR_CUDA: CUDA launch or runtime error";
+        case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace too small or misaligned";
+        case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a bounded device wait expired";
     }
     return "unknown gdn_status_t";
 }

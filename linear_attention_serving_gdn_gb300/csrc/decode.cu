@@ -190,13 +190,10 @@ decode_multi_kernel(const DecodeMultiArgs a) {
 
 template <int D>
 cudaError_t launch_decode_multi_d(const DecodeMultiArgs &a, cudaStream_t stream) {
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_multi_kernel<D>, kMultiThreads, 0);
-    if (e != cudaSuccess) return e;
+    static int occ[kMaxDevices] = {};
+    int dev = 0, sms = 0;
+    if (!current_device(&dev, &sms)) return cudaErrorInvalidDevice;
+    const int per_sm = blocks_per_sm(decode_multi_kernel<D>, kMultiThreads, dev, occ);
     const int64_t items = static_cast<int64_t>(a.num_rows) * a.h_v * (D / kMultiRows);
     const int64_t need = (items + (kMultiThreads / 32) - 1) / (kMultiThreads / 32);
     const int64_t cap = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
@@ -207,13 +204,10 @@ cudaError_t launch_decode_multi_d(const DecodeMultiArgs &a, cudaStream_t stream)
 
 template <int D, bool kRaw>
 cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t stream) {
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, kRaw>, kDecodeThreads, 0);
-    if (e != cudaSuccess) return e;
+    static int occ[kMaxDevices] = {};
+    int dev = 0, sms = 0;
+    if (!current_device(&dev, &sms)) return cudaErrorInvalidDevice;
+    const int per_sm = blocks_per_sm(decode_kernel<D, kRaw>, kDecodeThreads, dev, occ);
     const int64_t items = static_cast<int64_t>(a.num_rows) * a.h_v * (D / kRowsPerItem);
     const int64_t need = (items + (kDecodeThreads / 32) - 1) / (kDecodeThreads / 32);
     const int64_t cap = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);

@@ -75,6 +75,24 @@ struct PrefillArgs {
     int32_t emit_table_stride;
 };
 
+// Launch parameters that depend only on the device (SM count) or on a kernel
+// and the device (blocks per SM) are queried once per device and kept for the
+// life of the process, so a call costs no attribute or occupancy query.
+constexpr int kMaxDevices = 64;
+// Current device and its SM count; false if a query failed.
+bool current_device(int *dev, int *sms);
+// Blocks per SM of `kernel` at `threads` threads and no dynamic shared
+// memory on device `dev`, cached in `cache` (one slot per device).
+template <typename Kernel>
+int blocks_per_sm(Kernel kernel, int threads, int dev, int (&cache)[kMaxDevices]) {
+    if (dev >= 0 && dev < kMaxDevices && __atomic_load_n(&cache[dev], __ATOMIC_ACQUIRE) > 0)
+        return cache[dev];
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) n = 1;
+    if (dev >= 0 && dev < kMaxDevices) __atomic_store_n(&cache[dev], n, __ATOMIC_RELEASE);
+    return n;
+}
+
 // Launchers (decode.cu, prefill.cu).  Arguments are validated by the caller.
 cudaError_t launch_decode(const DecodeArgs &a, int d, cudaStream_t stream);
 cudaError_t launch_decode_multi(const DecodeMultiArgs &a, int d, cudaStream_t stream);

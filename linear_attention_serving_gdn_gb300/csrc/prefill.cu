@@ -11,130 +11,169 @@
 // Chunked form (UT / WY representation of the delta rule, Yang et al.,
 // "Parallelizing Linear Transformers with the Delta Rule over Sequence
 // Length", NeurIPS 2024, with the gating of Gated DeltaNet, ICLR 2025).
-// For a chunk of C = 64 tokens entering with state S0 (d_k x d_v), local
-// index t, G_t = sum_{s<=t} g_s, gamma_t = exp(G_t):
+// For a chunk of C = 64 tokens entering with state S (d_k x d_v), local index
+// t, G_t = sum_{s<=t} g_s, gamma_t = exp(G_t):
 //
-//     A_ts  = beta_t exp(G_t - G_s) k_t.k_s   (s < t),   T = (I + A)^-1
-//     V'    = V - diag(gamma) K S0
-//     U     = T diag(beta) V'                              (the rows u_t)
-//     O     = scale [diag(gamma) Q S0 + P U],  P_ts = exp(G_t - G_s) q_t.k_s (s <= t)
-//     S_C   = gamma_C S0 + Ktil^T U,           Ktil_t = exp(G_C - G_t) k_t
+//     A_ts = beta_t exp(G_t - G_s) k_t.k_s  (s < t),   T = (I + A)^-1
+//     T''  = T diag(beta),   T''' = T diag(beta gamma),   W = T''' K
+//     U    = T'' V - W S                                      (rows u_t)
+//     O    = Q~ S + P~ U,   Q~_t = scale gamma_t q_t,  P~_ts = scale exp(G_t - G_s) q_t.k_s (s <= t)
+//     S'   = gamma_C S + K^T diag(dec) U,   dec_t = exp(G_C - G_t)
 //
-// Products are computed transposed so that TMEM lane j is value column j:
-//     D1 = S0^T [Q;K]^T  (M = d_v, N = 128 tokens, K = d_k), double-buffered
-//     D3 = V'^T T''^T    (T'' = T diag(beta); reuses the K half of D1)
-//     D5 = gamma_C S0^T + (diag(dec) U)^T K,  dec_t = exp(G_C - G_t)
-//          (the fp32 state, accumulated in TMEM; K is read MN-major straight
-//          from its TMA tile, so Ktil is never formed)
-//     D6 = U^T P^T
-// and the Gram [Q;K] K^T (M = 128 tokens, N = 64, K = d_k).  Operands are
-// fp16 (inputs convert exactly from bf16 except below 2^-14); accumulation
-// and the state carry are fp32.
+// Only the products with S depend on the carried state; everything else
+// (Gram, decays, P~, A, the inverse, T'', W, the fp16 operand tiles) is local
+// to the chunk.  One CTA runs one (sequence, value head) chain, in two warp
+// groups:
 //
-// One CTA runs one (sequence, value head) chain, warp-specialised:
-//   chain group (warps 0-7; warps w and w + 4 share TMEM lane quarter w, so
-//     lane j is served by two threads, each taking half of the row's tokens
-//     or state columns): the steps that depend on the state,
-//     S1 -> V' -> S3 -> U -> S5/S6 -> new state, plus the output of the
-//     previous chunk while S1 runs;
-//   prep group (warps 8-15, lanes split the same way): the chunk-local
-//     operands of the next chunk -- Q/K tiles (TMA into a ring of three
-//     slots, issued a whole chunk ahead and converted to fp16 in place
-//     while the previous chunk's diagonal blocks are solved), decays, Gram,
-//     P, A, T = (I + A)^-1 (diagonal 16x16 blocks by substitution, then two
-//     doubling levels) and T'' -- into a double-buffered stage, handed over
-//     through mbarriers.
-// A chunk's arithmetic depends only on its own inputs and the fp32 state
-// entering it, so results do not depend on the batch, and restarting from an
-// emitted state reproduces the uninterrupted run bit for bit.
+//   chain group (warps 0-7; thread (j, hf): TMEM lane j = value column j,
+//     half hf of the lane's columns), per chunk:
+//       D_U  += S16^T (-W)^T          (D_U was preset to U'^T = V^T T''^T)
+//       D_O   = S16^T Q~^T            (output accumulator, two buffers)
+//       U^T, (diag(dec) U)^T -> fp16 A operands in TMEM
+//       D_S   = gamma_C D_S + (diag(dec) U)^T K,   D_O += U^T P~^T
+//       D_S  -> fp16 S16 (A operand in TMEM), emission, final state
+//     and writes the previous chunk's output while the next products run;
+//   prep group (warps 8-15), one chunk ahead: q, k, v tiles by TMA, the Gram
+//     [Q;K] K^T in bf16 straight from the TMA tiles, decays, P~, A, the
+//     inverse (16x16 diagonal blocks by substitution and the first doubling
+//     level on the CUDA cores in fp32; the second level, the 32x32 lower-left
+//     block, as two tcgen05 products), T'' and -T''', q~/k/v converted to fp16
+//     in place, U'^T preset by the chain's tensor-core issuer, and
+//     -W^T = K^T (-T''')^T.
 //
-// Every shared-memory index that depends on the thread index is masked to
-// its array's range, so no address can leave the allocation even for a
-// thread outside the branch that guards it.
+// The fp32 state lives in TMEM for the whole chain; its fp16 copy (an operand)
+// is written once per chunk.  A chunk's arithmetic depends only on its own
+// inputs and the fp32 state entering it, so results do not depend on the
+// batch, and restarting from an emitted state reproduces the uninterrupted
+// run bit for bit.
+//
+// Every wait is bounded.  A wait that runs out sets GDN_DEV_TIMEOUT, both
+// groups agree on the failure at their next group barrier and leave their
+// loops, and before TMEM is released the threads that issued asynchronous
+// work wait (again bounded) for every MMA and TMA copy still in flight.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "gdn_internal.cuh"
 #include "tc_ptx.cuh"
+
+#ifndef GDN_WAIT_CYCLES
+#define GDN_WAIT_CYCLES 2000000000LL
+#endif
 
 namespace gdn {
 namespace {
 
 constexpr int kThreads = 512;  // chain group + prep group
-constexpr int kGroup = 256;    // 8 warps per group: two warps per TMEM lane quarter
-constexpr int kBarChain = 1;   // named barrier ids (0 is __syncthreads)
+constexpr int kGroup = 256;
+constexpr int kBarChain = 1;  // named barrier ids (0 is __syncthreads)
 constexpr int kBarPrep = 2;
-// Upper bound on every wait, in SM clock cycles (~1 s): a wait that runs out
-// reports GDN_DEV_TIMEOUT instead of hanging.
-constexpr long long kWaitCycles = 2000000000LL;
+// Limit of every handshake wait between the groups, in SM clock cycles
+// (~1 s by default); a build may shorten it to exercise the failure path.
+constexpr long long kWaitCycles = GDN_WAIT_CYCLES;
+// Limit of the waits for work already in flight when a chain stops (~1 s).
+constexpr long long kDrainCycles = 2000000000LL;
 constexpr int kMaxOrder = 2048;
 
 struct PrefillLaunch {
     CUtensorMap tm_q, tm_k;  // q, k as 2-D [T][h_k d] bf16, 64 x 64 boxes, 128-byte swizzle
+    CUtensorMap tm_v;        // v as 2-D [T][h_v d] bf16, same boxes
     PrefillArgs a;
     int32_t n_order;
     int32_t order[kMaxOrder];  // launch rank -> sequence, longest first
 };
 
+// Row stride of the 64x64 fp32 inverse scratch: 68 floats keep 16-byte
+// alignment and put 8 consecutive rows on disjoint bank quads.
+constexpr int kLdM = 68;
+
 template <int D>
 struct Smem {
-    // Tensor-core operand tiles (K-major, 128-byte swizzle, 1024-aligned).
-    static constexpr uint32_t kQKBytes = 128 * D * 2;          // fp16 [128 rows: q then k][D]
-    static constexpr uint32_t kQK0 = 0;                          // ring of three slots
-    static constexpr uint32_t kTpp0 = kQK0 + 3 * kQKBytes;     // fp16 [64 rows t][64]  T''
-    static constexpr uint32_t kTpp1 = kTpp0 + 8192;
-    static constexpr uint32_t kP0 = kTpp1 + 8192;              // fp16 [64 rows t][64]  P
-    static constexpr uint32_t kP1 = kP0 + 8192;
-    static constexpr uint32_t kS0T = kP1 + 8192;               // fp16 [128 rows j][D]  S0^T
-    static constexpr uint32_t kVpT = kS0T + 128 * D * 2;       // fp16 [128 rows j][64] V'^T, then (diag(dec) U)^T
-    static constexpr uint32_t kUT = kVpT + 16384;              // fp16 [128 rows j][64] U^T
+    // Operand tiles (128-byte swizzle, 1024-aligned).
+    static constexpr uint32_t kQKBytes = 256u * D;  // per 64-wide block of d: q box (8 KB), k box (8 KB)
+    static constexpr uint32_t kQK0 = 0;             // ring of three slots
+    static constexpr uint32_t kVBytes = 128u * D;   // v boxes, 8 KB apart
+    static constexpr uint32_t kV0 = kQK0 + 3 * kQKBytes;  // ring of two slots
+    static constexpr uint32_t kWT = kV0 + 2 * kVBytes;    // -W^T [i][t] fp16 (MN-major B of S16 (-W)^T)
+    static constexpr uint32_t kP0 = kWT + 128u * D;       // P~ [t][s] fp16, two stages
+    static constexpr uint32_t kTpp = kP0 + 16384;         // T'' [t][s] fp16
+    static constexpr uint32_t kTppp = kTpp + 8192;        // -T''' [t][s] fp16
+    static constexpr uint32_t kL2A1 = kTppp + 8192;       // A_B (rows 32..63, cols 0..31 of A), K-major
+    static constexpr uint32_t kL2B1 = kL2A1 + 4096;       // T_top, MN-major B
+    static constexpr uint32_t kL2A2 = kL2B1 + 4096;       // T_bot, K-major
+    static constexpr uint32_t kL2B2 = kL2A2 + 4096;       // -X = -(A_B T_top), MN-major B
     // Plain buffers.
-    static constexpr uint32_t kGam0 = kUT + 16384;             // f32 [64] exp(G_t), stage 0
-    static constexpr uint32_t kGam1 = kGam0 + 256;
-    static constexpr uint32_t kGamC = kGam1 + 256;             // f32 [2][64] chain group's copies
-    static constexpr uint32_t kM = kGamC + 512;                // f32 [64][kLdM] A, then T
-    static constexpr uint32_t kW = kM + 64 * 68 * 4;           // f32 [4][16][16] block products
-    static constexpr uint32_t kG = kW + 4096;                  // f32 [64] cumulative log decay
-    static constexpr uint32_t kBeta = kG + 256;                // f32 [64]
-    static constexpr uint32_t kGraw = kBeta + 256;             // f32 [64]
-    static constexpr uint32_t kDec = kGraw + 256;              // f32 [2][64] exp(G_C - G_t), per stage
-    static constexpr uint32_t kBars = kDec + 512;              // 9 mbarriers
-    static constexpr uint32_t kTmem = kBars + 128;             // TMEM base address
-    static constexpr uint32_t kFail = kTmem + 4;               // int
-    static constexpr uint32_t kEoff = kFail + 4;               // long long [16]
+    static constexpr uint32_t kM = kL2B2 + 4096;          // f32 [64][kLdM]: A, then T
+    static constexpr uint32_t kWb = kM + 64 * kLdM * 4;   // f32 [2][16][16] level-1 products
+    static constexpr uint32_t kG = kWb + 4096;            // f32 [64] cumulative log decay
+    static constexpr uint32_t kGam = kG + 256;            // f32 [64] gamma
+    static constexpr uint32_t kBG = kGam + 256;           // f32 [64] beta gamma
+    static constexpr uint32_t kBeta = kBG + 256;          // f32 [64]
+    static constexpr uint32_t kGraw = kBeta + 256;        // f32 [64]
+    static constexpr uint32_t kDec = kGraw + 256;         // f32 [2][64] exp(G_C - G_t), per stage
+    static constexpr uint32_t kGc = kDec + 512;           // f32 [2] gamma_C, per stage
+    static constexpr uint32_t kBars = kGc + 16;           // 18 mbarriers
+    static constexpr uint32_t kTmem = kBars + 18 * 8;     // TMEM base address
+    static constexpr uint32_t kFail = kTmem + 4;          // int
+    static constexpr uint32_t kEoff = kFail + 12;         // long long [16]
     static constexpr uint32_t kBytes = kEoff + 128;
-    static constexpr uint32_t kAlloc = kBytes + 1024;          // + alignment slack
-    static_assert(kS0T % 1024 == 0 && kVpT % 1024 == 0 && kUT % 1024 == 0 && kBars % 8 == 0, "");
-    static_assert(kTpp0 % 1024 == 0 && kP0 % 1024 == 0 && kQKBytes % 1024 == 0, "");
-    static_assert(kM % 16 == 0 && kW % 16 == 0, "float4 access to the scratch");
+    static constexpr uint32_t kAlloc = kBytes + 1024;     // + alignment slack
+    static_assert(kV0 % 1024 == 0 && kWT % 1024 == 0 && kP0 % 1024 == 0 && kTpp % 1024 == 0, "");
+    static_assert(kL2A1 % 1024 == 0 && kL2A2 % 1024 == 0 && kL2B1 % 1024 == 0 && kL2B2 % 1024 == 0, "");
+    // A level-2 MMA reads 128 rows (16 KB) of its A tile; rows past 31 are
+    // don't-care but must lie inside the allocation.
+    static_assert(kL2A2 + 16384 <= kBytes, "");
+    static_assert(kM % 16 == 0 && kWb % 16 == 0 && kBars % 8 == 0 && kEoff % 8 == 0, "");
     static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
-// TMEM column map (512 columns; lane j = value column j).
-constexpr uint32_t kColD1 = 0;      // two buffers of 128: [0,64) (Q S0)^T, [64,128) (K S0)^T then U^T
-constexpr uint32_t kColD5 = 256;    // S^T state, D columns
-constexpr uint32_t kColD6 = 384;    // (P U)^T
-constexpr uint32_t kColGram = 448;  // lanes 0..63: Q K^T rows, 64..127: K K^T rows
+// TMEM column map (512 columns; lane j = value column j, or row of a prep product).
+constexpr uint32_t kColS = 0;       // fp32 state S^T, D columns
+constexpr uint32_t kColU = 128;     // U^T, 64 columns
+constexpr uint32_t kColO = 192;     // output accumulator O^T, two buffers of 64
+constexpr uint32_t kColS16 = 320;   // S^T fp16, packed (D / 2 columns): A operand
+constexpr uint32_t kColU16 = 384;   // U^T fp16 packed: A operand
+constexpr uint32_t kColUd16 = 416;  // (diag(dec) U)^T fp16 packed: A operand
+constexpr uint32_t kColPrep = 448;  // prep products: Gram; X and T_B; -W^T
 constexpr uint32_t kTmemCols = 512;
+
+// mbarriers.
+enum : int {
+    kBarTmaQK = 0,   // [3] q/k slot loaded
+    kBarTmaV = 3,    // [2] v slot loaded
+    kBarGram = 5,    // Gram done
+    kBarL2 = 6,      // level-2 products done (two per chunk)
+    kBarW = 7,       // -W^T done
+    kBarUReady = 8,  // T'' and v of the next chunk ready (chain may preset U'^T)
+    kBarReady = 9,   // [2] a chunk's operands ready for the chain
+    kBarA = 11,      // chain: D_U complete
+    kBarC = 12,      // chain: state update and output complete
+    kBarWFree = 13,  // chain done reading -W^T
+    kBarTFree = 14,  // chain done reading T'' and its v slot
+    kBarQKFree = 15, // chain done reading a q/k slot and its P~ / decay stage
+    kBarDrainC = 16,
+    kBarDrainP = 17,
+    kNumBars = 18
+};
 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// 8 bf16 (one uint4) -> 8 fp16 (one uint4), exact except below 2^-14.
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 w) {
+// 8 bf16 (one uint4) -> 8 fp16 times f (exact for f = 1 except below 2^-14).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 w, float f) {
     uint4 r;
-    r.x = pack_half2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
-    r.y = pack_half2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
-    r.z = pack_half2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u));
-    r.w = pack_half2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
+    r.x = pack_half2(f * __uint_as_float(w.x << 16), f * __uint_as_float(w.x & 0xffff0000u));
+    r.y = pack_half2(f * __uint_as_float(w.y << 16), f * __uint_as_float(w.y & 0xffff0000u));
+    r.z = pack_half2(f * __uint_as_float(w.z << 16), f * __uint_as_float(w.z & 0xffff0000u));
+    r.w = pack_half2(f * __uint_as_float(w.w << 16), f * __uint_as_float(w.w & 0xffff0000u));
     return r;
 }
 
-// TMA: one 2-D box of a tensor map into shared memory, completing on an
-// mbarrier that expects the box's bytes.
 __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -146,54 +185,41 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(bar)), "r"(bytes)
                  : "memory");
 }
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
 
-// Writes columns [c0, c0 + 32) of row r (fp32 bit patterns) as fp16 into a
-// 128-row K-major SW128 tile.
-__device__ __forceinline__ void store_f16_chunks32(uint8_t *tile, uint32_t r, int c0, const uint32_t (&x)[32]) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint4 v;
-        v.x = pack_half2(__uint_as_float(x[8 * q + 0]), __uint_as_float(x[8 * q + 1]));
-        v.y = pack_half2(__uint_as_float(x[8 * q + 2]), __uint_as_float(x[8 * q + 3]));
-        v.z = pack_half2(__uint_as_float(x[8 * q + 4]), __uint_as_float(x[8 * q + 5]));
-        v.w = pack_half2(__uint_as_float(x[8 * q + 6]), __uint_as_float(x[8 * q + 7]));
-        *reinterpret_cast<uint4 *>(tile + tc::sw128_chunk_offset(r, c0 / 8 + q, 128)) = v;
+// Byte offset of 16-byte chunk c (8 fp16 along N) of row k of an MN-major
+// SW128 tile (rows are the K index, 64 N elements per 128-byte row).
+__device__ __forceinline__ uint32_t mn_chunk_offset(uint32_t k, uint32_t c) {
+    return (k >> 3) * 1024u + (k & 7u) * 128u + (((c & 7u) ^ (k & 7u)) << 4);
+}
+
+// Bounded wait for the phase of `bar` with the given parity; gives up as
+// soon as any thread has flagged a failure, and flags one when it runs out.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, int *fail) {
+    const long long start = clock64();
+    while (!tc::mbar_try_wait(bar, parity)) {
+        if (*reinterpret_cast<volatile int *>(fail)) return false;
+        if (clock64() - start > kWaitCycles) {
+            atomicExch(fail, 1);
+            return false;
+        }
     }
+    return true;
 }
-
-// Writes 8 fp32 values as the 16-byte fp16 chunk `chunk` of row r of a K-major
-// SW128 tile of `rows` rows.
-__device__ __forceinline__ void store_chunk8_f16(uint8_t *tile, uint32_t rows, uint32_t r, uint32_t chunk,
-                                                 const float *x) {
-    uint4 v;
-    v.x = pack_half2(x[0], x[1]);
-    v.y = pack_half2(x[2], x[3]);
-    v.z = pack_half2(x[4], x[5]);
-    v.w = pack_half2(x[6], x[7]);
-    *reinterpret_cast<uint4 *>(tile + tc::sw128_chunk_offset(r, chunk, rows)) = v;
-}
-
-__device__ __forceinline__ uint32_t lane_addr(uint32_t tbase, int warp, uint32_t col) {
-    return tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + col;
-}
-
-template <int N>
-__device__ __forceinline__ void tmem_load_row(uint32_t taddr, float (&x)[N]) {
-    static_assert(N % 32 == 0, "");
-#pragma unroll
-    for (int c = 0; c < N; c += 32) {
-        uint32_t r[32];
-        tc::tmem_ld32(taddr + c, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[c + i] = __uint_as_float(r[i]);
-    }
+// Bounded wait for work already in flight (ignores the failure flag).
+__device__ __forceinline__ bool drain_bar(uint64_t *bar, uint32_t parity) {
+    const long long start = clock64();
+    while (!tc::mbar_try_wait(bar, parity))
+        if (clock64() - start > kDrainCycles) return false;
+    return true;
 }
 
 // Group barrier (named barrier over the group's 256 threads).
 __device__ __forceinline__ void group_sync(int id) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(kGroup) : "memory");
 }
-
 // Group barrier that returns true if any thread of the group passed `pred`.
 __device__ __forceinline__ bool group_any(int id, bool pred) {
     uint32_t r;
@@ -208,26 +234,11 @@ __device__ __forceinline__ bool group_any(int id, bool pred) {
     return r != 0;
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
-}
-
-// Bounded wait for the phase of `bar` with the given parity.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
-    const long long start = clock64();
-    while (!tc::mbar_try_wait(bar, parity))
-        if (clock64() - start > kWaitCycles) return false;
-    return true;
-}
-
-// Row stride of the 64x64 fp32 scratch: 68 floats keep 16-byte alignment and
-// put 8 consecutive rows on disjoint bank quads.
-constexpr int kLdM = 68;
-
 // Sum over s' < s of floor(L_s' / (64 E)), by the whole block.
 __device__ int64_t emit_offset(const int32_t *cu, int s, int E, long long *part) {
     long long acc = 0;
-    for (int i = threadIdx.x; i < s; i += blockDim.x) acc += (cu[i + 1] - cu[i]) / (kChunk * E);
+    const long long per = static_cast<long long>(kChunk) * E;
+    for (int i = threadIdx.x; i < s; i += blockDim.x) acc += (cu[i + 1] - cu[i]) / per;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = acc;
@@ -239,16 +250,12 @@ __device__ int64_t emit_offset(const int32_t *cu, int s, int E, long long *part)
     return tot;
 }
 
-// In place, M := (I + M)^-1 for a 64x64 strictly lower-triangular M (the
-// diagonal and upper triangle of M are ignored; the result has unit diagonal
-// and zeros above it inside the diagonal blocks), in two parts run by the
-// prep group (p = thread index within the group, 0..255).
-//
-// Part 1 (threads p < 64, block b = p / 16, column c = p % 16): the four
-// 16x16 diagonal blocks by right-looking forward substitution; each step
+// ---- the inverse, CUDA-core part ----------------------------------------------
+// Diagonal 16x16 blocks of T = (I + A)^-1 for a strictly lower-triangular A
+// held in M (fp32, row stride kLdM), by the 64 threads p < 64 (block
+// p / 16, column p % 16): right-looking forward substitution; each step
 // finishes x_j and updates the later rows independently of each other.
-// The new columns are kept in x[] and written by invert_diag_store after a
-// group barrier, once every thread has read the block's A entries.
+// The column is written over the block's A entries after a warp barrier.
 __device__ __forceinline__ void invert_diag_solve(const float *M, int p, float (&x)[16]) {
     const int c = p & 15, base = ((p >> 4) & 3) * 16;
     float acc[16];
@@ -262,18 +269,10 @@ __device__ __forceinline__ void invert_diag_solve(const float *M, int p, float (
         for (int i = j + 1; i < 16; ++i) acc[i] = fmaf(M[(base + i) * kLdM + base + j], xj, acc[i]);
     }
 }
-
-// Also writes the block's columns of T'' = T diag(beta) as fp16 into the
-// 64-row K-major operand tile Tpp (upper blocks of Tpp stay zero).
-__device__ __forceinline__ void invert_diag_store(float *M, int p, const float (&x)[16], uint8_t *Tpp,
-                                                  const float *beta) {
+__device__ __forceinline__ void invert_diag_store(float *M, int p, const float (&x)[16]) {
     const int c = p & 15, base = ((p >> 4) & 3) * 16;
-    const float bc = beta[base + c];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        M[(base + i) * kLdM + base + c] = x[i];
-        *reinterpret_cast<__half *>(Tpp + tc::sw128_offset(base + i, base + c, 64)) = __float2half_rn(x[i] * bc);
-    }
+    for (int i = 0; i < 16; ++i) M[(base + i) * kLdM + base + c] = x[i];
 }
 
 __device__ __forceinline__ void fma4(float4 &acc, float a, const float4 &t) {
@@ -282,20 +281,7 @@ __device__ __forceinline__ void fma4(float4 &acc, float a, const float4 &t) {
     acc.z = fmaf(a, t.z, acc.z);
     acc.w = fmaf(a, t.w, acc.w);
 }
-
-// Part 2, the off-diagonal blocks, as two doubling levels (16 block
-// products in four phases): with T_aa the inverted diagonal
-// blocks,
-//   level 1 (pairs of 16-blocks):  T_10 = -T_11 (A_10 T_00),  T_32 = -T_33 (A_32 T_22);
-//   level 2 (rows 32..63 x columns 0..31):  X = A_B T_top,  T_B = -T_bottom X,
-//   T_top = [[T_00, 0], [T_10, T_11]],  T_bottom = [[T_22, 0], [T_32, T_33]],
-//   i.e. X_a0 = A_a0 T_00 + A_a1 T_10, X_a1 = A_a1 T_11 (a = 2, 3),
-//        T_2b = -T_22 X_2b,  T_3b = -(T_32 X_2b + T_33 X_3b).
-// Level 1 runs in the two warps that solved the diagonal blocks (warp
-// barriers only); each level-2 output 16x16 block is computed by 64 threads
-// (row i = (p/4) % 16, columns 4 (p%4) .. + 3, float4 accesses) with
-// compile-time block indices per task.  Results go to M and, scaled by beta, as fp16 to the
-// T'' tile.  The caller provides the barrier after the last phase.
+// acc += X[i][0..16) * Y[0..16)[4cq .. 4cq + 4) for 16x16 blocks X, Y.
 template <int LDX, int LDY>
 __device__ __forceinline__ void block_mac(float4 &acc, const float *X, const float *Y, int i, int cq) {
 #pragma unroll
@@ -308,101 +294,92 @@ __device__ __forceinline__ void block_mac(float4 &acc, const float *X, const flo
         fma4(acc, x4.w, *reinterpret_cast<const float4 *>(y + 3 * LDY));
     }
 }
-
-template <int A, int B>
-__device__ __forceinline__ void store_t_block(float *M, uint8_t *Tpp, const float *beta, int i, int cq,
-                                              const float4 &acc) {
-    const int row = A * 16 + i, col = B * 16 + 4 * cq;
-    *reinterpret_cast<float4 *>(M + row * kLdM + col) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-    const float4 b4 = *reinterpret_cast<const float4 *>(beta + col);
-    uint2 hv;
-    hv.x = pack_half2(-acc.x * b4.x, -acc.y * b4.y);
-    hv.y = pack_half2(-acc.z * b4.z, -acc.w * b4.w);
-    *reinterpret_cast<uint2 *>(Tpp + tc::sw128_offset(row, col, 64)) = hv;
-}
-
-#define GDN_MB(a, b) (M + ((a) * 16) * kLdM + (b) * 16)
-// Level 1 by one warp (the warp that solved diagonal blocks A-1 and A):
-// lane = (row i = lane / 2, columns 8 (lane % 2) .. + 7), two float4 each;
-// Y_{A,A-1} = A_{A,A-1} T_{A-1,A-1} into W block (A == 3), then
-// T_{A,A-1} = -T_AA Y, with warp barriers only.
-template <int A>
-__device__ __forceinline__ void level1_warp(float *M, float *W, int lane, uint8_t *Tpp, const float *beta) {
+// First doubling level by one warp (the warp that solved diagonal blocks
+// B-1 and B): T_{B,B-1} = -T_BB (A_{B,B-1} T_{B-1,B-1}), in fp32.  Lane =
+// (row i = lane / 2, columns 8 (lane % 2) .. + 7).
+template <int B>
+__device__ __forceinline__ void level1_warp(float *M, float *Wb, int lane) {
     const int i = (lane >> 1) & 15, h = lane & 1;
-    float *Wy = W + (A == 3 ? 256 : 0);
+    float *Y = Wb + (B == 3 ? 256 : 0);
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        block_mac<kLdM, kLdM>(acc, M + (A * 16) * kLdM + (A - 1) * 16, M + ((A - 1) * 16) * kLdM + (A - 1) * 16, i,
+        block_mac<kLdM, kLdM>(acc, M + (B * 16) * kLdM + (B - 1) * 16, M + ((B - 1) * 16) * kLdM + (B - 1) * 16, i,
                               2 * h + u);
-        *reinterpret_cast<float4 *>(Wy + i * 16 + 4 * (2 * h + u)) = acc;
+        *reinterpret_cast<float4 *>(Y + i * 16 + 4 * (2 * h + u)) = acc;
     }
     __syncwarp();
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        block_mac<kLdM, 16>(acc, M + (A * 16) * kLdM + A * 16, Wy, i, 2 * h + u);
-        store_t_block<A, A - 1>(M, Tpp, beta, i, 2 * h + u, acc);
+        block_mac<kLdM, 16>(acc, M + (B * 16) * kLdM + B * 16, Y, i, 2 * h + u);
+        *reinterpret_cast<float4 *>(M + (B * 16 + i) * kLdM + (B - 1) * 16 + 4 * (2 * h + u)) =
+            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
 }
 
-template <int A, int B>  // level 2, X_AB into W block 2 (A - 2) + B
-__device__ __forceinline__ void l2_x(float *M, float *W, int i, int cq) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (B == 0) block_mac<kLdM, kLdM>(acc, GDN_MB(A, 0), GDN_MB(0, 0), i, cq);
-    block_mac<kLdM, kLdM>(acc, GDN_MB(A, 1), GDN_MB(1, B), i, cq);
-    *reinterpret_cast<float4 *>(W + (2 * (A - 2) + B) * 256 + i * 16 + 4 * cq) = acc;
-}
-template <int A, int B>  // level 2, T_AB = -(T_A2 X_2B + [A == 3] T_33 X_3B)
-__device__ __forceinline__ void l2_t(float *M, float *W, int i, int cq, uint8_t *Tpp, const float *beta) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    block_mac<kLdM, 16>(acc, GDN_MB(A, 2), W + B * 256, i, cq);
-    if (A == 3) block_mac<kLdM, 16>(acc, GDN_MB(3, 3), W + (2 + B) * 256, i, cq);
-    store_t_block<A, B>(M, Tpp, beta, i, cq, acc);
-}
-#undef GDN_MB
-
-// Level 2 (level 1 was done per warp right after the diagonal blocks).
-__device__ __forceinline__ void invert_offdiag(float *M, float *W, int p, uint8_t *Tpp, const float *beta) {
-    const int task = (p >> 6) & 3, i = (p >> 2) & 15, cq = p & 3;  // task uniform over 2 warps
-    switch (task) {
-        case 0: l2_x<2, 0>(M, W, i, cq); break;
-        case 1: l2_x<2, 1>(M, W, i, cq); break;
-        case 2: l2_x<3, 0>(M, W, i, cq); break;
-        default: l2_x<3, 1>(M, W, i, cq); break;
+// Writes 16 fp32 values v (columns 16q .. 16q + 15 of row t) as T'' = v beta
+// and -T''' = -v beta gamma into the two 64-row K-major fp16 tiles.
+__device__ __forceinline__ void store_t_segment(uint8_t *Tpp, uint8_t *Tppp, int t, int q, const float (&v)[16],
+                                                const float *beta, const float *bg) {
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+        const int s0 = 16 * q + 8 * h2;
+        uint4 a, b;
+        a.x = pack_half2(v[8 * h2 + 0] * beta[s0 + 0], v[8 * h2 + 1] * beta[s0 + 1]);
+        a.y = pack_half2(v[8 * h2 + 2] * beta[s0 + 2], v[8 * h2 + 3] * beta[s0 + 3]);
+        a.z = pack_half2(v[8 * h2 + 4] * beta[s0 + 4], v[8 * h2 + 5] * beta[s0 + 5]);
+        a.w = pack_half2(v[8 * h2 + 6] * beta[s0 + 6], v[8 * h2 + 7] * beta[s0 + 7]);
+        b.x = pack_half2(-v[8 * h2 + 0] * bg[s0 + 0], -v[8 * h2 + 1] * bg[s0 + 1]);
+        b.y = pack_half2(-v[8 * h2 + 2] * bg[s0 + 2], -v[8 * h2 + 3] * bg[s0 + 3]);
+        b.z = pack_half2(-v[8 * h2 + 4] * bg[s0 + 4], -v[8 * h2 + 5] * bg[s0 + 5]);
+        b.w = pack_half2(-v[8 * h2 + 6] * bg[s0 + 6], -v[8 * h2 + 7] * bg[s0 + 7]);
+        const uint32_t off = tc::sw128_chunk_offset(t, 2 * q + h2, 64);
+        *reinterpret_cast<uint4 *>(Tpp + off) = a;
+        *reinterpret_cast<uint4 *>(Tppp + off) = b;
     }
-    group_sync(kBarPrep);
-    switch (task) {
-        case 0: l2_t<2, 0>(M, W, i, cq, Tpp, beta); break;
-        case 1: l2_t<2, 1>(M, W, i, cq, Tpp, beta); break;
-        case 2: l2_t<3, 0>(M, W, i, cq, Tpp, beta); break;
-        default: l2_t<3, 1>(M, W, i, cq, Tpp, beta); break;
+}
+
+// Writes 32 values (fp32 bit patterns, scaled by f) as the four 16-byte fp16
+// chunks of a 32-column row: K-major row (`kmajor`) or MN-major row k.
+__device__ __forceinline__ void store_row32_f16(uint8_t *tile, int row, const uint32_t (&x)[32], float f,
+                                                bool kmajor) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 v;
+        v.x = pack_half2(f * __uint_as_float(x[8 * q + 0]), f * __uint_as_float(x[8 * q + 1]));
+        v.y = pack_half2(f * __uint_as_float(x[8 * q + 2]), f * __uint_as_float(x[8 * q + 3]));
+        v.z = pack_half2(f * __uint_as_float(x[8 * q + 4]), f * __uint_as_float(x[8 * q + 5]));
+        v.w = pack_half2(f * __uint_as_float(x[8 * q + 6]), f * __uint_as_float(x[8 * q + 7]));
+        const uint32_t off = kmajor ? tc::sw128_chunk_offset(row, q, 128) : mn_chunk_offset(row, q);
+        *reinterpret_cast<uint4 *>(tile + off) = v;
     }
 }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
+prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
     using SM = Smem<D>;
+    constexpr int kKB = D / 64;                              // 64-wide blocks of d
+    constexpr uint32_t kLboK = D == 128 ? 16384u : 0u;       // k box stride inside a q/k slot
+    constexpr uint32_t kLboV = D == 128 ? 8192u : 0u;        // v box stride inside a v slot
     const PrefillArgs &a = L.a;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    // Stage s (chunk parity) buffers, by offset from stage 0.
-    auto sQK = [&](int st) { return sm + SM::kQK0 + st * SM::kQKBytes; };
-    auto sTpp = [&](int st) { return sm + SM::kTpp0 + st * 8192; };
+    auto sQK = [&](int slot) { return sm + SM::kQK0 + slot * SM::kQKBytes; };
+    auto sV = [&](int slot) { return sm + SM::kV0 + slot * SM::kVBytes; };
     auto sP = [&](int st) { return sm + SM::kP0 + st * 8192; };
-    auto sGam = [&](int st) { return reinterpret_cast<float *>(sm + SM::kGam0 + st * 256); };
-    auto sGamC = [&](int st) { return reinterpret_cast<float *>(sm + SM::kGamC + st * 256); };
-    uint8_t *sS0T = sm + SM::kS0T, *sVpT = sm + SM::kVpT, *sUT = sm + SM::kUT;
-    float *sM = reinterpret_cast<float *>(sm + SM::kM), *sW = reinterpret_cast<float *>(sm + SM::kW);
-    float *sG = reinterpret_cast<float *>(sm + SM::kG), *sBeta = reinterpret_cast<float *>(sm + SM::kBeta);
-    float *sGraw = reinterpret_cast<float *>(sm + SM::kGraw);
     auto sDec = [&](int st) { return reinterpret_cast<float *>(sm + SM::kDec + st * 256); };
+    uint8_t *sWT = sm + SM::kWT, *sTpp = sm + SM::kTpp, *sTppp = sm + SM::kTppp;
+    uint8_t *sL2A1 = sm + SM::kL2A1, *sL2B1 = sm + SM::kL2B1, *sL2A2 = sm + SM::kL2A2, *sL2B2 = sm + SM::kL2B2;
+    float *sM = reinterpret_cast<float *>(sm + SM::kM), *sWb = reinterpret_cast<float *>(sm + SM::kWb);
+    float *sG = reinterpret_cast<float *>(sm + SM::kG), *sGam = reinterpret_cast<float *>(sm + SM::kGam);
+    float *sBG = reinterpret_cast<float *>(sm + SM::kBG), *sBeta = reinterpret_cast<float *>(sm + SM::kBeta);
+    float *sGraw = reinterpret_cast<float *>(sm + SM::kGraw), *sGc = reinterpret_cast<float *>(sm + SM::kGc);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SM::kBars);
-    // ready / freeb per stage (chunk parity); tma_bar per Q/K slot (chunk mod 3).
-    uint64_t *mma_bar = bars + 0, *gram_bar = bars + 1, *ready = bars + 2, *freeb = bars + 4, *tma_bar = bars + 6;
     uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(sm + SM::kTmem);
     int *fail = reinterpret_cast<int *>(sm + SM::kFail);
+    const volatile int *vfail = fail;
     long long *part = reinterpret_cast<long long *>(sm + SM::kEoff);
 
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -416,7 +393,7 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
     const int emit_first = a.emit_table ? a.emit_first[seq] : 0;
     const int src = a.src_slot ? a.src_slot[seq] : -1;
     const int dst = a.dst_slot ? a.dst_slot[seq] : -1;
-    const size_t ldq = static_cast<size_t>(a.h_k) * D, ldv = static_cast<size_t>(a.h_v) * D;
+    const size_t ldv = static_cast<size_t>(a.h_v) * D;
     const int n_chunks = (Lseq + kChunk - 1) / kChunk;
 
     if (src >= a.num_slots || dst >= a.num_slots) {
@@ -435,48 +412,36 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
         tc::tmem_relinquish();
     }
     if (tid == 0) {
-        tc::mbar_init(mma_bar, 1);
-        tc::mbar_init(gram_bar, 1);
-        tc::mbar_init(ready + 0, kGroup);
-        tc::mbar_init(ready + 1, kGroup);
-        tc::mbar_init(freeb + 0, kGroup);
-        tc::mbar_init(freeb + 1, kGroup);
-        tc::mbar_init(tma_bar + 0, 1);
-        tc::mbar_init(tma_bar + 1, 1);
-        tc::mbar_init(tma_bar + 2, 1);
+        for (int b = 0; b < kNumBars; ++b) tc::mbar_init(bars + b, 1);
         *fail = 0;
-    }
-    for (int e = tid; e < 2 * 8192 / 16; e += kThreads)  // upper blocks of T'' stay zero
-        reinterpret_cast<uint4 *>(sm + SM::kTpp0)[e] = make_uint4(0, 0, 0, 0);
-    if (D < 128) {  // rows >= D of the transposed operand tiles stay zero (d = 64 pads M to 128)
-        for (int e = tid; e < 128 * D * 2 / 16; e += kThreads)
-            reinterpret_cast<uint4 *>(sS0T)[e] = make_uint4(0, 0, 0, 0);
-        for (int e = tid; e < 16384 / 16; e += kThreads) {
-            reinterpret_cast<uint4 *>(sVpT)[e] = make_uint4(0, 0, 0, 0);
-            reinterpret_cast<uint4 *>(sUT)[e] = make_uint4(0, 0, 0, 0);
-        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tbase = *tmem_ptr;
-    const uint32_t my_lane = lane_addr(tbase, warp, 0);
+    const uint32_t tl = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);  // this warp's TMEM lanes
 
     if (warp < 8) {
         // ============================ chain group ==============================
-        // Thread (j, hf): value column j (TMEM lane j), half hf of the row's work.
         const int j = tid & 127, hf = tid >> 7;
-        const int jm = j & (D - 1);
-        constexpr int kHalfD = D / 2;  // state columns per thread
-        // Initial state row j, columns [hf D/2, (hf+1) D/2): fp32 into D5, fp16
-        // into the S0^T tile; or, for an empty sequence, to the destination.
-        if (j < D) {
-            const float *sp = src >= 0 ? a.state + ((static_cast<size_t>(src) * a.h_v + h) * D + jm) * D : nullptr;
-            float *dp = (Lseq == 0 && dst >= 0) ? a.state + ((static_cast<size_t>(dst) * a.h_v + h) * D + jm) * D
+        const bool jv = j < D;  // warp-uniform: d = 64 leaves lane quarters 2, 3 without a column
+        constexpr int kHalf = D / 2;
+        const uint32_t idU = tc::idesc_f16_f32acc(128, 64);
+        const uint32_t idS = tc::idesc_f16_f32acc(128, D) | tc::kIdescBmn;
+        const uint64_t dWT = tc::desc_mn_sw128(tc::smem_u32(sWT), 0);
+        bool failed = false, u_issued = false;
+        int prev_n = 0, prev_tok0 = 0, prev_s = 0;
+
+        // Initial state row j (half hf): fp32 into D_S, fp16 into S16; for an
+        // empty sequence straight to the destination slot.
+        if (jv) {
+            const float *sp = src >= 0 ? a.state + ((static_cast<size_t>(src) * a.h_v + h) * D + j) * D : nullptr;
+            float *dp = (Lseq == 0 && dst >= 0) ? a.state + ((static_cast<size_t>(dst) * a.h_v + h) * D + j) * D
                                                 : nullptr;
 #pragma unroll 1
-            for (int c0 = hf * kHalfD; c0 < (hf + 1) * kHalfD; c0 += 32) {
-                uint32_t r[32];
+            for (int c0 = hf * kHalf; c0 < (hf + 1) * kHalf; c0 += 32) {
+                uint32_t r[32], p16[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
                     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -487,203 +452,141 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                     r[i + 3] = __float_as_uint(v.w);
                     if (dp) __stcg(reinterpret_cast<float4 *>(dp + c0 + i), v);
                 }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) p16[i] = pack_half2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
                 if (Lseq > 0) {
-                    tc::tmem_st32(my_lane + kColD5 + c0, r);
-                    store_f16_chunks32(sS0T, jm, c0, r);
+                    tc::tmem_st32(tl + kColS + c0, r);
+                    tc::tmem_st16(tl + kColS16 + c0 / 2, p16);
                 }
             }
+        } else if (hf == 0 && Lseq > 0) {  // d = 64: rows 64..127 of the A operands stay zero
+            uint32_t z[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) z[i] = 0u;
+            tc::tmem_st32(tl + kColS16, z);
+            tc::tmem_st32(tl + kColU16, z);
+            tc::tmem_st32(tl + kColUd16, z);
         }
-        tc::fence_proxy_async_smem();
         tc::fence_before_sync();
         group_sync(kBarChain);
 
-        // Shared-memory descriptors; a K step adds its byte offset / 16.
-        const uint64_t dS0T = tc::desc_k_sw128(tc::smem_u32(sS0T));
-        const uint64_t dVpT = tc::desc_k_sw128(tc::smem_u32(sVpT));
-        const uint64_t dUT = tc::desc_k_sw128(tc::smem_u32(sUT));
-        constexpr uint32_t kIdN128 = tc::idesc_f16_f32acc(128, 128), kIdN64 = tc::idesc_f16_f32acc(128, 64);
-        constexpr uint32_t kIdNDbmn = tc::idesc_f16_f32acc_bmn(128, D);  // B (the K tile) MN-major
-        uint32_t mma_phase = 0;
-        bool failed = false;
-        int prev_n = 0, prev_tok0 = 0;
-        uint16_t *sOst = reinterpret_cast<uint16_t *>(sVpT);
-        uint16_t *sVst = reinterpret_cast<uint16_t *>(sUT);
+        // U'^T = V^T T''^T into D_U for chunk cc (v slot cc & 1 as MN-major A).
+        auto issue_u = [&](int cc) {
+            const uint64_t dV = tc::desc_mn_sw128(tc::smem_u32(sV(cc & 1)), kLboV);
+            const uint64_t dT = tc::desc_k_sw128(tc::smem_u32(sTpp));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                tc::mma_f16(tbase + kColU, dV + kk * (2048 >> 4), dT + kk * 2, idU | tc::kIdescAmn, kk > 0);
+            tc::mma_commit(bars + kBarTFree);
+        };
 
-        // Output of a finished chunk: o_t = scale (gamma_t (Q S0)_t + (P U)_t),
-        // tokens t = 32 hf .. 32 hf + 31 per thread, staged as bf16 [t][D] in
-        // the V'^T tile (free between S3 of that chunk and C2 of the next) and
-        // stored with 16-byte writes.
+        // Output of a finished chunk, o_t = (Q~ S + P~ U)_t, tokens 32 hf ..
+        // 32 hf + 31 of value column j, one bf16 per (token, j): a warp's 32
+        // lanes store 64 contiguous bytes per token.
         auto output = [&](int buf, int n_out, int tok_out) {
-            if (j < D) {
-                float qs[32], pu[32];
-                tmem_load_row<32>(my_lane + kColD1 + 128 * buf + 32 * hf, qs);
-                tmem_load_row<32>(my_lane + kColD6 + 32 * hf, pu);
-                const float *gam = sGamC(buf) + 32 * hf;
+            uint32_t r[32];
+            tc::tmem_ld32(tl + kColO + 64 * buf + 32 * hf, r);
+            uint16_t *op = a.o + static_cast<size_t>(tok_out + 32 * hf) * ldv + static_cast<size_t>(h) * D + j;
+            const int lim = n_out - 32 * hf;
 #pragma unroll
-                for (int i4 = 0; i4 < 32; i4 += 4) {
-                    const float4 g4 = *reinterpret_cast<const float4 *>(gam + i4);
-                    const float gg[4] = {g4.x, g4.y, g4.z, g4.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        sOst[(32 * hf + i4 + u) * D + jm] =
-                            float_to_bf16_bits(a.scale * fmaf(gg[u], qs[i4 + u], pu[i4 + u]));
-                }
-            }
-            tc::fence_before_sync();
-            group_sync(kBarChain);
-            for (int e = tid; e < n_out * (D / 8); e += kGroup) {
-                const int t = e / (D / 8), cc = e % (D / 8);
-                *reinterpret_cast<uint4 *>(a.o + static_cast<size_t>(tok_out + t) * ldv + static_cast<size_t>(h) * D +
-                                           cc * 8) = *reinterpret_cast<const uint4 *>(sOst + t * D + cc * 8);
-            }
-            // the staging tile is next written by C2, after the S1 barrier
+            for (int i = 0; i < 32; ++i)
+                if (i < lim) op[static_cast<size_t>(i) * ldv] = float_to_bf16_bits(__uint_as_float(r[i]));
         };
 
         for (int c = 0; c < n_chunks; ++c) {
-            const int s = c & 1, qs = c % 3;
+            const int s = c & 1;
             const int tok0 = t0 + c * kChunk;
             const int n = min(kChunk, Lseq - c * kChunk);
-            const uint32_t d1 = tbase + kColD1 + 128 * s;
-            const uint32_t d1_lane = my_lane + kColD1 + 128 * s;
+            uint8_t *qk = sQK(c % 3);
 
-            // ---- values of the chunk (independent of the prep group) ------------
-            constexpr int kPerV = 64 * (D / 8) / kGroup;
-            uint4 vv[kPerV];
-#pragma unroll
-            for (int it = 0; it < kPerV; ++it) {
-                const int e = tid + it * kGroup;
-                const int r = e / (D / 8), cc = e % (D / 8);
-                const size_t row = static_cast<size_t>(tok0 + min(r, n - 1));  // always a row of this chunk
-                vv[it] = __ldg(reinterpret_cast<const uint4 *>(a.v + row * ldv + static_cast<size_t>(h) * D + cc * 8));
-            }
-
-            // ---- wait for the chunk's operands ---------------------------------
-            // (a failed wait is agreed on at the S1 barrier below)
-            const bool ok_ready = __all_sync(0xffffffffu, mbar_wait_bounded(ready + s, (c >> 1) & 1));
+            // ---- P0: operands of chunk c; D_U += S16^T (-W)^T, D_O = S16^T Q~^T --
+            // (wait results that gate warp-collective TMEM accesses are made warp-uniform)
+            const bool okr = __all_sync(0xffffffffu, wait_bar(bars + kBarReady + s, (c >> 1) & 1, fail));
             tc::fence_after_sync();
-
-            // ---- S1: D1 = S0^T [Q;K]^T --------------------------------------------
-            if (tid == 0 && ok_ready) {
-                const uint64_t dQK = tc::desc_k_sw128(tc::smem_u32(sQK(qs)));
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = ((kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4;
-                    tc::mma_f16(d1, dS0T + off, dQK + off, kIdN128, kk > 0);
+            if (tid == 0 && okr) {
+                bool oku = u_issued;
+                if (!oku) {
+                    oku = wait_bar(bars + kBarUReady, c & 1, fail);
+                    if (oku) issue_u(c);
                 }
-                tc::mma_commit(mma_bar);
+                if (oku) {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        tc::mma_f16_ta(tbase + kColU, tbase + kColS16 + kk * 8, dWT + kk * (2048 >> 4),
+                                       idU | tc::kIdescBmn, 1);
+                    tc::mma_commit(bars + kBarA);
+                    tc::mma_commit(bars + kBarWFree);
+                    const uint64_t dQ = tc::desc_k_sw128(tc::smem_u32(qk));
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        tc::mma_f16_ta(tbase + kColO + 64 * s, tbase + kColS16 + kk * 8,
+                                       dQ + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), idU, kk > 0);
+                } else {
+                    atomicExch(fail, 1);
+                }
             }
             __syncwarp();
-            if (tid < 64 && ok_ready) sGamC(s)[tid & 63] = sGam(s)[tid & 63];  // kept for the output of this chunk
-            // values -> staging tile (the U^T tile is free until C4 of this chunk)
-#pragma unroll
-            for (int it = 0; it < kPerV; ++it) {
-                const int e = tid + it * kGroup;
-                const int r = e / (D / 8), cc = e % (D / 8);
-                *reinterpret_cast<uint4 *>(sVst + r * D + cc * 8) = r < n ? vv[it] : make_uint4(0, 0, 0, 0);
-            }
-
-            // ---- output of the previous chunk while S1 runs ---------------------
-            if (c > 0) output(s ^ 1, prev_n, prev_tok0);
-
-            // ---- C2: V'^T = V^T - (K S0)^T diag(gamma) --------------------------
-            const bool ok1 = mbar_wait_bounded(mma_bar, mma_phase);
-            mma_phase ^= 1u;
-            if (group_any(kBarChain, !ok1 || !ok_ready)) {
-                failed = true;
-                break;
-            }
-            tc::fence_after_sync();
-            if (j < D) {
-                float ks[32];
-                tmem_load_row<32>(d1_lane + 64 + 32 * hf, ks);
-                const float *gam = sGam(s) + 32 * hf;
-#pragma unroll
-                for (int i4 = 0; i4 < 32; i4 += 4) {
-                    const float4 g4 = *reinterpret_cast<const float4 *>(gam + i4);
-                    const float gg[4] = {g4.x, g4.y, g4.z, g4.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int i = i4 + u;
-                        ks[i] = __uint_as_float(static_cast<uint32_t>(sVst[(32 * hf + i) * D + jm]) << 16) - gg[u] * ks[i];
-                    }
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) store_chunk8_f16(sVpT, 128, jm, 4 * hf + q, ks + 8 * q);
-            }
-            tc::fence_proxy_async_smem();
-            tc::fence_before_sync();
-            group_sync(kBarChain);
-            if (tid == 0) {
-                tc::fence_after_sync();
-                const uint64_t dT = tc::desc_k_sw128(tc::smem_u32(sTpp(s)));
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) tc::mma_f16(d1 + 64, dVpT + kk * 2, dT + kk * 2, kIdN64, kk > 0);
-                tc::mma_commit(mma_bar);
-            }
-            __syncwarp();
-            if (j < D) {  // gamma_C scales the state while S3 runs
-                const float gC = sGam(s)[63];
+            if (c > 0 && jv) output(prev_s, prev_n, prev_tok0);
+            if (jv && okr) {  // gamma_C scales the fp32 state while the products run
+                const float gC = sGc[s];
 #pragma unroll 1
-                for (int c0 = hf * kHalfD; c0 < (hf + 1) * kHalfD; c0 += 32) {
+                for (int c0 = hf * kHalf; c0 < (hf + 1) * kHalf; c0 += 32) {
                     uint32_t r[32];
-                    tc::tmem_ld32(my_lane + kColD5 + c0, r);
+                    tc::tmem_ld32(tl + kColS + c0, r);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(gC * __uint_as_float(r[i]));
-                    tc::tmem_st32(my_lane + kColD5 + c0, r);
+                    tc::tmem_st32(tl + kColS + c0, r);
                 }
             }
-            tc::fence_before_sync();
-
-            // ---- C4: U^T and (diag(dec) U)^T to fp16; D5 += (diag(dec) U)^T K, D6 = U^T P^T
-            // (a failed wait is agreed on at the barrier that follows the phase;
-            // the V'^T tile is free once S3 has completed)
-            const bool ok2 = __all_sync(0xffffffffu, mbar_wait_bounded(mma_bar, mma_phase));
-            mma_phase ^= 1u;
+            const bool oka = __all_sync(0xffffffffu, okr && wait_bar(bars + kBarA, c & 1, fail));
             tc::fence_after_sync();
-            if (ok2 && j < D) {
-                float u[32];
-                tmem_load_row<32>(d1_lane + 64 + 32 * hf, u);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) store_chunk8_f16(sUT, 128, jm, 4 * hf + q, u + 8 * q);
+
+            // ---- P1: U^T and (diag(dec) U)^T to fp16 A operands --------------------
+            if (oka && jv) {
+                uint32_t r[32], pu[16], pd[16];
+                tc::tmem_ld32(tl + kColU + 32 * hf, r);
                 const float *dec = sDec(s) + 32 * hf;
 #pragma unroll
-                for (int i4 = 0; i4 < 32; i4 += 4) {
-                    const float4 d4 = *reinterpret_cast<const float4 *>(dec + i4);
-                    u[i4] *= d4.x;
-                    u[i4 + 1] *= d4.y;
-                    u[i4 + 2] *= d4.z;
-                    u[i4 + 3] *= d4.w;
+                for (int i = 0; i < 16; ++i) {
+                    const float u0 = __uint_as_float(r[2 * i]), u1 = __uint_as_float(r[2 * i + 1]);
+                    pu[i] = pack_half2(u0, u1);
+                    pd[i] = pack_half2(u0 * dec[2 * i], u1 * dec[2 * i + 1]);
                 }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) store_chunk8_f16(sVpT, 128, jm, 4 * hf + q, u + 8 * q);
+                tc::tmem_st16(tl + kColU16 + 16 * hf, pu);
+                tc::tmem_st16(tl + kColUd16 + 16 * hf, pd);
             }
-            tc::fence_proxy_async_smem();
             tc::fence_before_sync();
-            if (group_any(kBarChain, !ok2)) {
+            if (group_any(kBarChain, !oka || *vfail)) {
                 failed = true;
                 break;
             }
+
+            // ---- P2: D_S += (diag(dec) U)^T K, D_O += U^T P~^T; preset next U'^T --
             if (tid == 0) {
                 tc::fence_after_sync();
-                // K rows of the Q/K slot as B (N = key index i, K = token t), MN-major:
-                // 64-column boxes 16 KB apart, a 16-token K step is 2048 B.
-                const uint64_t dK = tc::desc_mn_sw128(tc::smem_u32(sQK(qs) + 8192), 16384);
+                const uint64_t dK = tc::desc_mn_sw128(tc::smem_u32(qk + 8192), kLboK);
                 const uint64_t dPs = tc::desc_k_sw128(tc::smem_u32(sP(s)));
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    tc::mma_f16(tbase + kColD5, dVpT + kk * 2, dK + kk * (2048 >> 4), kIdNDbmn, 1);
+                    tc::mma_f16_ta(tbase + kColS, tbase + kColUd16 + kk * 8, dK + kk * (2048 >> 4), idS, 1);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) tc::mma_f16(tbase + kColD6, dUT + kk * 2, dPs + kk * 2, kIdN64, kk > 0);
-                tc::mma_commit(mma_bar);
+                for (int kk = 0; kk < 4; ++kk)
+                    tc::mma_f16_ta(tbase + kColO + 64 * s, tbase + kColU16 + kk * 8, dPs + kk * 2, idU, 1);
+                tc::mma_commit(bars + kBarC);
+                tc::mma_commit(bars + kBarQKFree);
+                u_issued = false;
+                if (c + 1 < n_chunks && tc::mbar_test_wait(bars + kBarUReady, (c + 1) & 1)) {
+                    tc::fence_after_sync();
+                    issue_u(c + 1);
+                    u_issued = true;
+                }
             }
             __syncwarp();
-
-            // ---- C6: new state -> S0^T tile, emission, final state -----------------
-            const bool ok3 = __all_sync(0xffffffffu, mbar_wait_bounded(mma_bar, mma_phase));
-            mma_phase ^= 1u;
+            const bool okc = __all_sync(0xffffffffu, wait_bar(bars + kBarC, c & 1, fail));
             tc::fence_after_sync();
-            if (ok3) mbar_arrive(freeb + s);  // every MMA and read of this chunk's stage and Q/K slot is done
-            if (ok3 && j < D) {
+
+            // ---- P3: new state -> S16, emission, final state -------------------------
+            if (okc && jv) {
                 float *ep = nullptr;
                 if (E > 0 && n == kChunk && ((c + 1) % E) == 0) {
                     if (a.emit_table) {  // emission k of this sequence -> its cache block's slot
@@ -692,23 +595,26 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                                              ? a.emit_table[static_cast<int64_t>(seq) * a.emit_table_stride + col]
                                              : static_cast<int>(a.num_slots);
                         if (slot >= 0 && slot < a.num_slots)
-                            ep = a.state + ((static_cast<size_t>(slot) * a.h_v + h) * D + jm) * D;
+                            ep = a.state + ((static_cast<size_t>(slot) * a.h_v + h) * D + j) * D;
                         else if (slot >= 0 && tid == 0)
                             report(a.dev_status, GDN_DEV_BAD_SLOT);
                     } else if (a.chunk_states) {
                         const int64_t idx = eoff + (c + 1) / E - 1;
                         if (idx >= 0 && idx < a.chunk_capacity)
-                            ep = a.chunk_states + ((static_cast<size_t>(idx) * a.h_v + h) * D + jm) * D;
+                            ep = a.chunk_states + ((static_cast<size_t>(idx) * a.h_v + h) * D + j) * D;
                     }
                 }
                 float *dp = (c == n_chunks - 1 && dst >= 0)
-                                ? a.state + ((static_cast<size_t>(dst) * a.h_v + h) * D + jm) * D
+                                ? a.state + ((static_cast<size_t>(dst) * a.h_v + h) * D + j) * D
                                 : nullptr;
 #pragma unroll 1
-                for (int c0 = hf * kHalfD; c0 < (hf + 1) * kHalfD; c0 += 32) {
-                    uint32_t r[32];
-                    tc::tmem_ld32(my_lane + kColD5 + c0, r);
-                    store_f16_chunks32(sS0T, jm, c0, r);
+                for (int c0 = hf * kHalf; c0 < (hf + 1) * kHalf; c0 += 32) {
+                    uint32_t r[32], p16[16];
+                    tc::tmem_ld32(tl + kColS + c0, r);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        p16[i] = pack_half2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                    tc::tmem_st16(tl + kColS16 + c0 / 2, p16);
 #pragma unroll
                     for (int i = 0; i < 32; i += 4) {
                         const float4 v = make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
@@ -718,139 +624,112 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                     }
                 }
             }
-            tc::fence_proxy_async_smem();
             tc::fence_before_sync();
-            if (group_any(kBarChain, !ok3)) {
+            if (group_any(kBarChain, !okc || *vfail)) {
                 failed = true;
                 break;
             }
             prev_n = n;
             prev_tok0 = tok0;
+            prev_s = s;
         }
-        if (!failed && n_chunks > 0) output((n_chunks - 1) & 1, prev_n, prev_tok0);
-        if (failed) {
-            if (tid == 0) {
-                report(a.dev_status, GDN_DEV_TIMEOUT);
-                atomicExch(fail, 1);
-            }
-            // MMAs already issued get a bounded time to finish before the TMEM
-            // they write is released.
-            mbar_wait_bounded(mma_bar, mma_phase);
+        if (!failed && n_chunks > 0 && jv) output(prev_s, prev_n, prev_tok0);
+        if (failed && tid == 0) {
+            report(a.dev_status, GDN_DEV_TIMEOUT);
+            atomicExch(fail, 1);
+        }
+        if (tid == 0) {  // every MMA this thread issued has finished before TMEM is released
+            tc::mma_commit(bars + kBarDrainC);
+            drain_bar(bars + kBarDrainC, 0);
         }
     } else {
         // ============================= prep group ==============================
-        // Thread (p, hf): TMEM lane / Gram row p, half hf of the row's work.
+        // Thread (p, hf): TMEM lane / product row p, half hf of the row's columns.
         const int pid = tid - kGroup;  // 0..255
         const int p = pid & 127, hf = pid >> 7;
         bool failed = false;
-        const uint32_t aIdGram = tc::idesc_f16_f32acc(128, 64);
-        // q, k of a chunk go straight into its Q/K slot by TMA (bf16, 128-byte
-        // swizzle: the layout the MMA descriptors expect), issued at the start
-        // of the previous chunk's preparation; g, beta into registers at the
-        // same time.  The bf16 -> fp16 conversion runs in place, during the
-        // previous chunk's diagonal solve, by the warps that solve nothing.
-        constexpr uint32_t kTmaBytes = 2u * (D / 64) * 64 * 128;
+        int c_done = 0;                          // chunks whose loads the loop consumed
+        int qk_issued = -1, v_issued = -1;       // highest chunk whose copies were issued (pid 0)
+        constexpr uint32_t kQKTx = 2u * kKB * 8192u, kVTx = kKB * 8192u;
         float gv = 0.f, bv = 0.f;
         auto load_gb = [&](int cc) {
-            const int tk = t0 + cc * kChunk;
             const int nn = min(kChunk, Lseq - cc * kChunk);
             if (pid < 64) {
-                const size_t gi = static_cast<size_t>(tk + min(pid & 63, nn - 1)) * a.h_v + h;
+                const size_t gi = static_cast<size_t>(t0 + cc * kChunk + min(pid & 63, nn - 1)) * a.h_v + h;
                 gv = a.g[gi];
                 bv = a.beta[gi];
             }
         };
-        auto issue_tma = [&](int cc) {
-            const int tk = t0 + cc * kChunk;
-            if (pid == 0) {
-                const int slot = cc % 3;
-                uint8_t *tile = sQK(slot);
-                uint64_t *tb = tma_bar + slot;
-                mbar_expect_tx(tb, kTmaBytes);
+        auto issue_qk = [&](int cc) {  // q and k of chunk cc into slot cc % 3
+            uint8_t *tile = sQK(cc % 3);
+            uint64_t *tb = bars + kBarTmaQK + cc % 3;
+            mbar_expect_tx(tb, kQKTx);
 #pragma unroll
-                for (int kb = 0; kb < D / 64; ++kb) {
-                    tma_load_2d(tile + kb * 16384, &L.tm_q, kh * D + kb * 64, tk, tb);
-                    tma_load_2d(tile + kb * 16384 + 8192, &L.tm_k, kh * D + kb * 64, tk, tb);
-                }
+            for (int kb = 0; kb < kKB; ++kb) {
+                tma_load_2d(tile + kb * 16384, &L.tm_q, kh * D + kb * 64, t0 + cc * kChunk, tb);
+                tma_load_2d(tile + kb * 16384 + 8192, &L.tm_k, kh * D + kb * 64, t0 + cc * kChunk, tb);
             }
+            qk_issued = cc;
         };
-        // Waits for chunk cc's copies and converts its slot to fp16 in place
-        // (16-byte items first_e, first_e + step, ...); rows past the sequence
-        // end (the next sequence's tokens) become zeros.
-        auto convert = [&](int cc, int first_e, int step) -> bool {
-            const int slot = cc % 3;
-            const int nn = min(kChunk, Lseq - cc * kChunk);
-            uint8_t *tile = sQK(slot);
-            if (!mbar_wait_bounded(tma_bar + slot, (cc / 3) & 1)) return false;
-            for (int e = first_e; e < 64 * (D / 8); e += step) {
-                const int r = e / (D / 8), c8 = e % (D / 8);
-                uint4 *pq = reinterpret_cast<uint4 *>(tile + tc::sw128_chunk_offset(r, c8, 128));
-                uint4 *pk = reinterpret_cast<uint4 *>(tile + tc::sw128_chunk_offset(64 + r, c8, 128));
-                const uint4 z = make_uint4(0, 0, 0, 0);
-                const uint4 xq = *pq, xk = *pk;
-                *pq = r < nn ? bf16x8_to_f16x8(xq) : z;
-                *pk = r < nn ? bf16x8_to_f16x8(xk) : z;
-            }
-            tc::fence_proxy_async_smem();  // the converted tile is read by the tensor cores
-            return true;
+        auto issue_v = [&](int cc) {  // v of chunk cc into slot cc & 1
+            uint8_t *tile = sV(cc & 1);
+            uint64_t *tb = bars + kBarTmaV + (cc & 1);
+            mbar_expect_tx(tb, kVTx);
+#pragma unroll
+            for (int kb = 0; kb < kKB; ++kb) tma_load_2d(tile + kb * 8192, &L.tm_v, h * D + kb * 64, t0 + cc * kChunk, tb);
+            v_issued = cc;
         };
         if (n_chunks > 0) {
-            issue_tma(0);
-            if (n_chunks > 1) issue_tma(1);
-            load_gb(0);
-            if (!convert(0, pid, kGroup)) failed = true;
-        }
-        if (group_any(kBarPrep, failed)) failed = true;
-        for (int c = 0; c < n_chunks && !failed; ++c) {
-            const int s = c & 1, qs = c % 3;
-            const int tok0 = t0 + c * kChunk;
-            const int n = min(kChunk, Lseq - c * kChunk);
-            // ---- next chunk's copies (each chunk's tile is converted one chunk ahead)
-            uint8_t *qk = sQK(qs);
-            bool okt;
-            {
-                if (pid < 64) {  // g, beta of this chunk, loaded one chunk ahead
-                    const int t = pid & 63;
-                    sGraw[t] = t < n ? gv : 0.f;
-                    sBeta[t] = t < n ? bv : 0.f;
+            if (pid == 0) {
+                issue_qk(0);
+                issue_v(0);
+                if (n_chunks > 1) {
+                    issue_qk(1);
+                    issue_v(1);
                 }
-                // The next chunk's Q/K slot and this chunk's stage were both last
-                // used by chunk c - 2: one wait, by the issuing thread, covers
-                // both (the group barrier below orders every write of the stage
-                // after it).  Chunk 1's copies were issued with chunk 0's.
-                bool okf = true;
-                if (pid == 0 && c >= 2) okf = mbar_wait_bounded(freeb + s, ((c - 2) >> 1) & 1);
-                if (c >= 1 && c + 1 < n_chunks && okf) issue_tma(c + 1);
-                if (c + 1 < n_chunks) load_gb(c + 1);
-                if (c + 2 < n_chunks && pid < 128) {  // q, k rows of chunk c + 2 into L2
-                    const int rn = min(kChunk, Lseq - (c + 2) * kChunk);
-                    const int r = pid & 63;
-                    if (r < rn) {
-                        const size_t row = static_cast<size_t>(tok0 + 2 * kChunk + r);
-                        const uint16_t *src_row = (pid < 64 ? a.q : a.k) + row * ldq + kh * D;
-                        asm volatile("prefetch.global.L2 [%0];" ::"l"(src_row) : "memory");
-                        if (D > 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(src_row + 64) : "memory");
-                    }
-                }
-                okt = okf;
             }
-            tc::fence_before_sync();
-            if (group_any(kBarPrep, !okt)) {  // chunk c - 2 never finished: stop (bounded)
+            load_gb(0);
+        }
+
+        for (int c = 0; c < n_chunks; ++c) {
+            const int s = c & 1;
+            const int n = min(kChunk, Lseq - c * kChunk);
+            uint8_t *qk = sQK(c % 3);
+            uint8_t *vt = sV(c & 1);
+
+            // ---- Q1: v copies of chunk c + 1, this chunk's g and beta ----------------
+            bool ok = true;
+            if (pid == 0 && c >= 1) {
+                ok = wait_bar(bars + kBarTFree, (c - 1) & 1, fail);  // T'' and v slot of chunk c - 1 free
+                if (ok && c + 1 < n_chunks) issue_v(c + 1);
+            }
+            if (pid < 64) {
+                const int t = pid & 63;
+                sGraw[t] = t < n ? gv : 0.f;
+                sBeta[t] = t < n ? bv : 0.f;
+            }
+            if (c + 1 < n_chunks) load_gb(c + 1);
+            if (group_any(kBarPrep, !ok || *vfail)) {
                 failed = true;
                 break;
             }
-            // ---- Gram [Q;K] K^T (issued by warp 9 while warp 8 runs the prefix sum) --
-            if (pid == 32) {
-                tc::fence_after_sync();
-                const uint64_t dQK = tc::desc_k_sw128(tc::smem_u32(qk));
+
+            // ---- Q2: Gram [Q;K] K^T in bf16 from the TMA tile || prefix sum ----------
+            if (pid == 0) {
+                ok = wait_bar(bars + kBarTmaQK + c % 3, (c / 3) & 1, fail);
+                if (ok) {
+                    tc::fence_after_sync();
+                    const uint64_t dQK = tc::desc_k_sw128(tc::smem_u32(qk));
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = ((kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4;
-                    tc::mma_f16(tbase + kColGram, dQK + off, dQK + off + (64 * 128 >> 4), aIdGram, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                        tc::mma_f16(tbase + kColPrep, dQK + off, dQK + off + (8192 >> 4),
+                                    tc::idesc_f16_f32acc(128, 64) | tc::kIdescBf16, kk > 0);
+                    }
+                    tc::mma_commit(bars + kBarGram);
                 }
-                tc::mma_commit(gram_bar);
             }
-            if (pid < 32) {  // inclusive prefix sum of g over the chunk, fixed order
+            if (warp == 10) {  // inclusive prefix sum of g over the chunk, fixed order
                 const int l = pid & 31;
                 const float g0 = sGraw[2 * l], g1 = sGraw[2 * l + 1];
                 const float pair = g0 + g1;
@@ -863,25 +742,29 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                 const float excl = incl - pair;
                 const float G0 = excl + g0, G1 = excl + g0 + g1;
                 const float Gc = __shfl_sync(0xffffffffu, G1, 31);  // G_63, the chunk total
+                const float e0 = expf(G0), e1 = expf(G1);
                 sG[2 * l] = G0;
                 sG[2 * l + 1] = G1;
-                sGam(s)[2 * l] = expf(G0);
-                sGam(s)[2 * l + 1] = expf(G1);
+                sGam[2 * l] = e0;
+                sGam[2 * l + 1] = e1;
+                sBG[2 * l] = sBeta[2 * l] * e0;
+                sBG[2 * l + 1] = sBeta[2 * l + 1] * e1;
                 sDec(s)[2 * l] = expf(Gc - G0);
                 sDec(s)[2 * l + 1] = expf(Gc - G1);
+                if (l == 31) sGc[s] = e1;
             }
-            group_sync(kBarPrep);  // g cumsum, gamma, dec visible
-            __syncwarp();
-            // Each warp reads the Gram only once every lane saw it complete; a
-            // failure is agreed on at the barrier after P and A.
-            const bool okg = __all_sync(0xffffffffu, mbar_wait_bounded(gram_bar, c & 1));
-            tc::fence_after_sync();
+            if (group_any(kBarPrep, !ok || *vfail)) {
+                failed = true;
+                break;
+            }
 
-            // ---- P rows (lanes 0..63) and A rows (lanes 64..127), columns 32 hf.. ----
-            // Rows 0..31 x columns 32..63 are masked (warp-uniform): P gets zeros,
+            // ---- Q3: P~ rows (lanes 0..63) and A rows (lanes 64..127), columns 32 hf.. --
+            // Rows 0..31 x columns 32..63 are masked (warp-uniform): P~ gets zeros,
             // the upper triangle of A is never read.
+            const bool okg = __all_sync(0xffffffffu, wait_bar(bars + kBarGram, c & 1, fail));
+            tc::fence_after_sync();
             if (!okg) {
-                // nothing: the barrier below ends the loop
+                // the barrier below ends the loop
             } else if (hf == 1 && (p & 32) == 0) {
                 if (p < 64) {
                     const uint4 z = make_uint4(0, 0, 0, 0);
@@ -890,70 +773,230 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
                         *reinterpret_cast<uint4 *>(sP(s) + tc::sw128_chunk_offset(p & 63, q, 64)) = z;
                 }
             } else {
-                float x[32];
-                tmem_load_row<32>(my_lane + kColGram + 32 * hf, x);
+                uint32_t x[32];
+                tc::tmem_ld32(tl + kColPrep + 32 * hf, x);
                 const int r = p & 63;
                 const float Gr = sG[r];
+                const float f = p < 64 ? a.scale : sBeta[r];
+                const int diag = p < 64 ? 0 : 1;  // P~ keeps s == t, A does not
 #pragma unroll
                 for (int q4 = 0; q4 < 32; q4 += 4) {
                     const int q0 = 32 * hf + q4;
                     const float4 g4 = *reinterpret_cast<const float4 *>(sG + q0);
-                    x[q4 + 0] = (q0 + 0 <= r) ? __expf(Gr - g4.x) * x[q4 + 0] : 0.f;
-                    x[q4 + 1] = (q0 + 1 <= r) ? __expf(Gr - g4.y) * x[q4 + 1] : 0.f;
-                    x[q4 + 2] = (q0 + 2 <= r) ? __expf(Gr - g4.z) * x[q4 + 2] : 0.f;
-                    x[q4 + 3] = (q0 + 3 <= r) ? __expf(Gr - g4.w) * x[q4 + 3] : 0.f;
+                    const float gg[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        x[q4 + u] = __float_as_uint((q0 + u + diag <= r) ? f * __expf(Gr - gg[u]) * __uint_as_float(x[q4 + u])
+                                                                         : 0.f);
                 }
                 if (p < 64) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) store_chunk8_f16(sP(s), 64, r, 4 * hf + q, x + 8 * q);
-                } else {
-                    const float br = sBeta[r];
-#pragma unroll
-                    for (int q = 0; q < 32; q += 4) {
-                        const int q0 = 32 * hf + q;
-                        *reinterpret_cast<float4 *>(sM + r * kLdM + q0) =
-                            make_float4(q0 + 0 < r ? br * x[q + 0] : 0.f, q0 + 1 < r ? br * x[q + 1] : 0.f,
-                                        q0 + 2 < r ? br * x[q + 2] : 0.f, q0 + 3 < r ? br * x[q + 3] : 0.f);
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 v;
+                        v.x = pack_half2(__uint_as_float(x[8 * q + 0]), __uint_as_float(x[8 * q + 1]));
+                        v.y = pack_half2(__uint_as_float(x[8 * q + 2]), __uint_as_float(x[8 * q + 3]));
+                        v.z = pack_half2(__uint_as_float(x[8 * q + 4]), __uint_as_float(x[8 * q + 5]));
+                        v.w = pack_half2(__uint_as_float(x[8 * q + 6]), __uint_as_float(x[8 * q + 7]));
+                        *reinterpret_cast<uint4 *>(sP(s) + tc::sw128_chunk_offset(r, 4 * hf + q, 64)) = v;
                     }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 32; q += 4)
+                        *reinterpret_cast<float4 *>(sM + r * kLdM + 32 * hf + q) =
+                            make_float4(__uint_as_float(x[q]), __uint_as_float(x[q + 1]), __uint_as_float(x[q + 2]),
+                                        __uint_as_float(x[q + 3]));
+                    if (r >= 32 && hf == 0) store_row32_f16(sL2A1, r - 32, x, 1.f, true);  // A_B, fp16
                 }
             }
+            tc::fence_proxy_async_smem();
             tc::fence_before_sync();
-            if (group_any(kBarPrep, !okg)) {
+            if (group_any(kBarPrep, !okg || *vfail)) {
                 failed = true;
-                mbar_wait_bounded(gram_bar, c & 1);  // let an issued Gram finish before TMEM is freed
                 break;
             }
 
-            // ---- T = (I + A)^-1: diagonal blocks, then level 1 || next chunk's Q/K to fp16
-            // A diagonal block is solved and stored by the 16 lanes of one half
-            // warp (warps 8 and 9): a warp barrier orders its reads before the
-            // store, and the same warp then builds level 1 of the off-diagonal
-            // part; the group barrier below orders both before level 2.
-            bool okn = true;
+            // ---- Q4: diagonal blocks and level 1 (warps 8, 9) || q~, k, v to fp16 -----
+            bool okv = true;
             if (pid < 64) {
                 float xd[16];
                 invert_diag_solve(sM, pid, xd);
                 __syncwarp();
-                invert_diag_store(sM, pid, xd, sTpp(s), sBeta);
-                __syncwarp();  // warp 8 holds blocks 0, 1 and warp 9 blocks 2, 3: level 1 per warp
-                if (pid < 32) level1_warp<1>(sM, sW, pid & 31, sTpp(s), sBeta);
-                else level1_warp<3>(sM, sW, pid & 31, sTpp(s), sBeta);
-            } else if (c + 1 < n_chunks) {
-                okn = convert(c + 1, pid - 64, kGroup - 64);
+                invert_diag_store(sM, pid, xd);
+                __syncwarp();
+                if (pid < 32) level1_warp<1>(sM, sWb, pid & 31);
+                else level1_warp<3>(sM, sWb, pid & 31);
+                __syncwarp();
+                // Level-2 operands: T_top (rows 0..31, cols 0..31) as MN-major B
+                // (warp 8), T_bot (rows 32..63, cols 32..63) as K-major A (warp 9);
+                // the blocks above the diagonal blocks are zero.
+                const int r = pid & 31;
+                const int rb = pid < 32 ? 0 : 32;
+                uint32_t x[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    x[i] = (i >= 16 && r < 16) ? 0u : __float_as_uint(sM[(rb + r) * kLdM + rb + i]);
+                store_row32_f16(pid < 32 ? sL2B1 : sL2A2, r, x, 1.f, pid >= 32);
+            } else {
+                okv = wait_bar(bars + kBarTmaV + (c & 1), (c / 2) & 1, fail) &&
+                      wait_bar(bars + kBarTmaQK + c % 3, (c / 3) & 1, fail);
+                if (okv) {
+                    // 16-byte items of the q, k, v boxes: rows past the sequence end
+                    // become zeros; q is scaled by scale gamma_t (Q~).
+                    constexpr int kPerBox = 64 * 8;
+                    constexpr int kItems = 3 * kKB * kPerBox;
+                    for (int e = pid - 64; e < kItems; e += kGroup - 64) {
+                        const int which = e / (kKB * kPerBox), rem = e % (kKB * kPerBox);
+                        const int kb = rem / kPerBox, w = rem % kPerBox, r = w >> 3;
+                        uint8_t *base = which == 2 ? vt + kb * 8192 : qk + kb * 16384 + (which == 1 ? 8192 : 0);
+                        uint4 *ptr = reinterpret_cast<uint4 *>(base + w * 16);
+                        const float f = which == 0 ? a.scale * sGam[r] : 1.f;
+                        const uint4 x = *ptr;
+                        *ptr = r < n ? bf16x8_to_f16x8(x, f) : make_uint4(0, 0, 0, 0);
+                    }
+                }
             }
-            if (group_any(kBarPrep, !okn)) {  // diagonal blocks and level 1 visible to level 2
+            tc::fence_proxy_async_smem();
+            tc::fence_before_sync();
+            if (group_any(kBarPrep, !okv || *vfail)) {
                 failed = true;
                 break;
             }
-            // T'' = T diag(beta) is written as fp16 by the inverse itself.
-            invert_offdiag(sM, sW, pid, sTpp(s), sBeta);
+            c_done = c;  // this chunk's copies have all been waited for
+
+            // ---- Q5: level 2 on the tensor cores (warp 8) || T'', -T''' of the rest ---
+            bool okl = true;
+            if (pid < 32) {
+                // X = A_B T_top, then T_B = T_bot (-X): lanes 0..31 of the prep columns.
+                if (pid == 0) {
+                    tc::fence_after_sync();
+                    const uint64_t dA = tc::desc_k_sw128(tc::smem_u32(sL2A1));
+                    const uint64_t dB = tc::desc_mn_sw128(tc::smem_u32(sL2B1), 0);
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk)
+                        tc::mma_f16(tbase + kColPrep, dA + kk * 2, dB + kk * (2048 >> 4),
+                                    tc::idesc_f16_f32acc(128, 32) | tc::kIdescBmn, kk > 0);
+                    tc::mma_commit(bars + kBarL2);
+                }
+                __syncwarp();
+                okl = __all_sync(0xffffffffu, wait_bar(bars + kBarL2, 0, fail));
+                tc::fence_after_sync();
+                uint32_t x[32];
+                if (okl) {
+                    tc::tmem_ld32(tl + kColPrep, x);
+                    store_row32_f16(sL2B2, pid, x, -1.f, false);
+                }
+                tc::fence_proxy_async_smem();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (pid == 0 && okl) {
+                    tc::fence_after_sync();
+                    const uint64_t dA = tc::desc_k_sw128(tc::smem_u32(sL2A2));
+                    const uint64_t dB = tc::desc_mn_sw128(tc::smem_u32(sL2B2), 0);
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk)
+                        tc::mma_f16(tbase + kColPrep + 32, dA + kk * 2, dB + kk * (2048 >> 4),
+                                    tc::idesc_f16_f32acc(128, 32) | tc::kIdescBmn, kk > 0);
+                    tc::mma_commit(bars + kBarL2);
+                }
+                __syncwarp();
+                okl = okl && __all_sync(0xffffffffu, wait_bar(bars + kBarL2, 1, fail));
+                tc::fence_after_sync();
+                if (okl) {  // T_B: row 32 + pid, columns 0..31
+                    tc::tmem_ld32(tl + kColPrep + 32, x);
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        float v[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(x[16 * q + i]);
+                        store_t_segment(sTpp, sTppp, 32 + pid, q, v, sBeta, sBG);
+                    }
+                }
+            } else if (pid >= 64) {
+                // 16-column row segments of T (all but rows 32..63 x cols 0..31).
+                const int g = pid - 64;
+                const int t = g < 128 ? (g >> 2) : 32 + ((g - 128) >> 1);
+                const int q = g < 128 ? (g & 3) : 2 + ((g - 128) & 1);
+                float v[16];
+                if (q > (t >> 4)) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; i += 4) {
+                        const float4 m4 = *reinterpret_cast<const float4 *>(sM + t * kLdM + 16 * q + i);
+                        v[i] = m4.x;
+                        v[i + 1] = m4.y;
+                        v[i + 2] = m4.z;
+                        v[i + 3] = m4.w;
+                    }
+                }
+                store_t_segment(sTpp, sTppp, t, q, v, sBeta, sBG);
+            }
             tc::fence_proxy_async_smem();
-            mbar_arrive(ready + s);
-            group_sync(kBarPrep);  // scratch reuse by the next chunk
+            tc::fence_before_sync();
+            if (group_any(kBarPrep, !okl || *vfail)) {
+                failed = true;
+                break;
+            }
+            if (pid == 0) mbar_arrive(bars + kBarUReady);  // T'' and v of chunk c ready
+
+            // ---- Q6: -W^T = K^T (-T''')^T -> fp16 tile --------------------------------
+            if (pid == 0) {
+                ok = (c == 0) || wait_bar(bars + kBarWFree, (c - 1) & 1, fail);
+                if (ok) {
+                    tc::fence_after_sync();
+                    const uint64_t dK = tc::desc_mn_sw128(tc::smem_u32(qk + 8192), kLboK);
+                    const uint64_t dT = tc::desc_k_sw128(tc::smem_u32(sTppp));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_f16(tbase + kColPrep, dK + kk * (2048 >> 4), dT + kk * 2,
+                                    tc::idesc_f16_f32acc(128, 64) | tc::kIdescAmn, kk > 0);
+                    tc::mma_commit(bars + kBarW);
+                } else {
+                    atomicExch(fail, 1);
+                }
+            }
+            __syncwarp();
+            const bool okw = __all_sync(0xffffffffu, wait_bar(bars + kBarW, c & 1, fail));
+            tc::fence_after_sync();
+            if (okw && p < D) {  // row i = p of the MN-major -W^T tile, tokens 32 hf ..
+                uint32_t x[32];
+                tc::tmem_ld32(tl + kColPrep + 32 * hf, x);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 v;
+                    v.x = pack_half2(__uint_as_float(x[8 * q + 0]), __uint_as_float(x[8 * q + 1]));
+                    v.y = pack_half2(__uint_as_float(x[8 * q + 2]), __uint_as_float(x[8 * q + 3]));
+                    v.z = pack_half2(__uint_as_float(x[8 * q + 4]), __uint_as_float(x[8 * q + 5]));
+                    v.w = pack_half2(__uint_as_float(x[8 * q + 6]), __uint_as_float(x[8 * q + 7]));
+                    *reinterpret_cast<uint4 *>(sWT + mn_chunk_offset(p, 4 * hf + q)) = v;
+                }
+            }
+            tc::fence_proxy_async_smem();
+            tc::fence_before_sync();
+            if (group_any(kBarPrep, !okw || *vfail)) {
+                failed = true;
+                break;
+            }
+            // ---- hand over: q/k copies of chunk c + 2 into the slot of chunk c - 1 ----
+            if (pid == 0) {
+                bool okq = true;
+                if (c >= 1) okq = wait_bar(bars + kBarQKFree, (c - 1) & 1, fail);
+                if (okq && c + 2 < n_chunks) issue_qk(c + 2);
+                if (okq) mbar_arrive(bars + kBarReady + s);
+                else atomicExch(fail, 1);
+            }
+            c_done = c + 1;
         }
         if (failed && pid == 0) {
             report(a.dev_status, GDN_DEV_TIMEOUT);
             atomicExch(fail, 1);
+        }
+        if (pid == 0) {  // drain: this thread's MMAs, then every copy it issued that the loop did not consume
+            tc::mma_commit(bars + kBarDrainP);
+            drain_bar(bars + kBarDrainP, 0);
+            for (int cc = c_done; cc <= qk_issued; ++cc) drain_bar(bars + kBarTmaQK + cc % 3, (cc / 3) & 1);
+            for (int cc = c_done; cc <= v_issued; ++cc) drain_bar(bars + kBarTmaV + (cc & 1), (cc / 2) & 1);
         }
     }
 
@@ -963,13 +1006,21 @@ prefill_chunk_tc_kernel(const __grid_constant__ PrefillLaunch L) {
     if (warp == 0) tc::tmem_dealloc(tbase, kTmemCols);
 }
 
+// Dynamic shared memory is opted into once per device and head dim.
 template <int D>
 cudaError_t launch_d(const PrefillLaunch &L, cudaStream_t stream) {
+    static int set[kMaxDevices] = {};
     const uint32_t smem = Smem<D>::kAlloc;
-    cudaError_t e = cudaFuncSetAttribute(prefill_chunk_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    prefill_chunk_tc_kernel<D><<<L.a.num_seqs * L.a.h_v, kThreads, smem, stream>>>(L);
+    if (dev < 0 || dev >= kMaxDevices || !__atomic_load_n(&set[dev], __ATOMIC_ACQUIRE)) {
+        e = cudaFuncSetAttribute(prefill_chain_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDevices) __atomic_store_n(&set[dev], 1, __ATOMIC_RELEASE);
+    }
+    prefill_chain_kernel<D><<<L.a.num_seqs * L.a.h_v, kThreads, smem, stream>>>(L);
     return cudaGetLastError();
 }
 
@@ -1006,25 +1057,21 @@ bool encode_rows(CUtensorMap *m, const uint16_t *base, uint64_t rows, uint64_t c
 cudaError_t launch_prefill(const PrefillArgs &a, int d, const int32_t *cu_host, cudaStream_t stream) {
     if (a.num_seqs == 0) return cudaSuccess;
     static_assert(sizeof(PrefillLaunch) < 32000, "kernel parameter size");
-    // Longest sequences first, so the longest chains start in the first wave.
     PrefillLaunch L;
     L.a = a;
-    const uint64_t cols = static_cast<uint64_t>(a.h_k) * d;
-    if (a.total_tokens > 0 && (!encode_rows(&L.tm_q, a.q, a.total_tokens, cols) ||
-                               !encode_rows(&L.tm_k, a.k, a.total_tokens, cols)))
+    if (a.total_tokens > 0 &&
+        (!encode_rows(&L.tm_q, a.q, a.total_tokens, static_cast<uint64_t>(a.h_k) * d) ||
+         !encode_rows(&L.tm_k, a.k, a.total_tokens, static_cast<uint64_t>(a.h_k) * d) ||
+         !encode_rows(&L.tm_v, a.v, a.total_tokens, static_cast<uint64_t>(a.h_v) * d)))
         return cudaErrorNotSupported;
+    // Longest sequences first, so the longest chains start in the first wave
+    // (stable: equal lengths keep their order); beyond kMaxOrder sequences the
+    // rest keep their order.
     L.n_order = a.num_seqs < kMaxOrder ? a.num_seqs : kMaxOrder;
     for (int i = 0; i < L.n_order; ++i) L.order[i] = i;
-    for (int i = 1; i < L.n_order; ++i) {  // insertion sort by length, descending, stable
-        const int v = L.order[i];
-        const int lv = cu_host[v + 1] - cu_host[v];
-        int k = i - 1;
-        while (k >= 0 && (cu_host[L.order[k] + 1] - cu_host[L.order[k]]) < lv) {
-            L.order[k + 1] = L.order[k];
-            --k;
-        }
-        L.order[k + 1] = v;
-    }
+    std::stable_sort(L.order, L.order + L.n_order, [cu_host](int x, int y) {
+        return cu_host[x + 1] - cu_host[x] > cu_host[y + 1] - cu_host[y];
+    });
     return d == 128 ? launch_d<128>(L, stream) : launch_d<64>(L, stream);
 }
 

@@ -53,10 +53,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
 template <int D>
 cudaError_t launch_prep_d(const PrepArgs &a, cudaStream_t stream) {
     int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
+    if (!current_device(&dev, &sms)) return cudaErrorInvalidDevice;
     const int64_t rows = 2 * a.num_tokens * a.h_k;
     const int64_t need_rows = (rows + (kPrepThreads / 8) - 1) / (kPrepThreads / 8);
     const int64_t need_gate = (a.num_tokens * a.h_v + kPrepThreads - 1) / kPrepThreads;

@@ -1,6 +1,7 @@
 // Thin inline-PTX wrappers for the sm_100-family tensor-core path used by the
-// chunked prefill: mbarriers, TMEM allocation, tcgen05.mma (kind::f16),
-// tcgen05.commit, tcgen05.ld / tcgen05.st and the shared-memory matrix
+// chunked prefill: mbarriers, TMEM allocation, tcgen05.mma (kind::f16, A from
+// shared memory or from TMEM), tcgen05.commit, tcgen05.ld / tcgen05.st and the
+// shared-memory matrix
 // descriptors of the canonical K-major and MN-major 128-byte-swizzled
 // layouts.  Written from the PTX ISA description of these instructions.
 #pragma once
@@ -25,6 +26,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Non-blocking probe: true if the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
@@ -81,6 +95,19 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
         : "memory");
 }
 
+// The same with the A operand in TMEM: row m of A is TMEM lane m, its K
+// elements packed two per 32-bit column (the lower K index in the low half);
+// a K step of 16 elements advances a_tmem by 8 columns.
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on bar when every MMA issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -102,6 +129,11 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32acc(int M, int N) {
 __host__ __device__ constexpr uint32_t idesc_f16_f32acc_bmn(int M, int N) {
     return idesc_f16_f32acc(M, N) | (1u << 16);
 }
+// Modifier bits of the kind::f16 instruction descriptor: A given MN-major
+// ("transpose A"), and both operands bf16 instead of fp16.
+constexpr uint32_t kIdescAmn = 1u << 15;
+constexpr uint32_t kIdescBmn = 1u << 16;
+constexpr uint32_t kIdescBf16 = (1u << 7) | (1u << 10);
 
 // Shared-memory descriptor of a K-major operand in the 128-byte-swizzle
 // canonical layout: each row holds 64 fp16 (128 B) of the K dimension, rows
@@ -189,6 +221,27 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         GDN_W32(r)
         : "memory");
 }
+// 16-column forms (thread i of the warp: columns [col, col + 16) of its lane).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
 #undef GDN_R32
 #undef GDN_W32
 

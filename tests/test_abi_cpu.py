@@ -129,11 +129,11 @@ def test_input_prep_entries_reject_bad_arguments_on_the_host(lib):
                                      None) == 2
 
 
-def _prefill(lib, cu_host, n, E=0, cap=0, cs=None, dims=None):
+def _prefill(lib, cu_host, n, E=0, cap=0, cs=None, dims=None, ws=None, ws_bytes=0):
     dims = dims or _Dims(16, 32, 128, 128, 1.0)
     arr = (ctypes.c_int32 * len(cu_host))(*cu_host)
     return lib.gdn_prefill_varlen(ctypes.byref(dims), n, FAKE, arr, FAKE, FAKE, FAKE, FAKE, FAKE,
-                                  FAKE, 8, None, None, FAKE, cs, E, cap, None, None)
+                                  FAKE, 8, None, None, FAKE, cs, E, cap, ws, ws_bytes, None, None)
 
 
 def test_prefill_rejects_bad_arguments_on_the_host(lib):
@@ -143,14 +143,33 @@ def test_prefill_rejects_bad_arguments_on_the_host(lib):
     assert _prefill(lib, [0, 2000], 1, E=1, cap=31, cs=None) == 1  # stream missing
     assert _prefill(lib, [0, 2000], 1, E=-1) == 1
     assert _prefill(lib, [0, 10], 1, dims=_Dims(16, 32, 256, 256, 1.0)) == 2
+    assert _prefill(lib, [0, 2000], 1, E=(1 << 24) + 1, cap=1, cs=FAKE) == 1  # 64 E beyond int32 range
     assert _prefill(lib, [0], 0) == 0                              # no sequences: no-op
+
+
+def test_prefill_workspace_contract(lib):
+    import linear_attention_serving_gdn_gb300 as gdn
+    dims = _Dims(16, 32, 128, 128, 1.0)
+    need = lib.gdn_prefill_workspace_bytes(ctypes.byref(dims), 8, 4901)
+    assert need == gdn.gdn_prefill_workspace_bytes(16, 32, 128, 8, 4901)
+    assert lib.gdn_prefill_workspace_bytes(ctypes.byref(_Dims(16, 32, 96, 96, 1.0)), 8, 10) == ctypes.c_size_t(-1).value
+    assert lib.gdn_prefill_workspace_bytes(ctypes.byref(dims), -1, 10) == ctypes.c_size_t(-1).value
+    # A workspace must be 256-byte aligned and at least `need` bytes; both are
+    # checked on the host before anything is launched (GDN_ERR_WORKSPACE).
+    assert _prefill(lib, [0, 10], 1, ws=ctypes.c_void_p(0x10010), ws_bytes=1 << 20) == 4
+    if need > 0:
+        assert _prefill(lib, [0, 10], 1, ws=ctypes.c_void_p(0x10000), ws_bytes=need - 1) == 4
+        assert _prefill(lib, [0, 10], 1) == 4
+    for bad_dims in (_Dims(16, 32, 64, 128, 1.0), _Dims(16, 24, 128, 128, 1.0)):
+        assert _prefill(lib, [0, 10], 1, dims=bad_dims, ws=ctypes.c_void_p(0x10010)) in (1, 2)
 
 
 def _apc(lib, cu_host, n, E=17, table=FAKE, stride=4, first=FAKE, state=FAKE):
     dims = _Dims(16, 32, 128, 128, 1.0)
     arr = (ctypes.c_int32 * len(cu_host))(*cu_host)
     return lib.gdn_prefill_varlen_apc(ctypes.byref(dims), n, FAKE, arr, FAKE, FAKE, FAKE, FAKE, FAKE,
-                                      state, 8, None, None, FAKE, E, table, stride, first, None, None)
+                                      state, 8, None, None, FAKE, E, table, stride, first, None, 0, None,
+                                      None)
 
 
 def test_prefill_apc_rejects_bad_arguments_on_the_host(lib):
@@ -163,16 +182,40 @@ def test_prefill_apc_rejects_bad_arguments_on_the_host(lib):
     assert _apc(lib, [0], 0) == 0                                  # no sequences: no-op
 
 
+def _mixed(lib, dims, nd, n_p, cu, dec_src=FAKE, cs=None, E=0, cap=0, ws=None):
+    return lib.gdn_mixed_step(ctypes.byref(dims), nd, n_p, FAKE, cu, FAKE, FAKE, FAKE, FAKE, FAKE,
+                              FAKE, 8, dec_src, None, None, None, FAKE, cs, E, cap, ws, 0, None, None)
+
+
 def test_mixed_step_rejects_bad_arguments_on_the_host(lib):
     dims = _Dims(16, 16, 128, 128, 1.0)
     bad = (ctypes.c_int32 * 3)(0, 7, 2)
-    assert lib.gdn_mixed_step(ctypes.byref(dims), 4, 2, FAKE, bad, FAKE, FAKE, FAKE, FAKE, FAKE,
-                              FAKE, 8, FAKE, None, None, None, FAKE, None, 0, 0, None, None) == 1
+    assert _mixed(lib, dims, 4, 2, bad) == 1
     good = (ctypes.c_int32 * 2)(0, 7)
-    assert lib.gdn_mixed_step(ctypes.byref(dims), -1, 1, FAKE, good, FAKE, FAKE, FAKE, FAKE, FAKE,
-                              FAKE, 8, FAKE, None, None, None, FAKE, None, 0, 0, None, None) == 1
-    assert lib.gdn_mixed_step(ctypes.byref(dims), 4, 1, FAKE, good, FAKE, FAKE, FAKE, FAKE, FAKE,
-                              FAKE, 8, None, None, None, None, FAKE, None, 0, 0, None, None) == 1
+    assert _mixed(lib, dims, -1, 1, good) == 1
+    assert _mixed(lib, dims, 4, 1, good, dec_src=None) == 1
+
+
+def test_mixed_step_validates_the_prefill_half_before_launching_decode(lib):
+    # Valid decode rows but a bad prefill half: the call must fail validation
+    # (1 or 4) before the decode kernel is launched.  Without a GPU a launch
+    # would have returned GDN_ERR_CUDA (3) instead.
+    dims = _Dims(16, 16, 128, 128, 1.0)
+    cu = (ctypes.c_int32 * 2)(0, 2000)
+    assert _mixed(lib, dims, 4, 1, cu, cs=ctypes.c_void_p(0x10008), E=1, cap=31) == 1  # misaligned stream
+    assert _mixed(lib, dims, 4, 1, cu, cs=FAKE, E=1, cap=30) == 1                       # 31 emits needed
+    assert _mixed(lib, dims, 4, 1, cu, E=(1 << 24) + 1) == 1                            # emission stride
+    assert _mixed(lib, dims, 4, 1, cu, ws=ctypes.c_void_p(0x10010)) == 4               # workspace alignment
+
+
+def test_status_from_device_word(lib):
+    import linear_attention_serving_gdn_gb300 as gdn
+    assert gdn.gdn_status_from_device(0) == 0
+    assert gdn.gdn_status_from_device(gdn.GDN_DEV_TIMEOUT) == 5
+    assert gdn.gdn_status_from_device(gdn.GDN_DEV_TIMEOUT | gdn.GDN_DEV_BAD_SLOT) == 5
+    assert gdn.gdn_status_from_device(gdn.GDN_DEV_BAD_SLOT) == 1
+    assert "workspace" in gdn.gdn_status_string(4)
+    assert "wait" in gdn.gdn_status_string(5)
 
 
 def test_status_strings(lib):
