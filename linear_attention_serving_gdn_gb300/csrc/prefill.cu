@@ -108,15 +108,14 @@ struct Smem {
     // Plain buffers.
     static constexpr uint32_t kM = kL2B2 + 4096;          // f32 [64][kLdM]: A, then T
     static constexpr uint32_t kWb = kM + 64 * kLdM * 4;   // f32 [2][16][16] level-1 products
-    static constexpr uint32_t kG = kWb + 4096;            // f32 [64] cumulative log decay
-    static constexpr uint32_t kGam = kG + 256;            // f32 [64] gamma
+    static constexpr uint32_t kGl = kWb + 4096;           // f32 [64] cumulative log decay G, times log2(e)
+    static constexpr uint32_t kGam = kGl + 256;           // f32 [64] gamma
     static constexpr uint32_t kBG = kGam + 256;           // f32 [64] beta gamma
     static constexpr uint32_t kBeta = kBG + 256;          // f32 [64]
-    static constexpr uint32_t kGraw = kBeta + 256;        // f32 [64]
-    static constexpr uint32_t kDec = kGraw + 256;         // f32 [2][64] exp(G_C - G_t), per stage
+    static constexpr uint32_t kDec = kBeta + 256;         // f32 [2][64] exp(G_C - G_t), per stage
     static constexpr uint32_t kGc = kDec + 512;           // f32 [2] gamma_C, per stage
-    static constexpr uint32_t kBars = kGc + 16;           // 18 mbarriers
-    static constexpr uint32_t kTmem = kBars + 18 * 8;     // TMEM base address
+    static constexpr uint32_t kBars = kGc + 16;           // 20 mbarriers
+    static constexpr uint32_t kTmem = kBars + 20 * 8;     // TMEM base address
     static constexpr uint32_t kFail = kTmem + 4;          // int
     static constexpr uint32_t kEoff = kFail + 12;         // long long [16]
     static constexpr uint32_t kBytes = kEoff + 128;
@@ -156,7 +155,9 @@ enum : int {
     kBarQKFree = 15, // chain done reading a q/k slot and its P~ / decay stage
     kBarDrainC = 16,
     kBarDrainP = 17,
-    kNumBars = 18
+    kBarGamReady = 18, // decays of the chunk the prep group works on are in shared memory
+    kBarConvDone = 19, // chain group: q~, k, v of that chunk converted to fp16
+    kNumBars = 20
 };
 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
@@ -174,6 +175,16 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 w, float f) {
     return r;
 }
 
+// 8 bf16 (one uint4) -> 8 fp16 (exact except below 2^-14).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 w) {
+    uint4 r;
+    r.x = pack_half2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
+    r.y = pack_half2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+    r.z = pack_half2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u));
+    r.w = pack_half2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
+    return r;
+}
+
 __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -187,6 +198,25 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
+
+// (a, b) * (s, t) as one packed fp32x2 multiply (round to nearest, as two
+// separate fp32 multiplies would give).
+__device__ __forceinline__ void mul2(uint32_t &a, uint32_t &b, float s, float t) {
+    asm("{\n\t.reg .b64 x, f, y;\n\t"
+        "mov.b64 x, {%0, %1};\n\t"
+        "mov.b64 f, {%2, %3};\n\t"
+        "mul.rn.f32x2 y, x, f;\n\t"
+        "mov.b64 {%0, %1}, y;\n\t}"
+        : "+r"(a), "+r"(b)
+        : "f"(s), "f"(t));
+}
+
+// 2^x by the hardware approximation (the operation __expf is built on).
+__device__ __forceinline__ float exp2f_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // Byte offset of 16-byte chunk c (8 fp16 along N) of row k of an MN-major
@@ -253,20 +283,26 @@ __device__ int64_t emit_offset(const int32_t *cu, int s, int E, long long *part)
 // ---- the inverse, CUDA-core part ----------------------------------------------
 // Diagonal 16x16 blocks of T = (I + A)^-1 for a strictly lower-triangular A
 // held in M (fp32, row stride kLdM), by the 64 threads p < 64 (block
-// p / 16, column p % 16): right-looking forward substitution; each step
-// finishes x_j and updates the later rows independently of each other.
-// The column is written over the block's A entries after a warp barrier.
+// p / 16, column c = p % 16), left-looking: x_i = [i == c] - sum_{j<i} A_ij x_j,
+// which gives x_i = 0 above the diagonal since x_j = 0 for j < c.  Rows are
+// read as float4 (shared-memory bandwidth is shared with the tensor cores'
+// operand reads).  The column is written over the block's A entries after a
+// warp barrier.
 __device__ __forceinline__ void invert_diag_solve(const float *M, int p, float (&x)[16]) {
     const int c = p & 15, base = ((p >> 4) & 3) * 16;
-    float acc[16];
+    const float *row = M + base * kLdM + base;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+    for (int i = 0; i < 16; ++i) {
+        float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const float xj = (j < c) ? 0.f : (j == c ? 1.f : -acc[j]);
-        x[j] = xj;
-#pragma unroll
-        for (int i = j + 1; i < 16; ++i) acc[i] = fmaf(M[(base + i) * kLdM + base + j], xj, acc[i]);
+        for (int j4 = 0; j4 < i; j4 += 4) {
+            const float4 m = *reinterpret_cast<const float4 *>(row + i * kLdM + j4);
+            acc0 = fmaf(m.x, x[j4], acc0);
+            if (j4 + 1 < i) acc1 = fmaf(m.y, x[j4 + 1], acc1);
+            if (j4 + 2 < i) acc0 = fmaf(m.z, x[j4 + 2], acc0);
+            if (j4 + 3 < i) acc1 = fmaf(m.w, x[j4 + 3], acc1);
+        }
+        x[i] = i == c ? 1.f : (i < c ? 0.f : -(acc0 + acc1));
     }
 }
 __device__ __forceinline__ void invert_diag_store(float *M, int p, const float (&x)[16]) {
@@ -373,9 +409,9 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
     uint8_t *sWT = sm + SM::kWT, *sTpp = sm + SM::kTpp, *sTppp = sm + SM::kTppp;
     uint8_t *sL2A1 = sm + SM::kL2A1, *sL2B1 = sm + SM::kL2B1, *sL2A2 = sm + SM::kL2A2, *sL2B2 = sm + SM::kL2B2;
     float *sM = reinterpret_cast<float *>(sm + SM::kM), *sWb = reinterpret_cast<float *>(sm + SM::kWb);
-    float *sG = reinterpret_cast<float *>(sm + SM::kG), *sGam = reinterpret_cast<float *>(sm + SM::kGam);
+    float *sGl = reinterpret_cast<float *>(sm + SM::kGl), *sGam = reinterpret_cast<float *>(sm + SM::kGam);
     float *sBG = reinterpret_cast<float *>(sm + SM::kBG), *sBeta = reinterpret_cast<float *>(sm + SM::kBeta);
-    float *sGraw = reinterpret_cast<float *>(sm + SM::kGraw), *sGc = reinterpret_cast<float *>(sm + SM::kGc);
+    float *sGc = reinterpret_cast<float *>(sm + SM::kGc);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + SM::kBars);
     uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(sm + SM::kTmem);
     int *fail = reinterpret_cast<int *>(sm + SM::kFail);
@@ -430,7 +466,7 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
         const uint32_t idU = tc::idesc_f16_f32acc(128, 64);
         const uint32_t idS = tc::idesc_f16_f32acc(128, D) | tc::kIdescBmn;
         const uint64_t dWT = tc::desc_mn_sw128(tc::smem_u32(sWT), 0);
-        bool failed = false, u_issued = false;
+        bool failed = false;
         int prev_n = 0, prev_tok0 = 0, prev_s = 0;
 
         // Initial state row j (half hf): fp32 into D_S, fp16 into S16; for an
@@ -489,8 +525,8 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
             uint16_t *op = a.o + static_cast<size_t>(tok_out + 32 * hf) * ldv + static_cast<size_t>(h) * D + j;
             const int lim = n_out - 32 * hf;
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (i < lim) op[static_cast<size_t>(i) * ldv] = float_to_bf16_bits(__uint_as_float(r[i]));
+            for (int i = 0; i < 32; ++i, op += ldv)
+                if (i < lim) *op = float_to_bf16_bits(__uint_as_float(r[i]));
         };
 
         for (int c = 0; c < n_chunks; ++c) {
@@ -499,17 +535,48 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
             const int n = min(kChunk, Lseq - c * kChunk);
             uint8_t *qk = sQK(c % 3);
 
+            // ---- C0: q~, k, v of chunk c to fp16 in place (while the prep group
+            // finishes the chunk): after the Gram has read the bf16 q/k tile.
+            // Thread tid owns the 16-byte items tid and tid + 256 of every 64 x 64
+            // box (rows tid / 8 and tid / 8 + 32); rows past the sequence end
+            // become zeros; q is scaled by scale gamma_t.
+            {
+                bool ok0 = wait_bar(bars + kBarGram, c & 1, fail) && wait_bar(bars + kBarGamReady, c & 1, fail) &&
+                           wait_bar(bars + kBarTmaQK + c % 3, (c / 3) & 1, fail) &&
+                           wait_bar(bars + kBarTmaV + (c & 1), (c / 2) & 1, fail);
+                if (ok0) {
+                    uint8_t *vt = sV(c & 1);
+                    const int r0 = tid >> 3;
+                    const float f0 = a.scale * sGam[r0], f1 = a.scale * sGam[r0 + 32];
+#pragma unroll
+                    for (int b = 0; b < 3 * kKB; ++b) {
+                        const int kind = b / kKB, kb = b % kKB;
+                        uint8_t *base = (kind == 2 ? vt + kb * 8192 : qk + kb * 16384 + (kind == 1 ? 8192 : 0)) + tid * 16;
+                        const uint4 x0 = *reinterpret_cast<const uint4 *>(base);
+                        const uint4 x1 = *reinterpret_cast<const uint4 *>(base + 4096);
+                        uint4 y0 = make_uint4(0, 0, 0, 0), y1 = make_uint4(0, 0, 0, 0);
+                        if (r0 < n) y0 = kind == 0 ? bf16x8_to_f16x8(x0, f0) : bf16x8_to_f16x8(x0);
+                        if (r0 + 32 < n) y1 = kind == 0 ? bf16x8_to_f16x8(x1, f1) : bf16x8_to_f16x8(x1);
+                        *reinterpret_cast<uint4 *>(base) = y0;
+                        *reinterpret_cast<uint4 *>(base + 4096) = y1;
+                    }
+                }
+                tc::fence_proxy_async_smem();  // read by the tensor cores
+                if (group_any(kBarChain, !ok0 || *vfail)) {
+                    failed = true;
+                    break;
+                }
+                if (tid == 0) mbar_arrive(bars + kBarConvDone);
+            }
+
             // ---- P0: operands of chunk c; D_U += S16^T (-W)^T, D_O = S16^T Q~^T --
             // (wait results that gate warp-collective TMEM accesses are made warp-uniform)
             const bool okr = __all_sync(0xffffffffu, wait_bar(bars + kBarReady + s, (c >> 1) & 1, fail));
             tc::fence_after_sync();
             if (tid == 0 && okr) {
-                bool oku = u_issued;
-                if (!oku) {
-                    oku = wait_bar(bars + kBarUReady, c & 1, fail);
-                    if (oku) issue_u(c);
-                }
+                const bool oku = wait_bar(bars + kBarUReady, c & 1, fail);  // T'' (v was converted above)
                 if (oku) {
+                    issue_u(c);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
                         tc::mma_f16_ta(tbase + kColU, tbase + kColS16 + kk * 8, dWT + kk * (2048 >> 4),
@@ -534,7 +601,7 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                     uint32_t r[32];
                     tc::tmem_ld32(tl + kColS + c0, r);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(gC * __uint_as_float(r[i]));
+                    for (int i = 0; i < 32; i += 2) mul2(r[i], r[i + 1], gC, gC);
                     tc::tmem_st32(tl + kColS + c0, r);
                 }
             }
@@ -548,9 +615,11 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                 const float *dec = sDec(s) + 32 * hf;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float u0 = __uint_as_float(r[2 * i]), u1 = __uint_as_float(r[2 * i + 1]);
-                    pu[i] = pack_half2(u0, u1);
-                    pd[i] = pack_half2(u0 * dec[2 * i], u1 * dec[2 * i + 1]);
+                    uint32_t u0 = r[2 * i], u1 = r[2 * i + 1];
+                    pu[i] = pack_half2(__uint_as_float(u0), __uint_as_float(u1));
+                    const float2 d2 = *reinterpret_cast<const float2 *>(dec + 2 * i);
+                    mul2(u0, u1, d2.x, d2.y);
+                    pd[i] = pack_half2(__uint_as_float(u0), __uint_as_float(u1));
                 }
                 tc::tmem_st16(tl + kColU16 + 16 * hf, pu);
                 tc::tmem_st16(tl + kColUd16 + 16 * hf, pd);
@@ -574,12 +643,6 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                     tc::mma_f16_ta(tbase + kColO + 64 * s, tbase + kColU16 + kk * 8, dPs + kk * 2, idU, 1);
                 tc::mma_commit(bars + kBarC);
                 tc::mma_commit(bars + kBarQKFree);
-                u_issued = false;
-                if (c + 1 < n_chunks && tc::mbar_test_wait(bars + kBarUReady, (c + 1) & 1)) {
-                    tc::fence_after_sync();
-                    issue_u(c + 1);
-                    u_issued = true;
-                }
             }
             __syncwarp();
             const bool okc = __all_sync(0xffffffffu, wait_bar(bars + kBarC, c & 1, fail));
@@ -651,13 +714,17 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
         int c_done = 0;                          // chunks whose loads the loop consumed
         int qk_issued = -1, v_issued = -1;       // highest chunk whose copies were issued (pid 0)
         constexpr uint32_t kQKTx = 2u * kKB * 8192u, kVTx = kKB * 8192u;
-        float gv = 0.f, bv = 0.f;
+        // g and beta of a chunk, tokens 2l and 2l + 1 in lane l of warp 10 (zeros
+        // past the sequence end), loaded a chunk ahead.
+        float gv0 = 0.f, gv1 = 0.f, bv0 = 0.f, bv1 = 0.f;
         auto load_gb = [&](int cc) {
-            const int nn = min(kChunk, Lseq - cc * kChunk);
-            if (pid < 64) {
-                const size_t gi = static_cast<size_t>(t0 + cc * kChunk + min(pid & 63, nn - 1)) * a.h_v + h;
-                gv = a.g[gi];
-                bv = a.beta[gi];
+            if (warp == 10) {
+                const int nn = min(kChunk, Lseq - cc * kChunk), l = pid & 31;
+                const size_t gi = static_cast<size_t>(t0 + cc * kChunk + 2 * l) * a.h_v + h;
+                gv0 = 2 * l < nn ? a.g[gi] : 0.f;
+                bv0 = 2 * l < nn ? a.beta[gi] : 0.f;
+                gv1 = 2 * l + 1 < nn ? a.g[gi + a.h_v] : 0.f;
+                bv1 = 2 * l + 1 < nn ? a.beta[gi + a.h_v] : 0.f;
             }
         };
         auto issue_qk = [&](int cc) {  // q and k of chunk cc into slot cc % 3
@@ -679,6 +746,22 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
             for (int kb = 0; kb < kKB; ++kb) tma_load_2d(tile + kb * 8192, &L.tm_v, h * D + kb * 64, t0 + cc * kChunk, tb);
             v_issued = cc;
         };
+        // Gram [Q;K] K^T of chunk cc in bf16, straight from its TMA tile, into the
+        // prep columns (issued as soon as the previous chunk's -W^T has been read
+        // out of them).
+        auto issue_gram = [&](int cc) -> bool {
+            if (!wait_bar(bars + kBarTmaQK + cc % 3, (cc / 3) & 1, fail)) return false;
+            tc::fence_after_sync();
+            const uint64_t dQK = tc::desc_k_sw128(tc::smem_u32(sQK(cc % 3)));
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                tc::mma_f16(tbase + kColPrep, dQK + off, dQK + off + (8192 >> 4),
+                            tc::idesc_f16_f32acc(128, 64) | tc::kIdescBf16, kk > 0);
+            }
+            tc::mma_commit(bars + kBarGram);
+            return true;
+        };
         if (n_chunks > 0) {
             if (pid == 0) {
                 issue_qk(0);
@@ -687,6 +770,7 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                     issue_qk(1);
                     issue_v(1);
                 }
+                issue_gram(0);
             }
             load_gb(0);
         }
@@ -697,41 +781,13 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
             uint8_t *qk = sQK(c % 3);
             uint8_t *vt = sV(c & 1);
 
-            // ---- Q1: v copies of chunk c + 1, this chunk's g and beta ----------------
+            // ---- Q2: prefix sum of the decays (the Gram is already running) -----------
             bool ok = true;
-            if (pid == 0 && c >= 1) {
-                ok = wait_bar(bars + kBarTFree, (c - 1) & 1, fail);  // T'' and v slot of chunk c - 1 free
-                if (ok && c + 1 < n_chunks) issue_v(c + 1);
-            }
-            if (pid < 64) {
-                const int t = pid & 63;
-                sGraw[t] = t < n ? gv : 0.f;
-                sBeta[t] = t < n ? bv : 0.f;
-            }
-            if (c + 1 < n_chunks) load_gb(c + 1);
-            if (group_any(kBarPrep, !ok || *vfail)) {
-                failed = true;
-                break;
-            }
-
-            // ---- Q2: Gram [Q;K] K^T in bf16 from the TMA tile || prefix sum ----------
-            if (pid == 0) {
-                ok = wait_bar(bars + kBarTmaQK + c % 3, (c / 3) & 1, fail);
-                if (ok) {
-                    tc::fence_after_sync();
-                    const uint64_t dQK = tc::desc_k_sw128(tc::smem_u32(qk));
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                        tc::mma_f16(tbase + kColPrep, dQK + off, dQK + off + (8192 >> 4),
-                                    tc::idesc_f16_f32acc(128, 64) | tc::kIdescBf16, kk > 0);
-                    }
-                    tc::mma_commit(bars + kBarGram);
-                }
-            }
             if (warp == 10) {  // inclusive prefix sum of g over the chunk, fixed order
                 const int l = pid & 31;
-                const float g0 = sGraw[2 * l], g1 = sGraw[2 * l + 1];
+                const float g0 = gv0, g1 = gv1;
+                sBeta[2 * l] = bv0;
+                sBeta[2 * l + 1] = bv1;
                 const float pair = g0 + g1;
                 float incl = pair;
 #pragma unroll
@@ -743,15 +799,18 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                 const float G0 = excl + g0, G1 = excl + g0 + g1;
                 const float Gc = __shfl_sync(0xffffffffu, G1, 31);  // G_63, the chunk total
                 const float e0 = expf(G0), e1 = expf(G1);
-                sG[2 * l] = G0;
-                sG[2 * l + 1] = G1;
+                sGl[2 * l] = G0 * 1.4426950408889634f;
+                sGl[2 * l + 1] = G1 * 1.4426950408889634f;
                 sGam[2 * l] = e0;
                 sGam[2 * l + 1] = e1;
-                sBG[2 * l] = sBeta[2 * l] * e0;
-                sBG[2 * l + 1] = sBeta[2 * l + 1] * e1;
+                sBG[2 * l] = bv0 * e0;
+                sBG[2 * l + 1] = bv1 * e1;
                 sDec(s)[2 * l] = expf(Gc - G0);
                 sDec(s)[2 * l + 1] = expf(Gc - G1);
                 if (l == 31) sGc[s] = e1;
+                __syncwarp();
+                if (l == 0) mbar_arrive(bars + kBarGamReady);
+                if (c + 1 < n_chunks) load_gb(c + 1);
             }
             if (group_any(kBarPrep, !ok || *vfail)) {
                 failed = true;
@@ -773,21 +832,34 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                         *reinterpret_cast<uint4 *>(sP(s) + tc::sw128_chunk_offset(p & 63, q, 64)) = z;
                 }
             } else {
+                // exp(G_r - G_c) f = exp2(Gl_r + log2 f - Gl_c) with Gl = G log2(e);
+                // f = beta_r (A rows) is folded into the exponent when positive.
+                // Only the warps on a diagonal 32 x 32 block apply the mask.
                 uint32_t x[32];
                 tc::tmem_ld32(tl + kColPrep + 32 * hf, x);
                 const int r = p & 63;
-                const float Gr = sG[r];
-                const float f = p < 64 ? a.scale : sBeta[r];
-                const int diag = p < 64 ? 0 : 1;  // P~ keeps s == t, A does not
+                const bool isA = p >= 64;
+                const float br = isA ? sBeta[r] : 1.f;
+                const bool fold = br > 0.f;
+                const float Er = sGl[r] + (fold ? __log2f(br) : 0.f);
+                const float post = isA ? (fold ? 1.f : br) : a.scale;
+                const bool diag_blk = (hf == 0) == ((p & 32) == 0);  // warp-uniform
+                const int lim = isA ? r - 1 : r;                      // A: s < t, P~: s <= t
 #pragma unroll
                 for (int q4 = 0; q4 < 32; q4 += 4) {
                     const int q0 = 32 * hf + q4;
-                    const float4 g4 = *reinterpret_cast<const float4 *>(sG + q0);
+                    const float4 g4 = *reinterpret_cast<const float4 *>(sGl + q0);
                     const float gg[4] = {g4.x, g4.y, g4.z, g4.w};
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        x[q4 + u] = __float_as_uint((q0 + u + diag <= r) ? f * __expf(Gr - gg[u]) * __uint_as_float(x[q4 + u])
-                                                                         : 0.f);
+                    for (int u = 0; u < 4; ++u) {
+                        float y = exp2f_approx(Er - gg[u]) * __uint_as_float(x[q4 + u]);
+                        if (diag_blk && q0 + u > lim) y = 0.f;
+                        x[q4 + u] = __float_as_uint(y);
+                    }
+                }
+                if (post != 1.f) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[i] = __float_as_uint(post * __uint_as_float(x[i]));
                 }
                 if (p < 64) {
 #pragma unroll
@@ -815,9 +887,16 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                 break;
             }
 
-            // ---- Q4: diagonal blocks and level 1 (warps 8, 9) || q~, k, v to fp16 -----
+            // ---- Q4: diagonal blocks and level 1 (warps 8, 9) ----------------------------
             bool okv = true;
             if (pid < 64) {
+                // T'' and the v slot of chunk c - 1 are free once the chain's U'^T
+                // product of that chunk is done (long before this point): the v
+                // copies of chunk c + 1 go there, a whole chunk ahead.
+                if (pid == 0 && c >= 1) {
+                    okv = wait_bar(bars + kBarTFree, (c - 1) & 1, fail);
+                    if (okv && c + 1 < n_chunks) issue_v(c + 1);
+                }
                 float xd[16];
                 invert_diag_solve(sM, pid, xd);
                 __syncwarp();
@@ -836,24 +915,6 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                 for (int i = 0; i < 32; ++i)
                     x[i] = (i >= 16 && r < 16) ? 0u : __float_as_uint(sM[(rb + r) * kLdM + rb + i]);
                 store_row32_f16(pid < 32 ? sL2B1 : sL2A2, r, x, 1.f, pid >= 32);
-            } else {
-                okv = wait_bar(bars + kBarTmaV + (c & 1), (c / 2) & 1, fail) &&
-                      wait_bar(bars + kBarTmaQK + c % 3, (c / 3) & 1, fail);
-                if (okv) {
-                    // 16-byte items of the q, k, v boxes: rows past the sequence end
-                    // become zeros; q is scaled by scale gamma_t (Q~).
-                    constexpr int kPerBox = 64 * 8;
-                    constexpr int kItems = 3 * kKB * kPerBox;
-                    for (int e = pid - 64; e < kItems; e += kGroup - 64) {
-                        const int which = e / (kKB * kPerBox), rem = e % (kKB * kPerBox);
-                        const int kb = rem / kPerBox, w = rem % kPerBox, r = w >> 3;
-                        uint8_t *base = which == 2 ? vt + kb * 8192 : qk + kb * 16384 + (which == 1 ? 8192 : 0);
-                        uint4 *ptr = reinterpret_cast<uint4 *>(base + w * 16);
-                        const float f = which == 0 ? a.scale * sGam[r] : 1.f;
-                        const uint4 x = *ptr;
-                        *ptr = r < n ? bf16x8_to_f16x8(x, f) : make_uint4(0, 0, 0, 0);
-                    }
-                }
             }
             tc::fence_proxy_async_smem();
             tc::fence_before_sync();
@@ -942,7 +1003,8 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
 
             // ---- Q6: -W^T = K^T (-T''')^T -> fp16 tile --------------------------------
             if (pid == 0) {
-                ok = (c == 0) || wait_bar(bars + kBarWFree, (c - 1) & 1, fail);
+                ok = ((c == 0) || wait_bar(bars + kBarWFree, (c - 1) & 1, fail)) &&
+                     wait_bar(bars + kBarConvDone, c & 1, fail);  // k of chunk c in fp16
                 if (ok) {
                     tc::fence_after_sync();
                     const uint64_t dK = tc::desc_mn_sw128(tc::smem_u32(qk + 8192), kLboK);
@@ -980,11 +1042,13 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
             }
             // ---- hand over: q/k copies of chunk c + 2 into the slot of chunk c - 1 ----
             if (pid == 0) {
-                bool okq = true;
-                if (c >= 1) okq = wait_bar(bars + kBarQKFree, (c - 1) & 1, fail);
+                mbar_arrive(bars + kBarReady + s);
+                bool okq = c + 1 >= n_chunks || issue_gram(c + 1);
+                // The chain is done with chunk c - 1 (q/k slot, P~ and decay stage)
+                // before the next chunk's preparation reuses them.
+                if (okq && c >= 1) okq = wait_bar(bars + kBarQKFree, (c - 1) & 1, fail);
                 if (okq && c + 2 < n_chunks) issue_qk(c + 2);
-                if (okq) mbar_arrive(bars + kBarReady + s);
-                else atomicExch(fail, 1);
+                if (!okq) atomicExch(fail, 1);
             }
             c_done = c + 1;
         }
