@@ -38,6 +38,7 @@ import gdn_inputs as gi  # noqa: E402
 DECODE_ROWS, H, D = 256, 16, 128
 # Algorithmic bytes per decode row: state read + write, q, k, v, o, g, beta, slot index.
 DECODE_BYTES_PER_ROW = 2 * H * D * D * 4 + 2 * H * D * 2 + 2 * H * D * 2 + 2 * H * 4 + 4
+DECODE_BYTES_PER_ROW_H16 = DECODE_BYTES_PER_ROW  # the mixed step's decode rows have the same shape
 # Algorithmic flops per prefill token (GVA H_k=16, H_v=32, d=128, C=64):
 # shared K K^T and Q K^T per key head, then per value head the WY products,
 # W S0, Q S0, (M o QK^T) U and K~^T U.
@@ -271,6 +272,24 @@ def time_decode_e2e_eager(torch, gdn, t, steps, warmup, world):
     return s.elapsed_time(e), h2d, d2h
 
 
+def timed_median(torch, fn, reps=20, warm=10):
+    """Median device time (ms) of `reps` calls after `warm` untimed ones, each
+    bracketed by CUDA events on the current stream; clocks sampled meanwhile."""
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    with Clocks(torch.cuda.current_device()) as clk:
+        ev = []
+        for _ in range(reps):
+            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            z.record()
+            ev.append((a, z))
+        torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(z) for a, z in ev), clk.summary()
+
+
 def prefill_case(torch, gdn, wl, dev, reps, E=0):
     b = wl["prefill"]
     q, k, v = bf16(torch, b.q, dev), bf16(torch, b.k, dev), bf16(torch, b.v, dev)
@@ -288,26 +307,17 @@ def prefill_case(torch, gdn, wl, dev, reps, E=0):
         gdn.gdn_prefill_varlen(q, k, v, g, beta, cu, cu_h, o, state=cache, dst_slot=dst,
                                chunk_states=cs, emit_every_chunks=E)
 
-    call()
-    torch.cuda.synchronize()
-    ev = []
-    for _ in range(reps):
-        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        call()
-        z.record()
-        ev.append((a, z))
-    torch.cuda.synchronize()
-    ms = statistics.median(a.elapsed_time(z) for a, z in ev)
+    ms, clocks = timed_median(torch, call, reps=reps)
     T = b.total_tokens
     fl = prefill_flops_per_token(b.h_k, b.h_v, b.d) * T
     return {"workload": wl["name"], "seqlens": b.seqlens if n <= 16 else f"{n} x {b.seqlens[0]}",
-            "tokens": T, "ms": ms, "tokens_per_s": T / (ms * 1e-3),
+            "tokens": T, "ms": ms, "timing": f"median of {reps} calls after 10 warm-up calls",
+            "tokens_per_s": T / (ms * 1e-3),
             "algorithmic_tflops": fl / (ms * 1e-3) / 1e12, "emit_every_chunks": E,
-            "emitted_states": n_emit}
+            "emitted_states": n_emit, "clocks": clocks}
 
 
-def mixed_case(torch, gdn, dev, reps):
+def mixed_case(torch, gdn, dev, reps, peaks):
     wl = gi.mixed_step(0)
     dec, pre = wl["decode"], wl["prefill"]
     nd = dec.num_seqs
@@ -339,23 +349,22 @@ def mixed_case(torch, gdn, dev, reps):
         main.wait_stream(s_dec)
         main.wait_stream(s_pre)
 
-    def timed(fn):
-        fn()
-        torch.cuda.synchronize()
-        ev = []
-        for _ in range(reps):
-            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            z.record()
-            ev.append((a, z))
-        torch.cuda.synchronize()
-        return statistics.median(a.elapsed_time(z) for a, z in ev)
-
-    ms = timed(call)
-    ms2 = timed(colaunch)
+    ms, clocks = timed_median(torch, call, reps=reps)
+    ms2, _ = timed_median(torch, colaunch, reps=reps)
+    # Roofline of the step: the decode rows are bound by HBM, the prefill by
+    # the tensor cores, and the two run one after the other, so the floor is
+    # the sum of the two parts' roofline times.
+    dec_bytes = nd * DECODE_BYTES_PER_ROW_H16
+    pre_flops = pre.total_tokens * prefill_flops_per_token(pre.h_k, pre.h_v, pre.d)
+    floor_ms = (dec_bytes / (peaks["hbm_gbs"] * 1e9) + pre_flops / (peaks["bf16_tflops"] * 1e12)) * 1e3
     return {"workload": wl["name"], "decode_rows": nd, "prefill_seqlens": pre.seqlens, "ms": ms,
-            "tokens_per_s": (nd + pre.total_tokens) / (ms * 1e-3), "colaunch_two_streams_ms": ms2}
+            "timing": f"median of {reps} calls after 10 warm-up calls",
+            "tokens_per_s": (nd + pre.total_tokens) / (ms * 1e-3), "colaunch_two_streams_ms": ms2,
+            "roofline": {"bound": "hbm (decode rows) + tensor (prefill)", "decode_bytes": dec_bytes,
+                         "prefill_flops": pre_flops, "floor_ms": floor_ms, "frac": floor_ms / ms,
+                         "peak_hbm_gbs": peaks["hbm_gbs"], "peak_tflops": peaks["bf16_tflops"],
+                         "peak_source": peaks["source"]},
+            "clocks": clocks}
 
 
 def multi_decode_case(torch, gdn, dev, peaks, rows=256, T=4, reps=10):
@@ -474,11 +483,11 @@ def decode_latency_case(torch, gdn, dev, rows_list=(1, 8, 64, 256), iters=200):
 def run_extra(torch, gdn, dev, wanted, peaks, prefix_seqlen=32768):
     extra = []
     if "prefill" in wanted:
-        extra.append(prefill_case(torch, gdn, gi.prefill_qwen3next_gva(0), dev, reps=5))
+        extra.append(prefill_case(torch, gdn, gi.prefill_qwen3next_gva(0), dev, reps=20))
     if "prefix" in wanted:
-        extra.append(prefill_case(torch, gdn, gi.prefix_cache_prefill(0, seqlen=prefix_seqlen), dev, reps=3, E=17))
+        extra.append(prefill_case(torch, gdn, gi.prefix_cache_prefill(0, seqlen=prefix_seqlen), dev, reps=20, E=17))
     if "mixed" in wanted:
-        extra.append(mixed_case(torch, gdn, dev, reps=5))
+        extra.append(mixed_case(torch, gdn, dev, reps=20, peaks=peaks))
     if "graph" in wanted:
         extra.append(decode_latency_case(torch, gdn, dev))
     if "multi" in wanted:
@@ -526,31 +535,83 @@ def measured_traffic(kernel: str, workload: str = "decode_r256_h16_d128"):
 # CPU oracle (baseline and reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_decode_rate(n_rows, n_steps, seed=0):
-    """Time the fp64 oracle on n_rows decode rows x n_steps tokens each, all
-    host cores; returns (rows/s, seconds, threads)."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "hardware")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
+def oracle_decode_rate(n_rows, n_steps, threads, seed=0):
+    """Time the fp64 oracle on n_rows decode rows x n_steps tokens each (H=16,
+    d=128) with `threads` OpenMP threads; returns (rows/s, seconds)."""
     import oracle
     b = gi.token_batch([n_steps] * n_rows, H, H, D, seed, init_state=True)
-    threads = oracle.max_threads()
     t0 = time.perf_counter()
     oracle.run_chains(b, n_threads=threads)
     dt = time.perf_counter() - t0
-    return n_rows * n_steps / dt, dt, threads
+    return n_rows * n_steps / dt, dt
 
 
-def cpu_baseline(target_s=10.0):
-    """Oracle on a bounded sample of the decode workload: all 256 rows, as
-    many recurrent steps as fit in about target_s seconds."""
+def decode_steps_for(target_s, threads, rows=DECODE_ROWS):
+    """Recurrent steps per row so that `rows` rows take about target_s seconds."""
     steps = 1
     while True:
-        rate, dt, threads = oracle_decode_rate(DECODE_ROWS, steps)
-        if dt >= target_s or steps >= 4096:
-            break
-        steps = max(steps * 2, int(steps * target_s / max(dt, 1e-3) * 1.1))
-    return {"value": rate, "unit": "decode rows/s", "cores": threads, "kind": "oracle",
-            "seconds": dt,
+        rate, dt = oracle_decode_rate(rows, steps, threads)
+        if dt >= 0.25 * target_s or steps >= 1 << 14:
+            return max(1, int(steps * target_s / max(dt, 1e-3)))
+        steps *= 4
+
+
+def oracle_prefill_rate(threads, n_seq_sample):
+    """fp64 oracle on the first n_seq_sample sequences of the 8-sequence GVA
+    prefill (H_k=16, H_v=32, d=128), every value head; returns (prefill
+    tokens/s, seconds, tokens)."""
+    import oracle
+    b = gi.prefill_qwen3next_gva(0)["prefill"]
+    pairs = [(s, h) for s in range(n_seq_sample) for h in range(b.h_v)]
+    tokens = int(b.cu_seqlens[n_seq_sample])
+    t0 = time.perf_counter()
+    oracle.run_chains(b, pairs=pairs, n_threads=threads)
+    dt = time.perf_counter() - t0
+    return tokens / dt, dt, tokens
+
+
+def cpu_baseline(target_s=6.0):
+    """The fp64 oracle on the host cores: decode rows/s and prefill tokens/s,
+    each on all cores and on one thread, on bounded samples of the workloads."""
+    import oracle
+    cores = oracle.max_threads()
+    nproc = os.cpu_count()
+    steps = decode_steps_for(target_s, cores)
+    rate_all, dt_all = oracle_decode_rate(DECODE_ROWS, steps, cores)
+    rows1 = 16
+    rate_1, dt_1 = oracle_decode_rate(rows1, max(1, steps // 2), 1)
+    p_all, pdt_all, ptok = oracle_prefill_rate(cores, 8)
+    p_1, pdt_1, ptok1 = oracle_prefill_rate(1, 2)
+    return {"value": rate_all, "unit": "decode rows/s", "cores": cores, "kind": "oracle",
+            "seconds": dt_all,
             "sample": f"{DECODE_ROWS} rows x {steps} recurrent steps of the 256-row decode workload "
-                      f"(H=16, d=128), fp64 token recurrence, OpenMP over (row, head) chains"}
+                      f"(H=16, d=128), fp64 token recurrence, OpenMP over (row, head) chains",
+            "one_thread": {"value": rate_1, "unit": "decode rows/s", "seconds": dt_1,
+                           "sample": f"{rows1} rows x {max(1, steps // 2)} recurrent steps, 1 thread"},
+            "prefill": {"value": p_all, "unit": "prefill tokens/s", "cores": cores, "seconds": pdt_all,
+                        "sample": f"the whole 8-sequence GVA prefill ({ptok} tokens, H_k=16, H_v=32, d=128)",
+                        "one_thread": {"value": p_1, "unit": "prefill tokens/s", "seconds": pdt_1,
+                                       "sample": f"its first 2 sequences ({ptok1} tokens), 1 thread"}},
+            "nproc": nproc, "cpu_model": cpu_model()}
 
 
 DECODE_METRIC = "GDN decode rows/s (packed recurrent decode, fp32 state)"
@@ -566,29 +627,47 @@ def decode_config(n_slots, world=1):
 def reference_arm(args):
     # The oracle runs on the host cores of rank 0 only; no process group or
     # GPU is needed, so the other ranks of a torchrun launch exit at once.
+    # Each step is one oracle call on the same sample shape as the decode
+    # cpu_baseline: all 256 rows x S recurrent steps (S sized so that a call
+    # takes about two seconds), so the two CPU figures measure the same work.
+    import oracle
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    rows = 64
-    rate, dt, threads = oracle_decode_rate(rows, 1)
+    threads = oracle.max_threads()
+    steps = decode_steps_for(2.0, threads)
     for _ in range(args.warmup):
-        oracle_decode_rate(rows, 1)
+        oracle_decode_rate(DECODE_ROWS, steps, threads)
     times = []
     for _ in range(args.steps):
-        r, d, threads = oracle_decode_rate(rows, 1)
+        _, d = oracle_decode_rate(DECODE_ROWS, steps, threads)
         times.append(d)
     tot = sum(times)
-    value = rows * args.steps / tot
+    value = DECODE_ROWS * steps * args.steps / tot
     line = {"impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "rows/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": decode_config(2 * DECODE_ROWS, world),
             "cpu_baseline": {"value": value, "unit": "rows/s", "cores": threads, "kind": "oracle",
-                             "sample": f"{rows} of the 256 decode rows per step, 1 recurrent step"},
+                             "sample": f"{DECODE_ROWS} rows x {steps} recurrent steps per step (H=16, d=128)",
+                             "nproc": os.cpu_count(), "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def host_cost():
+    """Host time per C-ABI call measured from C (csrc/tools/host_cost.cpp)."""
+    from linear_attention_serving_gdn_gb300 import _build
+    exe = _build.HOST_COST
+    if not os.path.exists(exe):
+        return None
+    try:
+        out = subprocess.run([exe, "2000"], capture_output=True, text=True, timeout=120)
+        return json.loads(out.stdout.strip().splitlines()[-1])
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError):
+        return None
 
 
 # ---------------------------------------------------------------------------
@@ -671,6 +750,8 @@ def main():
     }
     if wanted - {"decode"}:
         line["workloads"] = run_extra(torch, gdn, dev, wanted, peaks, args.prefix_seqlen)
+    if rank == 0:
+        line["host_us_per_call"] = host_cost()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:

@@ -73,7 +73,12 @@ def load_library() -> ctypes.CDLL:
         return _lib
     if not os.path.exists(_build.LIB):
         raise ImportError(f"libgdn.so is not built ({_build.LIB}); run __graft_entry__.build()")
-    lib = ctypes.CDLL(_build.LIB)
+    _lib = _configure(ctypes.CDLL(_build.LIB))
+    return _lib
+
+
+def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Declare the C signatures of every entry point on a loaded library."""
     lib.gdn_decode_packed.restype = ctypes.c_int
     lib.gdn_decode_packed.argtypes = [ctypes.POINTER(Dims), _I32, _P, _P, _P, _P, _P, _P, _I64,
                                       _P, _P, _P, _P, _P]
@@ -111,7 +116,6 @@ def load_library() -> ctypes.CDLL:
     lib.gdn_grid_emit_every_chunks.argtypes = [_I32]
     lib.gdn_status_string.restype = ctypes.c_char_p
     lib.gdn_status_string.argtypes = [ctypes.c_int]
-    _lib = lib
     return lib
 
 

@@ -43,6 +43,10 @@ def up_to_date() -> bool:
     if not os.path.exists(LIB):
         return False
     t = os.path.getmtime(LIB)
+    tool = os.path.join(OUT_DIR, "gdn_host_cost")
+    tool_src = os.path.join(CSRC, "tools", "host_cost.cpp")
+    if not os.path.exists(tool) or os.path.getmtime(tool) < max(os.path.getmtime(tool_src), t):
+        return False
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
@@ -80,7 +84,42 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    build_tools()
     return LIB
+
+
+HOST_COST = os.path.join(OUT_DIR, "gdn_host_cost")
+
+
+def build_tools() -> str:
+    """Build the host-cost probe (csrc/tools/host_cost.cpp) against the library."""
+    src = os.path.join(CSRC, "tools", "host_cost.cpp")
+    out = os.path.join(OUT_DIR, "gdn_host_cost")
+    cmd = [nvcc(), *ARCH, "-O2", "-std=c++17", "-I", INCLUDE, src, "-o", out, "-L", OUT_DIR, "-lgdn",
+           "-Xlinker", "-rpath", "-Xlinker", OUT_DIR, "-cudart", "static"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"host-cost probe build failed:\n{r.stdout}\n{r.stderr}")
+    return out
+
+
+def build_variant(name: str, defines: list[str], force: bool = False) -> str:
+    """Build the library with extra preprocessor definitions into
+    ``_lib_<name>/libgdn.so`` (used by tests that need a differently
+    configured kernel, e.g. a short handshake wait limit)."""
+    global OUT_DIR, LIB
+    saved = OUT_DIR, LIB, os.environ.get("GDN_NVCC_EXTRA")
+    try:
+        OUT_DIR = os.path.join(HERE, f"_lib_{name}")
+        LIB = os.path.join(OUT_DIR, "libgdn.so")
+        os.environ["GDN_NVCC_EXTRA"] = " ".join([saved[2] or ""] + [f"-D{d}" for d in defines]).strip()
+        return build(force=force)
+    finally:
+        OUT_DIR, LIB = saved[0], saved[1]
+        if saved[2] is None:
+            os.environ.pop("GDN_NVCC_EXTRA", None)
+        else:
+            os.environ["GDN_NVCC_EXTRA"] = saved[2]
 
 
 if __name__ == "__main__":
