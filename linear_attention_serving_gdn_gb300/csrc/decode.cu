@@ -104,16 +104,41 @@ constexpr int kMultiGroups = 4;
 constexpr int kMultiRows = kRowsPerGroup * kMultiGroups;  // 16
 
 // Multi-token decode (speculative tokens): the item's 16 state rows stay in
-// registers across the row's tokens; after token t the state is stored at
+// registers across the row's tokens, whose inputs (up to kStageTokens of them)
+// are staged in shared memory by asynchronous copies issued before the state
+// is loaded; after token t the state is stored at
 // dst_slots[r * T + t] when that entry is >= 0 (a snapshot a verifier can
 // roll back to), or, with dst_slots == NULL, once after the last token back
 // to src_slot[r].  Every step is the same update_row as the packed decode, so
 // T tokens here equal T packed-decode calls bit for bit.
+// Per warp, the inputs of up to kStageTokens tokens of its current row are
+// staged in shared memory by asynchronous copies issued when the item starts:
+// one memory round trip per item instead of one per token.
+constexpr int kStageTokens = 8;
+template <int D>
+struct MultiStage {
+    static constexpr int kK = 0, kQ = 2 * D, kV = 4 * D, kG = kV + 2 * kMultiRows, kB = kG + 16;
+    static constexpr int kBytes = kB + 16;  // per token: k, q rows (bf16), the item's v, g, beta
+};
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+                 "l"(gmem)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+                 "l"(gmem)
+                 : "memory");
+}
+
 template <int D>
 __global__ void __launch_bounds__(kMultiThreads, 2)
 decode_multi_kernel(const DecodeMultiArgs a) {
     constexpr int V4 = D / 32;
     constexpr int kItemsPerHead = D / kMultiRows;
+    using MS = MultiStage<D>;
+    __shared__ __align__(16) uint8_t stage_all[kMultiThreads / 32][kStageTokens][MS::kBytes];
     const int lane = threadIdx.x & 31;
     const int sub = lane >> 3;
     const int l8 = lane & 7;
@@ -122,14 +147,45 @@ decode_multi_kernel(const DecodeMultiArgs a) {
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int group = a.h_v / a.h_k;
 
-    for (int64_t it = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-         it < n_items; it += nwarps) {
+    const bool staged = T <= kStageTokens;
+    // Copies of item iit's token inputs into this warp's stage (one commit
+    // group): rows of k and q (D / 8 16-byte pieces each), the item's v
+    // (kMultiRows / 8 pieces), g and beta.
+    auto issue_stage = [&](int64_t iit) {
+        const int row0_ = static_cast<int>(iit % kItemsPerHead) * kMultiRows;
+        const int64_t rh_ = iit / kItemsPerHead;
+        const int h_ = static_cast<int>(rh_ % a.h_v), r_ = static_cast<int>(rh_ / a.h_v), kh_ = h_ / group;
+        uint8_t(*st)[MS::kBytes] = stage_all[threadIdx.x >> 5];
+        for (int t = 0; t < T; ++t) {
+            const size_t tok = static_cast<size_t>(r_) * T + t;
+            const size_t gh = tok * a.h_v + h_;
+            if (lane < D / 8) {
+                cp_async16(st[t] + MS::kK + 16 * lane, a.k + (tok * a.h_k + kh_) * D + 8 * lane);
+                cp_async16(st[t] + MS::kQ + 16 * lane, a.q + (tok * a.h_k + kh_) * D + 8 * lane);
+            } else if (lane < D / 8 + kMultiRows / 8) {
+                const int pc = lane - D / 8;
+                cp_async16(st[t] + MS::kV + 16 * pc, a.v + gh * D + row0_ + 8 * pc);
+            } else if (lane == 30) {
+                cp_async4(st[t] + MS::kG, a.g + gh);
+            } else if (lane == 31) {
+                cp_async4(st[t] + MS::kB, a.beta + gh);
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    for (int64_t it = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; it < n_items;
+         it += nwarps) {
         const int blk = static_cast<int>(it % kItemsPerHead);
         const int64_t rh = it / kItemsPerHead;
         const int h = static_cast<int>(rh % a.h_v);
         const int r = static_cast<int>(rh / a.h_v);
         const int row0 = blk * kMultiRows;
         const int kh = h / group;
+        uint8_t(*stage)[MS::kBytes] = stage_all[threadIdx.x >> 5];
+        if (staged) {
+            __syncwarp();  // the previous item's reads of the stage are done
+            issue_stage(it);
+        }
 
         const int src = a.src_slot[r];
         if (src < 0 || src >= a.num_slots) {
@@ -149,16 +205,30 @@ decode_multi_kernel(const DecodeMultiArgs a) {
             for (int m = 0; m < V4; ++m)
                 s[i][m] = ld_state4(sp + static_cast<size_t>(j) * D + 4 * (l8 + 8 * m));
         }
+        if (staged) {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+            __syncwarp();
+        }
         for (int t = 0; t < T; ++t) {
             const size_t tok = static_cast<size_t>(r) * T + t;
             float kk[V4 * 4], qq[V4 * 4];
-            load_bf16_slice<V4>(a.k + (tok * a.h_k + kh) * D, l8, kk);
-            load_bf16_slice<V4>(a.q + (tok * a.h_k + kh) * D, l8, qq);
             const size_t gh = tok * a.h_v + h;
-            const float alpha = expf(a.g[gh]);
-            const float beta = a.beta[gh];
+            float alpha, beta;
+            const uint16_t *vrow;
+            if (staged) {
+                load_bf16_slice<V4>(reinterpret_cast<const uint16_t *>(stage[t] + MS::kK), l8, kk);
+                load_bf16_slice<V4>(reinterpret_cast<const uint16_t *>(stage[t] + MS::kQ), l8, qq);
+                alpha = expf(*reinterpret_cast<const float *>(stage[t] + MS::kG));
+                beta = *reinterpret_cast<const float *>(stage[t] + MS::kB);
+                vrow = reinterpret_cast<const uint16_t *>(stage[t] + MS::kV) - row0;
+            } else {
+                load_bf16_slice<V4>(a.k + (tok * a.h_k + kh) * D, l8, kk);
+                load_bf16_slice<V4>(a.q + (tok * a.h_k + kh) * D, l8, qq);
+                alpha = expf(a.g[gh]);
+                beta = a.beta[gh];
+                vrow = a.v + gh * D;
+            }
             const float kq = octet_dot<V4>(kk, qq);
-            const uint16_t *vrow = a.v + gh * D;
             uint16_t *orow = a.o + gh * D;
             int dst = -1;
             if (a.dst_slots) {

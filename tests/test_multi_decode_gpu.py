@@ -48,7 +48,8 @@ def _setup(rows, T, h_k, h, d, seed):
 
 
 @pytest.mark.parametrize("rows,T,h_k,h,d,scale", [(16, 4, 4, 16, 128, 1.0), (5, 7, 2, 6, 64, 0.125),
-                                                 (3, 1, 4, 4, 128, 1.0)])
+                                                 (3, 1, 4, 4, 128, 1.0),
+                                                 (4, 11, 4, 8, 128, 1.0)])  # more tokens than the stage holds
 def test_multi_decode_outputs_and_snapshots_vs_oracle(gdn, rows, T, h_k, h, d, scale):
     b, src, dst, cache, x = _setup(rows, T, h_k, h, d, seed=21)
     o = torch.empty((rows * T, h, d), dtype=torch.bfloat16, device="cuda")
