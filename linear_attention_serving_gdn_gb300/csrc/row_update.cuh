@@ -89,32 +89,57 @@ __device__ __forceinline__ float octet_dot(const float (&kk)[V4 * 4], const floa
     return octet_sum(acc);
 }
 
-// Updates the lane's slice of one row in place and returns o_j.
+// Packed fp32x2 arithmetic (round to nearest, as two separate fp32
+// operations would give): d = a * b + c and d = a * b on element pairs.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// Updates the lane's slice of one row in place and returns o_j.  The two dot
+// products run as packed pairs: even and odd elements of the slice are summed
+// in separate halves, which are added before the octet reduction.
 template <int V4>
 __device__ __forceinline__ float update_row(float4 (&s)[V4], const float (&kk)[V4 * 4],
                                             const float (&qq)[V4 * 4], float alpha, float beta,
                                             float vj, float kq, float scale) {
-    float a = 0.f, b = 0.f;
+    float2 a2 = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int m = 0; m < V4; ++m) {
-        a = fmaf(s[m].x, kk[4 * m + 0], a);
-        b = fmaf(s[m].x, qq[4 * m + 0], b);
-        a = fmaf(s[m].y, kk[4 * m + 1], a);
-        b = fmaf(s[m].y, qq[4 * m + 1], b);
-        a = fmaf(s[m].z, kk[4 * m + 2], a);
-        b = fmaf(s[m].z, qq[4 * m + 2], b);
-        a = fmaf(s[m].w, kk[4 * m + 3], a);
-        b = fmaf(s[m].w, qq[4 * m + 3], b);
+        const float2 s01 = make_float2(s[m].x, s[m].y), s23 = make_float2(s[m].z, s[m].w);
+        a2 = fma2(s01, make_float2(kk[4 * m + 0], kk[4 * m + 1]), a2);
+        b2 = fma2(s01, make_float2(qq[4 * m + 0], qq[4 * m + 1]), b2);
+        a2 = fma2(s23, make_float2(kk[4 * m + 2], kk[4 * m + 3]), a2);
+        b2 = fma2(s23, make_float2(qq[4 * m + 2], qq[4 * m + 3]), b2);
     }
-    a = octet_sum(a);
-    b = octet_sum(b);
+    const float a = octet_sum(a2.x + a2.y);
+    const float b = octet_sum(b2.x + b2.y);
     const float u = beta * (vj - alpha * a);
+    const float2 al = make_float2(alpha, alpha), uu = make_float2(u, u);
 #pragma unroll
     for (int m = 0; m < V4; ++m) {
-        s[m].x = fmaf(kk[4 * m + 0], u, alpha * s[m].x);
-        s[m].y = fmaf(kk[4 * m + 1], u, alpha * s[m].y);
-        s[m].z = fmaf(kk[4 * m + 2], u, alpha * s[m].z);
-        s[m].w = fmaf(kk[4 * m + 3], u, alpha * s[m].w);
+        const float2 s01 = fma2(make_float2(kk[4 * m + 0], kk[4 * m + 1]), uu, mul2(al, make_float2(s[m].x, s[m].y)));
+        const float2 s23 = fma2(make_float2(kk[4 * m + 2], kk[4 * m + 3]), uu, mul2(al, make_float2(s[m].z, s[m].w)));
+        s[m] = make_float4(s01.x, s01.y, s23.x, s23.y);
     }
     return scale * fmaf(u, kq, alpha * b);
 }
