@@ -198,37 +198,86 @@ def time_decode(torch, gdn, t, steps, warmup, world):
     return total_ms, [total_ms / steps] * steps
 
 
-def time_decode_e2e(torch, gdn, t, steps, warmup, world):
-    """End to end, as a serving loop runs decode: each step is one CUDA-graph
-    replay of [pinned host -> device copy of the step's packed q, k, v, g,
-    beta; gdn_decode_packed; device -> host copy of o], captured from the
-    public entry point once per input buffer (two buffers, alternating).
-    The state cache stays resident on the device.  Every step moves all of
-    its bytes inside the timed region; replays run back to back on one
-    stream, so a step's copies do not overlap another step's decode (a
-    decode step's inputs depend on the previous step's outputs)."""
+# Row groups of the end-to-end decode step (measured on the GB300, us per
+# 256-row step: 1 group 120, 2 groups 116, 4 groups 127, 8 groups 143: each
+# group adds graph-node dependencies of a few us; host copies run at
+# ~180 GB/s H2D and ~145 GB/s D2H).
+E2E_PARTS = 2
+
+
+def decode_e2e_graphs(torch, gdn, t, parts):
+    """The end-to-end decode step as CUDA graphs (two, for two alternating
+    device input buffers), captured from the public entry point: the step's
+    q, k, v, g, beta go from pinned host memory to the device, the decode
+    runs, o comes back to pinned host memory.  The step's rows are split into
+    `parts` groups (parts = 1: one copy, one call, one copy): group i's inputs
+    are copied on an input stream, its decode runs on the capturing stream
+    once they have landed, and its o is copied back on an output stream once
+    its decode has finished, so the copies of one group overlap the decode of
+    the others.  A row's result does not depend on the rows sharing its
+    launch, so the groups compute exactly what one call over all rows does.
+    Returns (graphs, h2d bytes per step, d2h bytes per step, o_host)."""
     names = ("q", "k", "v", "g", "beta")
-    sizes = [t[n].numel() * t[n].element_size() for n in names]
+    rows = t["q"].shape[0]
+    if rows % parts:
+        raise ValueError(f"{rows} rows do not split into {parts} equal groups")
+    pr = rows // parts
+    sizes = [t[n][:pr].numel() * t[n].element_size() for n in names]
     offs = [0]
     for sz in sizes:
         offs.append(offs[-1] + (sz + 255) // 256 * 256)
-    host = torch.empty(offs[-1], dtype=torch.uint8).pin_memory()
-    for n, o0, sz in zip(names, offs, sizes):
-        host[o0:o0 + sz].copy_(t[n].contiguous().view(torch.uint8).reshape(-1).cpu())
+    stride = offs[-1]  # one group's packed inputs
+    host = torch.empty(stride * parts, dtype=torch.uint8).pin_memory()
+    for p in range(parts):
+        for n, o0, sz in zip(names, offs, sizes):
+            src = t[n][p * pr:(p + 1) * pr].contiguous().view(torch.uint8).reshape(-1).cpu()
+            host[p * stride + o0:p * stride + o0 + sz].copy_(src)
     o_host = torch.empty(t["o"].shape, dtype=t["o"].dtype).pin_memory()
-    h2d = sum(sizes)
+    h2d = sum(sizes) * parts
     d2h = o_host.numel() * o_host.element_size()
-    dev_in = [torch.empty(offs[-1], dtype=torch.uint8, device=t["q"].device) for _ in range(2)]
+    dev = t["q"].device
+    dev_in = [torch.empty(stride * parts, dtype=torch.uint8, device=dev) for _ in range(2)]
     outs = [torch.empty_like(t["o"]) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     graphs = []
     for b in range(2):
-        x = {n: dev_in[b][o0:o0 + sz].view(t[n].dtype).view(t[n].shape) for n, o0, sz in zip(names, offs, sizes)}
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            dev_in[b].copy_(host, non_blocking=True)
-            gdn.gdn_decode_packed(x["q"], x["k"], x["v"], x["g"], x["beta"], t["cache"], t["src"], outs[b])
-            o_host.copy_(outs[b], non_blocking=True)
+            main = torch.cuda.current_stream()
+            s_in.wait_stream(main)
+            s_out.wait_stream(main)
+            landed = []
+            with torch.cuda.stream(s_in):
+                for p in range(parts):
+                    dev_in[b][p * stride:(p + 1) * stride].copy_(host[p * stride:(p + 1) * stride], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(s_in)
+                    landed.append(ev)
+            for p in range(parts):
+                main.wait_event(landed[p])
+                x = {n: dev_in[b][p * stride + o0:p * stride + o0 + sz].view(t[n].dtype).view((pr,) + tuple(t[n].shape[1:]))
+                     for n, o0, sz in zip(names, offs, sizes)}
+                rs = slice(p * pr, (p + 1) * pr)
+                gdn.gdn_decode_packed(x["q"], x["k"], x["v"], x["g"], x["beta"], t["cache"], t["src"][rs], outs[b][rs])
+                done = torch.cuda.Event()
+                done.record(main)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(done)
+                    o_host[rs].copy_(outs[b][rs], non_blocking=True)
+            main.wait_stream(s_in)
+            main.wait_stream(s_out)
         graphs.append(g)
+    return graphs, h2d, d2h, o_host
+
+
+def time_decode_e2e(torch, gdn, t, steps, warmup, world, parts=1):
+    """End to end, as a serving loop runs decode: each step is one replay of
+    the graphs of decode_e2e_graphs (alternating input buffers).  The state
+    cache stays resident on the device; every step moves all of its input and
+    output bytes inside the timed region.  Replays run back to back on one
+    stream, so no step's copies overlap another step's decode (a decode
+    step's inputs depend on the previous step's outputs)."""
+    graphs, h2d, d2h, _ = decode_e2e_graphs(torch, gdn, t, parts)
     for k in range(warmup):
         graphs[k & 1].replay()
     torch.cuda.synchronize()
@@ -721,8 +770,10 @@ def main():
         total_ms, per_launch = time_decode(torch, gdn, t, args.steps, args.warmup, world)
     clocks = clk.summary()
     total_ms = max_over_ranks(torch, world, total_ms)
-    e2e_ms, h2d, d2h = time_decode_e2e(torch, gdn, t, args.steps, args.warmup, world)
+    e2e_ms, h2d, d2h = time_decode_e2e(torch, gdn, t, args.steps, args.warmup, world, parts=E2E_PARTS)
     e2e_ms = max_over_ranks(torch, world, e2e_ms)
+    e2e_serial_ms, _, _ = time_decode_e2e(torch, gdn, t, args.steps, args.warmup, world, parts=1)
+    e2e_serial_ms = max_over_ranks(torch, world, e2e_serial_ms)
     e2e_eager_ms, _, _ = time_decode_e2e_eager(torch, gdn, t, args.steps, args.warmup, world)
     e2e_eager_ms = max_over_ranks(torch, world, e2e_eager_ms)
 
@@ -744,7 +795,11 @@ def main():
                      "bytes_per_launch": bytes_per_launch, "launch_ms": launch_ms},
         "e2e": {"value": rows_total / (e2e_ms * 1e-3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "mode": "one CUDA-graph replay per step of [H2D packed inputs, gdn_decode_packed, D2H o]",
+                "mode": f"one CUDA-graph replay per step; the 256 rows in {E2E_PARTS} groups, each [H2D of its "
+                        "packed inputs on an input stream, gdn_decode_packed, D2H of its o on an output stream], "
+                        "so one group's copies overlap another's decode",
+                "serial_value": rows_total / (e2e_serial_ms * 1e-3),
+                "serial_mode": "one CUDA-graph replay per step of [H2D packed inputs, gdn_decode_packed, D2H o]",
                 "eager_value": rows_total / (e2e_eager_ms * 1e-3),
                 "eager_mode": "the same step issued from Python: H2D, decode, D2H on one stream"},
         "gpu_launches": args.steps,

@@ -167,3 +167,24 @@ def test_decode_prefill_colaunch_on_two_streams(gdn):
     torch.cuda.synchronize()
     assert torch.equal(_bits(o_gr), _bits(o_ref)) and torch.equal(cache_gr, cache_ref)
     assert st.item() == 0
+
+
+@pytest.mark.parametrize("parts", [2, 4])
+def test_end_to_end_step_in_row_groups_matches_single_call(gdn, parts):
+    """The benchmark's end-to-end decode step with its rows split into groups
+    (host copies of one group overlapping the decode of another, on three
+    streams, captured as a CUDA graph) gives the o and the states of the
+    single-group step bit for bit, over two replays."""
+    import bench
+    res = []
+    for p in (1, parts):
+        _, t = bench.decode_setup(torch, seed=0, dev="cuda")
+        graphs, h2d, d2h, o_host = bench.decode_e2e_graphs(torch, gdn, t, p)
+        graphs[0].replay()
+        graphs[1].replay()
+        torch.cuda.synchronize()
+        res.append((o_host.clone(), t["cache"].clone(), h2d, d2h))
+    (o1, s1, i1, d1), (o2, s2, i2, d2) = res
+    assert (i1, d1) == (i2, d2)
+    assert torch.equal(_bits(o1), _bits(o2))
+    assert torch.equal(s1, s2)
