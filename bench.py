@@ -457,7 +457,7 @@ def multi_decode_case(torch, gdn, dev, peaks, rows=256, T=4, reps=10):
     return out
 
 
-def prep_case(torch, gdn, dev, peaks, T=131072, h_k=16, h_v=32, reps=10):
+def prep_case(torch, gdn, dev, peaks, T=131072, h_k=16, h_v=32, reps=20):
     """Input preparation over 131072 tokens (H_k=16, H_v=32, d=128): q, k
     read and written in bf16, a, b read and g, beta written in fp32."""
     raw = gi.raw_inputs(T, h_k, h_v, D, 9)
@@ -470,21 +470,11 @@ def prep_case(torch, gdn, dev, peaks, T=131072, h_k=16, h_v=32, reps=10):
     def call():
         gdn.gdn_prep_inputs(q_raw, k_raw, a, b_, A_log, dt_bias, q, k, g, beta)
 
-    call()
-    torch.cuda.synchronize()
-    ev = []
-    for _ in range(reps):
-        a0, z0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a0.record()
-        call()
-        z0.record()
-        ev.append((a0, z0))
-    torch.cuda.synchronize()
-    ms = statistics.median(a0.elapsed_time(z0) for a0, z0 in ev)
+    ms, clocks = timed_median(torch, call, reps=reps)
     byts = T * (2 * 2 * h_k * D * 2 + 4 * h_v * 4)
     gbs = byts / (ms * 1e-3) / 1e9
     return {"workload": f"prep_inputs_t{T}_hk{h_k}_hv{h_v}_d128", "ms": ms, "tokens_per_s": T / (ms * 1e-3),
-            "bytes_per_launch": byts,
+            "bytes_per_launch": byts, "timing": f"median of {reps} calls after 10 warm-up calls", "clocks": clocks,
             "roofline": {"bound": "hbm", "kernel": "prep_kernel<128>", "achieved": gbs, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"]}}
 

@@ -22,22 +22,32 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
     const int64_t rows = 2 * rows_per_tensor;  // q rows, then k rows
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    // Warp-uniform loop over groups of 4 rows (one per lane octet): every lane
-    // takes part in the octet reductions; octets past the end only skip I/O.
-    for (int64_t base = warp * 4; base < rows; base += nwarps * 4) {
-        const int64_t row = base + sub;
-        const bool live = row < rows;
-        const bool is_k = row >= rows_per_tensor;
-        const int64_t rr = is_k ? row - rows_per_tensor : row;
-        float x[V4 * 4];
-        if (live) {
-            load_bf16_slice<V4>((is_k ? a.k_raw : a.q_raw) + rr * D, l8, x);
-        } else {
+    // Warp-uniform loop over 8 rows at a time, two groups of 4 (one row per
+    // lane octet), both groups' loads issued before either reduction: every
+    // lane takes part in the octet reductions; octets past the end only skip
+    // I/O.
+    for (int64_t base = warp * 8; base < rows; base += nwarps * 8) {
+        float x[2][V4 * 4];
+        bool live[2], is_k[2];
+        int64_t rr[2];
 #pragma unroll
-            for (int e = 0; e < V4 * 4; ++e) x[e] = 0.f;
+        for (int u = 0; u < 2; ++u) {
+            const int64_t row = base + 4 * u + sub;
+            live[u] = row < rows;
+            is_k[u] = row >= rows_per_tensor;
+            rr[u] = is_k[u] ? row - rows_per_tensor : row;
+            if (live[u]) {
+                load_bf16_slice<V4>((is_k[u] ? a.k_raw : a.q_raw) + rr[u] * D, l8, x[u]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < V4 * 4; ++e) x[u][e] = 0.f;
+            }
         }
-        normalize_bf16<V4>(x, a.eps);
-        if (live) store_bf16_slice<V4>((is_k ? a.k : a.q) + rr * D, l8, x);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            normalize_bf16<V4>(x[u], a.eps);
+            if (live[u]) store_bf16_slice<V4>((is_k[u] ? a.k : a.q) + rr[u] * D, l8, x[u]);
+        }
     }
     const int64_t n_gate = a.num_tokens * a.h_v;
     for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_gate;
@@ -52,13 +62,17 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
 
 template <int D>
 cudaError_t launch_prep_d(const PrepArgs &a, cudaStream_t stream) {
+    static int occ[kMaxDevices] = {};
     int dev = 0, sms = 0;
     if (!current_device(&dev, &sms)) return cudaErrorInvalidDevice;
     const int64_t rows = 2 * a.num_tokens * a.h_k;
-    const int64_t need_rows = (rows + (kPrepThreads / 8) - 1) / (kPrepThreads / 8);
+    const int64_t need_rows = (rows + (kPrepThreads / 4) - 1) / (kPrepThreads / 4);  // 8 rows per warp
     const int64_t need_gate = (a.num_tokens * a.h_v + kPrepThreads - 1) / kPrepThreads;
     int64_t grid = need_rows > need_gate ? need_rows : need_gate;
-    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    // One wave of resident blocks: every block walks the rows with the same
+    // grid stride, so blocks beyond the resident count would run as a short,
+    // half-empty second wave.
+    const int64_t cap = static_cast<int64_t>(sms) * blocks_per_sm(prep_kernel<D>, kPrepThreads, dev, occ);
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
     prep_kernel<D><<<static_cast<int>(grid), kPrepThreads, 0, stream>>>(a);
