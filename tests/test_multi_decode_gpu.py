@@ -124,3 +124,35 @@ def test_multi_decode_in_place_padded_rows_and_bad_snapshot_slot(gdn):
         assert np.array_equal(o2n[r * T:(r + 1) * T], o1n[r * T:(r + 1) * T])
     snap_last = gu.get_states_math(c2, dst[[0, 2, 3, 4, 5], T - 1])
     assert np.array_equal(snap_last, gu.get_states_math(c_inplace, src[[0, 2, 3, 4, 5]]))
+
+
+def test_multi_decode_final_only_with_next_item_prefetch(gdn):
+    """Final state only, T >= 3 and more items than the grid has warps: each
+    warp prefetches its next item's state into L2.  Outputs and final states
+    equal T in-place packed-decode calls bit for bit and match the oracle; a
+    padded row (src < 0) is skipped by both, its prefetch included."""
+    rows, T, h, d = 48, 4, 16, 128  # 48 x 16 x 8 = 6144 items, more than 2 x 8 warps per SM on 152 SMs
+    b, src, _, cache_m, x = _setup(rows, T, 16, h, d, seed=13)
+    src = src.copy()
+    src[5] = -1
+    cache_p = cache_m.clone()
+    src_t = torch.from_numpy(src).cuda()
+    o_m = torch.empty((rows * T, h, d), dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_decode_multi(T, x["q"], x["k"], x["v"], x["g"], x["beta"], cache_m, src_t, o_m)
+    o_p = torch.empty((rows, T, h, d), dtype=torch.bfloat16, device="cuda")
+    for t in range(T):
+        idx = torch.from_numpy(np.arange(rows) * T + t).cuda()
+        step = {n: x[n].index_select(0, idx).contiguous() for n in ("q", "k", "v", "g", "beta")}
+        ot = torch.empty((rows, h, d), dtype=torch.bfloat16, device="cuda")
+        gdn.gdn_decode_packed(step["q"], step["k"], step["v"], step["g"], step["beta"], cache_p, src_t, ot)
+        o_p[:, t] = ot
+    torch.cuda.synchronize()
+    assert torch.equal(o_m.view(torch.int16), o_p.reshape(rows * T, h, d).view(torch.int16))
+    assert torch.equal(cache_m, cache_p)
+    live = np.array([r for r in range(rows) if src[r] >= 0])
+    ref = oracle.run_chains(b)
+    o_ref = gu.o_ref_dense(b, ref).reshape(rows, T, h, d)
+    gu.assert_o_close(gu.o_to_numpy(o_m).reshape(rows, T, h, d)[live], o_ref[live])
+    assert o_m.reshape(rows, T, h, d)[5].float().abs().max().item() == 0.0
+    gu.assert_state_close(gu.get_states_math(cache_m, src[live]),
+                          ref["s_final"].reshape(rows, h, d, d)[live], "final states")
