@@ -529,45 +529,47 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                 if (i < lim) *op = float_to_bf16_bits(__uint_as_float(r[i]));
         };
 
-        for (int c = 0; c < n_chunks; ++c) {
+        // ---- C0: q~, k, v of chunk cc to fp16 in place: after the Gram has read
+        // the bf16 q/k tile.  Chunk 0 before the loop, chunk c + 1 while the
+        // state update of chunk c runs on the tensor cores.  Thread tid owns the
+        // 16-byte items tid and tid + 256 of every 64 x 64 box (rows tid / 8 and
+        // tid / 8 + 32); rows past the sequence end become zeros; q is scaled by
+        // scale gamma_t.  Returns false when the group fails.
+        auto convert = [&](int cc) -> bool {
+            const int ncc = min(kChunk, Lseq - cc * kChunk);
+            uint8_t *qkc = sQK(cc % 3);
+            bool ok0 = wait_bar(bars + kBarGram, cc & 1, fail) && wait_bar(bars + kBarGamReady, cc & 1, fail) &&
+                       wait_bar(bars + kBarTmaQK + cc % 3, (cc / 3) & 1, fail) &&
+                       wait_bar(bars + kBarTmaV + (cc & 1), (cc / 2) & 1, fail);
+            if (ok0) {
+                uint8_t *vt = sV(cc & 1);
+                const int r0 = tid >> 3;
+                const float f0 = a.scale * sGam[r0], f1 = a.scale * sGam[r0 + 32];
+#pragma unroll
+                for (int b = 0; b < 3 * kKB; ++b) {
+                    const int kind = b / kKB, kb = b % kKB;
+                    uint8_t *base = (kind == 2 ? vt + kb * 8192 : qkc + kb * 16384 + (kind == 1 ? 8192 : 0)) + tid * 16;
+                    const uint4 x0 = *reinterpret_cast<const uint4 *>(base);
+                    const uint4 x1 = *reinterpret_cast<const uint4 *>(base + 4096);
+                    uint4 y0 = make_uint4(0, 0, 0, 0), y1 = make_uint4(0, 0, 0, 0);
+                    if (r0 < ncc) y0 = kind == 0 ? bf16x8_to_f16x8(x0, f0) : bf16x8_to_f16x8(x0);
+                    if (r0 + 32 < ncc) y1 = kind == 0 ? bf16x8_to_f16x8(x1, f1) : bf16x8_to_f16x8(x1);
+                    *reinterpret_cast<uint4 *>(base) = y0;
+                    *reinterpret_cast<uint4 *>(base + 4096) = y1;
+                }
+            }
+            tc::fence_proxy_async_smem();  // read by the tensor cores
+            if (group_any(kBarChain, !ok0 || *vfail)) return false;
+            if (tid == 0) mbar_arrive(bars + kBarConvDone);
+            return true;
+        };
+
+        if (n_chunks > 0 && !convert(0)) failed = true;
+        for (int c = 0; c < n_chunks && !failed; ++c) {
             const int s = c & 1;
             const int tok0 = t0 + c * kChunk;
             const int n = min(kChunk, Lseq - c * kChunk);
             uint8_t *qk = sQK(c % 3);
-
-            // ---- C0: q~, k, v of chunk c to fp16 in place (while the prep group
-            // finishes the chunk): after the Gram has read the bf16 q/k tile.
-            // Thread tid owns the 16-byte items tid and tid + 256 of every 64 x 64
-            // box (rows tid / 8 and tid / 8 + 32); rows past the sequence end
-            // become zeros; q is scaled by scale gamma_t.
-            {
-                bool ok0 = wait_bar(bars + kBarGram, c & 1, fail) && wait_bar(bars + kBarGamReady, c & 1, fail) &&
-                           wait_bar(bars + kBarTmaQK + c % 3, (c / 3) & 1, fail) &&
-                           wait_bar(bars + kBarTmaV + (c & 1), (c / 2) & 1, fail);
-                if (ok0) {
-                    uint8_t *vt = sV(c & 1);
-                    const int r0 = tid >> 3;
-                    const float f0 = a.scale * sGam[r0], f1 = a.scale * sGam[r0 + 32];
-#pragma unroll
-                    for (int b = 0; b < 3 * kKB; ++b) {
-                        const int kind = b / kKB, kb = b % kKB;
-                        uint8_t *base = (kind == 2 ? vt + kb * 8192 : qk + kb * 16384 + (kind == 1 ? 8192 : 0)) + tid * 16;
-                        const uint4 x0 = *reinterpret_cast<const uint4 *>(base);
-                        const uint4 x1 = *reinterpret_cast<const uint4 *>(base + 4096);
-                        uint4 y0 = make_uint4(0, 0, 0, 0), y1 = make_uint4(0, 0, 0, 0);
-                        if (r0 < n) y0 = kind == 0 ? bf16x8_to_f16x8(x0, f0) : bf16x8_to_f16x8(x0);
-                        if (r0 + 32 < n) y1 = kind == 0 ? bf16x8_to_f16x8(x1, f1) : bf16x8_to_f16x8(x1);
-                        *reinterpret_cast<uint4 *>(base) = y0;
-                        *reinterpret_cast<uint4 *>(base + 4096) = y1;
-                    }
-                }
-                tc::fence_proxy_async_smem();  // read by the tensor cores
-                if (group_any(kBarChain, !ok0 || *vfail)) {
-                    failed = true;
-                    break;
-                }
-                if (tid == 0) mbar_arrive(bars + kBarConvDone);
-            }
 
             // ---- P0: operands of chunk c; D_U += S16^T (-W)^T, D_O = S16^T Q~^T --
             // (wait results that gate warp-collective TMEM accesses are made warp-uniform)
@@ -645,6 +647,10 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                 tc::mma_commit(bars + kBarQKFree);
             }
             __syncwarp();
+            if (c + 1 < n_chunks && !convert(c + 1)) {  // the next chunk's operands, while these products run
+                failed = true;
+                break;
+            }
             const bool okc = __all_sync(0xffffffffu, wait_bar(bars + kBarC, c & 1, fail));
             tc::fence_after_sync();
 
