@@ -32,13 +32,15 @@
 //       U^T, (diag(dec) U)^T -> fp16 A operands in TMEM
 //       D_S   = gamma_C D_S + (diag(dec) U)^T K,   D_O += U^T P~^T
 //       D_S  -> fp16 S16 (A operand in TMEM), emission, final state
-//     and writes the previous chunk's output while the next products run;
+//     writes the previous chunk's output while the first products run, and
+//     converts the next chunk's q~, k, v tiles to fp16 in place (after the
+//     prep group's Gram has read them) while the state update runs;
 //   prep group (warps 8-15), one chunk ahead: q, k, v tiles by TMA, the Gram
 //     [Q;K] K^T in bf16 straight from the TMA tiles, decays, P~, A, the
 //     inverse (16x16 diagonal blocks by substitution and the first doubling
 //     level on the CUDA cores in fp32; the second level, the 32x32 lower-left
-//     block, as two tcgen05 products), T'' and -T''', q~/k/v converted to fp16
-//     in place, U'^T preset by the chain's tensor-core issuer, and
+//     block, as two tcgen05 products), T'' and -T''' (U'^T = V^T T''^T is
+//     then preset by the chain's tensor-core issuer), and
 //     -W^T = K^T (-T''')^T.
 //
 // The fp32 state lives in TMEM for the whole chain; its fp16 copy (an operand)
@@ -576,7 +578,7 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
             const bool okr = __all_sync(0xffffffffu, wait_bar(bars + kBarReady + s, (c >> 1) & 1, fail));
             tc::fence_after_sync();
             if (tid == 0 && okr) {
-                const bool oku = wait_bar(bars + kBarUReady, c & 1, fail);  // T'' (v was converted above)
+                const bool oku = wait_bar(bars + kBarUReady, c & 1, fail);  // T'' (v of chunk c is converted already)
                 if (oku) {
                     issue_u(c);
 #pragma unroll
