@@ -28,15 +28,17 @@
 //   chain group (warps 0-7; thread (j, hf): TMEM lane j = value column j,
 //     half hf of the lane's columns), per chunk:
 //       D_U  += S16^T (-W)^T          (D_U was preset to U'^T = V^T T''^T)
-//       D_O   = S16^T Q~^T            (output accumulator, two buffers)
+//       D_O   = S16^T Q~^T            (output accumulator)
 //       U^T, (diag(dec) U)^T -> fp16 A operands in TMEM
 //       D_S   = gamma_C D_S + (diag(dec) U)^T K,   D_O += U^T P~^T
 //       D_S  -> fp16 S16 (A operand in TMEM), emission, final state
-//     writes the previous chunk's output while the first products run, and
-//     converts the next chunk's q~, k, v tiles to fp16 in place (after the
-//     prep group's Gram has read them) while the state update runs;
-//   prep group (warps 8-15), one chunk ahead: q, k, v tiles by TMA, the Gram
-//     [Q;K] K^T in bf16 straight from the TMA tiles, decays, P~, A, the
+//     writes the previous chunk's output while the first products run (the
+//     output product of the chunk waits for it), converts the next chunk's
+//     q~, k, v tiles to fp16 in place (after their Gram has read them) while
+//     the state update runs, and then queues the Gram [Q;K] K^T of the chunk
+//     after next (bf16, straight from its TMA tile, into its own TMEM columns);
+//   prep group (warps 8-15), one chunk ahead: q, k, v tiles by TMA (and the
+//     first chunk's Gram), decays, P~ and A from the Gram, the
 //     inverse (16x16 diagonal blocks by substitution and the first doubling
 //     level on the CUDA cores in fp32; the second level, the 32x32 lower-left
 //     block, as two tcgen05 products), T'' and -T''' (U'^T = V^T T''^T is
@@ -116,8 +118,8 @@ struct Smem {
     static constexpr uint32_t kBeta = kBG + 256;          // f32 [64]
     static constexpr uint32_t kDec = kBeta + 256;         // f32 [2][64] exp(G_C - G_t), per stage
     static constexpr uint32_t kGc = kDec + 512;           // f32 [2] gamma_C, per stage
-    static constexpr uint32_t kBars = kGc + 16;           // 20 mbarriers
-    static constexpr uint32_t kTmem = kBars + 20 * 8;     // TMEM base address
+    static constexpr uint32_t kBars = kGc + 16;           // 21 mbarriers
+    static constexpr uint32_t kTmem = kBars + 21 * 8;     // TMEM base address
     static constexpr uint32_t kFail = kTmem + 4;          // int
     static constexpr uint32_t kEoff = kFail + 12;         // long long [16]
     static constexpr uint32_t kBytes = kEoff + 128;
@@ -134,11 +136,12 @@ struct Smem {
 // TMEM column map (512 columns; lane j = value column j, or row of a prep product).
 constexpr uint32_t kColS = 0;       // fp32 state S^T, D columns
 constexpr uint32_t kColU = 128;     // U^T, 64 columns
-constexpr uint32_t kColO = 192;     // output accumulator O^T, two buffers of 64
+constexpr uint32_t kColO = 192;     // output accumulator O^T, 64 columns
+constexpr uint32_t kColGram = 256;  // Gram [Q;K] K^T of a chunk, 64 columns
 constexpr uint32_t kColS16 = 320;   // S^T fp16, packed (D / 2 columns): A operand
 constexpr uint32_t kColU16 = 384;   // U^T fp16 packed: A operand
 constexpr uint32_t kColUd16 = 416;  // (diag(dec) U)^T fp16 packed: A operand
-constexpr uint32_t kColPrep = 448;  // prep products: Gram; X and T_B; -W^T
+constexpr uint32_t kColPrep = 448;  // prep products: X and T_B; -W^T
 constexpr uint32_t kTmemCols = 512;
 
 // mbarriers.
@@ -159,7 +162,8 @@ enum : int {
     kBarDrainP = 17,
     kBarGamReady = 18, // decays of the chunk the prep group works on are in shared memory
     kBarConvDone = 19, // chain group: q~, k, v of that chunk converted to fp16
-    kNumBars = 20
+    kBarGramFree = 20, // prep group done reading a chunk's Gram from TMEM
+    kNumBars = 21
 };
 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
@@ -394,6 +398,21 @@ __device__ __forceinline__ void store_row32_f16(uint8_t *tile, int row, const ui
     }
 }
 
+// Gram [Q;K] K^T of one chunk in bf16, straight from its q/k TMA tile (q box,
+// then k box, per 64-wide block of d), into the Gram TMEM columns; completion
+// is signalled on `bar`.
+template <int D>
+__device__ __forceinline__ void gram_mma(uint32_t tbase, const uint8_t *qk_tile, uint64_t *bar) {
+    const uint64_t dQK = tc::desc_k_sw128(tc::smem_u32(qk_tile));
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+        tc::mma_f16(tbase + kColGram, dQK + off, dQK + off + (8192 >> 4),
+                    tc::idesc_f16_f32acc(128, 64) | tc::kIdescBf16, kk > 0);
+    }
+    tc::mma_commit(bar);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
@@ -469,7 +488,7 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
         const uint32_t idS = tc::idesc_f16_f32acc(128, D) | tc::kIdescBmn;
         const uint64_t dWT = tc::desc_mn_sw128(tc::smem_u32(sWT), 0);
         bool failed = false;
-        int prev_n = 0, prev_tok0 = 0, prev_s = 0;
+        int prev_n = 0, prev_tok0 = 0;
 
         // Initial state row j (half hf): fp32 into D_S, fp16 into S16; for an
         // empty sequence straight to the destination slot.
@@ -521,9 +540,9 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
         // Output of a finished chunk, o_t = (Q~ S + P~ U)_t, tokens 32 hf ..
         // 32 hf + 31 of value column j, one bf16 per (token, j): a warp's 32
         // lanes store 64 contiguous bytes per token.
-        auto output = [&](int buf, int n_out, int tok_out) {
+        auto output = [&](int n_out, int tok_out) {
             uint32_t r[32];
-            tc::tmem_ld32(tl + kColO + 64 * buf + 32 * hf, r);
+            tc::tmem_ld32(tl + kColO + 32 * hf, r);
             uint16_t *op = a.o + static_cast<size_t>(tok_out + 32 * hf) * ldv + static_cast<size_t>(h) * D + j;
             const int lim = n_out - 32 * hf;
 #pragma unroll
@@ -566,7 +585,22 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
             return true;
         };
 
+        // The Gram of chunk cc, queued by thread 0 once the conversion of chunk
+        // cc - 1 is done and the prep group has read the Gram of chunk cc - 1
+        // (so that neither still waits on the previous completion of kBarGram):
+        // it runs behind the products already queued and is complete long
+        // before the prep group needs it.
+        auto issue_gram_ahead = [&](int cc) -> bool {
+            if (!wait_bar(bars + kBarGramFree, (cc - 1) & 1, fail) ||
+                !wait_bar(bars + kBarTmaQK + cc % 3, (cc / 3) & 1, fail))
+                return false;
+            tc::fence_after_sync();
+            gram_mma<D>(tbase, sQK(cc % 3), bars + kBarGram);
+            return true;
+        };
+
         if (n_chunks > 0 && !convert(0)) failed = true;
+        if (!failed && tid == 0 && n_chunks > 1 && !issue_gram_ahead(1)) atomicExch(fail, 1);
         for (int c = 0; c < n_chunks && !failed; ++c) {
             const int s = c & 1;
             const int tok0 = t0 + c * kChunk;
@@ -587,17 +621,12 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                                        idU | tc::kIdescBmn, 1);
                     tc::mma_commit(bars + kBarA);
                     tc::mma_commit(bars + kBarWFree);
-                    const uint64_t dQ = tc::desc_k_sw128(tc::smem_u32(qk));
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        tc::mma_f16_ta(tbase + kColO + 64 * s, tbase + kColS16 + kk * 8,
-                                       dQ + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), idU, kk > 0);
                 } else {
                     atomicExch(fail, 1);
                 }
             }
             __syncwarp();
-            if (c > 0 && jv) output(prev_s, prev_n, prev_tok0);
+            if (c > 0 && jv) output(prev_n, prev_tok0);
             if (jv && okr) {  // gamma_C scales the fp32 state while the products run
                 const float gC = sGc[s];
 #pragma unroll 1
@@ -609,6 +638,21 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                     tc::tmem_st32(tl + kColS + c0, r);
                 }
             }
+            // The previous chunk's output has been read: D_O = S16^T Q~^T may start.
+            tc::fence_before_sync();
+            if (group_any(kBarChain, !okr || *vfail)) {
+                failed = true;
+                break;
+            }
+            if (tid == 0) {
+                tc::fence_after_sync();
+                const uint64_t dQ = tc::desc_k_sw128(tc::smem_u32(qk));
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    tc::mma_f16_ta(tbase + kColO, tbase + kColS16 + kk * 8,
+                                   dQ + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), idU, kk > 0);
+            }
+            __syncwarp();
             const bool oka = __all_sync(0xffffffffu, okr && wait_bar(bars + kBarA, c & 1, fail));
             tc::fence_after_sync();
 
@@ -644,7 +688,7 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                     tc::mma_f16_ta(tbase + kColS, tbase + kColUd16 + kk * 8, dK + kk * (2048 >> 4), idS, 1);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    tc::mma_f16_ta(tbase + kColO + 64 * s, tbase + kColU16 + kk * 8, dPs + kk * 2, idU, 1);
+                    tc::mma_f16_ta(tbase + kColO, tbase + kColU16 + kk * 8, dPs + kk * 2, idU, 1);
                 tc::mma_commit(bars + kBarC);
                 tc::mma_commit(bars + kBarQKFree);
             }
@@ -653,6 +697,7 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                 failed = true;
                 break;
             }
+            if (tid == 0 && c + 2 < n_chunks && !issue_gram_ahead(c + 2)) atomicExch(fail, 1);
             const bool okc = __all_sync(0xffffffffu, wait_bar(bars + kBarC, c & 1, fail));
             tc::fence_after_sync();
 
@@ -702,9 +747,8 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
             }
             prev_n = n;
             prev_tok0 = tok0;
-            prev_s = s;
         }
-        if (!failed && n_chunks > 0 && jv) output(prev_s, prev_n, prev_tok0);
+        if (!failed && n_chunks > 0 && jv) output(prev_n, prev_tok0);
         if (failed && tid == 0) {
             report(a.dev_status, GDN_DEV_TIMEOUT);
             atomicExch(fail, 1);
@@ -754,22 +798,6 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
             for (int kb = 0; kb < kKB; ++kb) tma_load_2d(tile + kb * 8192, &L.tm_v, h * D + kb * 64, t0 + cc * kChunk, tb);
             v_issued = cc;
         };
-        // Gram [Q;K] K^T of chunk cc in bf16, straight from its TMA tile, into the
-        // prep columns (issued as soon as the previous chunk's -W^T has been read
-        // out of them).
-        auto issue_gram = [&](int cc) -> bool {
-            if (!wait_bar(bars + kBarTmaQK + cc % 3, (cc / 3) & 1, fail)) return false;
-            tc::fence_after_sync();
-            const uint64_t dQK = tc::desc_k_sw128(tc::smem_u32(sQK(cc % 3)));
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                tc::mma_f16(tbase + kColPrep, dQK + off, dQK + off + (8192 >> 4),
-                            tc::idesc_f16_f32acc(128, 64) | tc::kIdescBf16, kk > 0);
-            }
-            tc::mma_commit(bars + kBarGram);
-            return true;
-        };
         if (n_chunks > 0) {
             if (pid == 0) {
                 issue_qk(0);
@@ -778,7 +806,13 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                     issue_qk(1);
                     issue_v(1);
                 }
-                issue_gram(0);
+                // the first chunk's Gram (the chain group queues the later ones)
+                if (wait_bar(bars + kBarTmaQK, 0, fail)) {
+                    tc::fence_after_sync();
+                    gram_mma<D>(tbase, sQK(0), bars + kBarGram);
+                } else {
+                    atomicExch(fail, 1);
+                }
             }
             load_gb(0);
         }
@@ -844,7 +878,7 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                 // f = beta_r (A rows) is folded into the exponent when positive.
                 // Only the warps on a diagonal 32 x 32 block apply the mask.
                 uint32_t x[32];
-                tc::tmem_ld32(tl + kColPrep + 32 * hf, x);
+                tc::tmem_ld32(tl + kColGram + 32 * hf, x);
                 const int r = p & 63;
                 const bool isA = p >= 64;
                 const float br = isA ? sBeta[r] : 1.f;
@@ -894,6 +928,7 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                 failed = true;
                 break;
             }
+            if (pid == 0) mbar_arrive(bars + kBarGramFree);  // the chain may issue the next Gram
 
             // ---- Q4: diagonal blocks and level 1 (warps 8, 9) ----------------------------
             bool okv = true;
@@ -1051,7 +1086,7 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
             // ---- hand over: q/k copies of chunk c + 2 into the slot of chunk c - 1 ----
             if (pid == 0) {
                 mbar_arrive(bars + kBarReady + s);
-                bool okq = c + 1 >= n_chunks || issue_gram(c + 1);
+                bool okq = true;
                 // The chain is done with chunk c - 1 (q/k slot, P~ and decay stage)
                 // before the next chunk's preparation reuses them.
                 if (okq && c >= 1) okq = wait_bar(bars + kBarQKFree, (c - 1) & 1, fail);
