@@ -764,7 +764,7 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
         const int p = pid & 127, hf = pid >> 7;
         bool failed = false;
         int c_done = 0;                          // chunks whose loads the loop consumed
-        int qk_issued = -1, v_issued = -1;       // highest chunk whose copies were issued (pid 0)
+        int qk_issued = -1, v_issued = -1;       // highest chunk whose copies this thread issued (pid 0, 64)
         constexpr uint32_t kQKTx = 2u * kKB * 8192u, kVTx = kKB * 8192u;
         // g and beta of a chunk, tokens 2l and 2l + 1 in lane l of warp 10 (zeros
         // past the sequence end), loaded a chunk ahead.
@@ -932,14 +932,15 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
 
             // ---- Q4: diagonal blocks and level 1 (warps 8, 9) ----------------------------
             bool okv = true;
-            if (pid < 64) {
+            if (pid == 64 && c >= 1) {
                 // T'' and the v slot of chunk c - 1 are free once the chain's U'^T
                 // product of that chunk is done (long before this point): the v
-                // copies of chunk c + 1 go there, a whole chunk ahead.
-                if (pid == 0 && c >= 1) {
-                    okv = wait_bar(bars + kBarTFree, (c - 1) & 1, fail);
-                    if (okv && c + 1 < n_chunks) issue_v(c + 1);
-                }
+                // copies of chunk c + 1 go there, a whole chunk ahead (issued by
+                // warp 10, idle in this phase).
+                okv = wait_bar(bars + kBarTFree, (c - 1) & 1, fail);
+                if (okv && c + 1 < n_chunks) issue_v(c + 1);
+            }
+            if (pid < 64) {
                 float xd[16];
                 invert_diag_solve(sM, pid, xd);
                 __syncwarp();
@@ -1105,6 +1106,8 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
             for (int cc = c_done; cc <= qk_issued; ++cc) drain_bar(bars + kBarTmaQK + cc % 3, (cc / 3) & 1);
             for (int cc = c_done; cc <= v_issued; ++cc) drain_bar(bars + kBarTmaV + (cc & 1), (cc / 2) & 1);
         }
+        if (pid == 64)  // the v copies this thread issued
+            for (int cc = c_done; cc <= v_issued; ++cc) drain_bar(bars + kBarTmaV + (cc & 1), (cc / 2) & 1);
     }
 
     tc::fence_before_sync();
