@@ -178,3 +178,37 @@ def test_I4_run_to_run_determinism(gdn):
         outs.append((o, c))
     assert torch.equal(_bits(outs[0][0]), _bits(outs[1][0]))
     assert torch.equal(_bits(outs[0][1]), _bits(outs[1][1]))
+
+
+@pytest.mark.parametrize("which", ["gva_d128", "tiny_d64"])
+def test_I4_prefill_repeatable_under_concurrent_load(gdn, which):
+    """The prefill kernel's two warp groups hand work to each other through
+    shared memory, TMEM and barriers; a missing barrier shows up as results
+    that change with timing.  Six runs of the same prefill (with emission),
+    three of them while decode launches on another stream compete for the
+    SMs, must give the same o, final states and emitted states bit for bit."""
+    if which == "gva_d128":
+        b = gi.prefill_qwen3next_gva(0)["prefill"]
+    else:
+        b = gi.token_batch([64, 100, 1, 130, 700], 4, 4, 64, 17)
+    rows = 256
+    dec = gi.token_batch([1] * rows, 16, 16, 128, 3, init_state=True)
+    dcache = gu.empty_cache(rows, 16, 128)
+    dx = gu.batch_to_device(dec)
+    dsrc = torch.arange(rows, dtype=torch.int32, device="cuda")
+    do = torch.empty((rows, 16, 128), dtype=torch.bfloat16, device="cuda")
+    side = torch.cuda.Stream()
+    ref = None
+    for run in range(6):
+        if run % 2:
+            with torch.cuda.stream(side):
+                for _ in range(4):
+                    gdn.gdn_decode_packed(dx["q"], dx["k"], dx["v"], dx["g"], dx["beta"], dcache, dsrc, do)
+        res = _prefill(gdn, b, E=1)
+        torch.cuda.synchronize()
+        if ref is None:
+            ref = res
+            continue
+        assert torch.equal(_bits(res[0]), _bits(ref[0])), run
+        assert torch.equal(res[1], ref[1]), run
+        assert torch.equal(res[2], ref[2]), run
