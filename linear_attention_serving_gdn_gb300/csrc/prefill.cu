@@ -678,7 +678,7 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                 break;
             }
 
-            // ---- P2: D_S += (diag(dec) U)^T K, D_O += U^T P~^T; preset next U'^T --
+            // ---- P2: D_S += (diag(dec) U)^T K, D_O += U^T P~^T ------------------------
             if (tid == 0) {
                 tc::fence_after_sync();
                 const uint64_t dK = tc::desc_mn_sw128(tc::smem_u32(qk + 8192), kLboK);
