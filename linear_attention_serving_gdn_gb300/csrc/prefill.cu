@@ -75,6 +75,7 @@ constexpr int kThreads = 512;  // chain group + prep group
 constexpr int kGroup = 256;
 constexpr int kBarChain = 1;  // named barrier ids (0 is __syncthreads)
 constexpr int kBarPrep = 2;
+constexpr int kBarPairL1 = 3;  // 3, 4: warps 8 + 12, 9 + 13 (first inverse level)
 // Limit of every handshake wait between the groups, in SM clock cycles
 // (~1 s by default); a build may shorten it to exercise the failure path.
 constexpr long long kWaitCycles = GDN_WAIT_CYCLES;
@@ -336,28 +337,32 @@ __device__ __forceinline__ void block_mac(float4 &acc, const float *X, const flo
         fma4(acc, x4.w, *reinterpret_cast<const float4 *>(y + 3 * LDY));
     }
 }
-// First doubling level by one warp (the warp that solved diagonal blocks
-// B-1 and B): T_{B,B-1} = -T_BB (A_{B,B-1} T_{B-1,B-1}), in fp32.  Lane =
-// (row i = lane / 2, columns 8 (lane % 2) .. + 7).
+// First doubling level: T_{B,B-1} = -T_BB (A_{B,B-1} T_{B-1,B-1}) in fp32,
+// lane = (row i = lane / 2, column group cq of four columns).
+// Half of it (columns 4 cq .. 4 cq + 3, cq = 2 (lane % 2) + u) by one warp,
+// the other half (the other u) by a second warp, with barrier `bar` (64
+// threads) around each step: before the first, the diagonal blocks are
+// stored; between the two, both warps have read all of A_{B,B-1}, which the
+// second step overwrites with T_{B,B-1}; after the second, all of T_{B,B-1}
+// is in place.  Each warp reads back only its own part of Y.
+__device__ __forceinline__ void pair_sync(int id) {  // two warps
+    asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
+
 template <int B>
-__device__ __forceinline__ void level1_warp(float *M, float *Wb, int lane) {
-    const int i = (lane >> 1) & 15, h = lane & 1;
+__device__ __forceinline__ void level1_half(float *M, float *Wb, int lane, int u, int bar) {
+    const int i = (lane >> 1) & 15, cq = 2 * (lane & 1) + u;
     float *Y = Wb + (B == 3 ? 256 : 0);
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        block_mac<kLdM, kLdM>(acc, M + (B * 16) * kLdM + (B - 1) * 16, M + ((B - 1) * 16) * kLdM + (B - 1) * 16, i,
-                              2 * h + u);
-        *reinterpret_cast<float4 *>(Y + i * 16 + 4 * (2 * h + u)) = acc;
-    }
-    __syncwarp();
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        block_mac<kLdM, 16>(acc, M + (B * 16) * kLdM + B * 16, Y, i, 2 * h + u);
-        *reinterpret_cast<float4 *>(M + (B * 16 + i) * kLdM + (B - 1) * 16 + 4 * (2 * h + u)) =
-            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-    }
+    pair_sync(bar);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    block_mac<kLdM, kLdM>(acc, M + (B * 16) * kLdM + (B - 1) * 16, M + ((B - 1) * 16) * kLdM + (B - 1) * 16, i, cq);
+    *reinterpret_cast<float4 *>(Y + i * 16 + 4 * cq) = acc;
+    pair_sync(bar);
+    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    block_mac<kLdM, 16>(acc, M + (B * 16) * kLdM + B * 16, Y, i, cq);
+    *reinterpret_cast<float4 *>(M + (B * 16 + i) * kLdM + (B - 1) * 16 + 4 * cq) =
+        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    pair_sync(bar);
 }
 
 // Writes 16 fp32 values v (columns 16q .. 16q + 15 of row t) as T'' = v beta
@@ -540,11 +545,11 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
         // Output of a finished chunk, o_t = (Q~ S + P~ U)_t, tokens 32 hf ..
         // 32 hf + 31 of value column j, one bf16 per (token, j): a warp's 32
         // lanes store 64 contiguous bytes per token.
-        auto output = [&](int n_out, int tok_out) {
+        auto output = [&](int n_out, int tok_out, int hh) {
             uint32_t r[32];
-            tc::tmem_ld32(tl + kColO + 32 * hf, r);
-            uint16_t *op = a.o + static_cast<size_t>(tok_out + 32 * hf) * ldv + static_cast<size_t>(h) * D + j;
-            const int lim = n_out - 32 * hf;
+            tc::tmem_ld32(tl + kColO + 32 * hh, r);
+            uint16_t *op = a.o + static_cast<size_t>(tok_out + 32 * hh) * ldv + static_cast<size_t>(h) * D + j;
+            const int lim = n_out - 32 * hh;
 #pragma unroll
             for (int i = 0; i < 32; ++i, op += ldv)
                 if (i < lim) *op = float_to_bf16_bits(__uint_as_float(r[i]));
@@ -626,11 +631,15 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                 }
             }
             __syncwarp();
-            if (c > 0 && jv) output(prev_n, prev_tok0);
-            if (jv && okr) {  // gamma_C scales the fp32 state while the products run
+            // Warp 0 issues the products; warp 4 (same TMEM lanes) does both halves of
+            // their lanes' output and state scaling.
+            const int h_lo = warp == 4 ? 0 : hf, h_hi = warp == 4 ? 2 : hf + 1;
+            if (c > 0 && jv && warp != 0)
+                for (int hh = h_lo; hh < h_hi; ++hh) output(prev_n, prev_tok0, hh);
+            if (jv && okr && warp != 0) {  // gamma_C scales the fp32 state while the products run
                 const float gC = sGc[s];
 #pragma unroll 1
-                for (int c0 = hf * kHalf; c0 < (hf + 1) * kHalf; c0 += 32) {
+                for (int c0 = h_lo * kHalf; c0 < h_hi * kHalf; c0 += 32) {
                     uint32_t r[32];
                     tc::tmem_ld32(tl + kColS + c0, r);
 #pragma unroll
@@ -678,7 +687,7 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                 break;
             }
 
-            // ---- P2: D_S += (diag(dec) U)^T K, D_O += U^T P~^T ------------------------
+            // ---- P2: D_S += (diag(dec) U)^T K, D_O += U^T P~^T; preset next U'^T --
             if (tid == 0) {
                 tc::fence_after_sync();
                 const uint64_t dK = tc::desc_mn_sw128(tc::smem_u32(qk + 8192), kLboK);
@@ -748,7 +757,7 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
             prev_n = n;
             prev_tok0 = tok0;
         }
-        if (!failed && n_chunks > 0 && jv) output(prev_n, prev_tok0);
+        if (!failed && n_chunks > 0 && jv) output(prev_n, prev_tok0, hf);
         if (failed && tid == 0) {
             report(a.dev_status, GDN_DEV_TIMEOUT);
             atomicExch(fail, 1);
@@ -930,7 +939,7 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
             }
             if (pid == 0) mbar_arrive(bars + kBarGramFree);  // the chain may issue the next Gram
 
-            // ---- Q4: diagonal blocks and level 1 (warps 8, 9) ----------------------------
+            // ---- Q4: diagonal blocks (warps 8, 9) and level 1 (warps 8, 9, 12, 13) -------
             bool okv = true;
             if (pid == 64 && c >= 1) {
                 // T'' and the v slot of chunk c - 1 are free once the chain's U'^T
@@ -945,10 +954,9 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                 invert_diag_solve(sM, pid, xd);
                 __syncwarp();
                 invert_diag_store(sM, pid, xd);
-                __syncwarp();
-                if (pid < 32) level1_warp<1>(sM, sWb, pid & 31);
-                else level1_warp<3>(sM, sWb, pid & 31);
-                __syncwarp();
+                // level 1 in two halves: this warp and warp 12 (or 13)
+                if (pid < 32) level1_half<1>(sM, sWb, pid & 31, 0, kBarPairL1);
+                else level1_half<3>(sM, sWb, pid & 31, 0, kBarPairL1 + 1);
                 // Level-2 operands: T_top (rows 0..31, cols 0..31) as MN-major B
                 // (warp 8), T_bot (rows 32..63, cols 32..63) as K-major A (warp 9);
                 // the blocks above the diagonal blocks are zero.
@@ -959,6 +967,9 @@ prefill_chain_kernel(const __grid_constant__ PrefillLaunch L) {
                 for (int i = 0; i < 32; ++i)
                     x[i] = (i >= 16 && r < 16) ? 0u : __float_as_uint(sM[(rb + r) * kLdM + rb + i]);
                 store_row32_f16(pid < 32 ? sL2B1 : sL2A2, r, x, 1.f, pid >= 32);
+            } else if (pid >= 128 && pid < 192) {  // warps 12, 13: the other half of level 1
+                if (pid < 160) level1_half<1>(sM, sWb, pid & 31, 1, kBarPairL1);
+                else level1_half<3>(sM, sWb, pid & 31, 1, kBarPairL1 + 1);
             }
             tc::fence_proxy_async_smem();
             tc::fence_before_sync();
