@@ -26,7 +26,7 @@ def gdn():
     return m
 
 
-@pytest.mark.parametrize("case", range(12))
+@pytest.mark.parametrize("case", range(40))
 def test_random_mixed_step_vs_oracle(gdn, case):
     rng = np.random.default_rng(1000 + case)
     h_k, h_v, d = HEADS[case % len(HEADS)]
