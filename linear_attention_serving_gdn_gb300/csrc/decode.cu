@@ -274,14 +274,184 @@ decode_multi_kernel(const DecodeMultiArgs a) {
     }
 }
 
+// Multi-token decode for rows of at most kPfTokens tokens: as decode_multi_kernel,
+// but each warp also holds its next item in shared memory: while the tokens of
+// the current item run from registers, the next item's 16 state rows (8 KB) and
+// token inputs are already being copied into the warp's buffers by cp.async, so
+// an item starts with shared-memory loads instead of a memory round trip.  The
+// token inputs are double-buffered; the state buffer is single: each lane copies
+// into it only the pieces it reads back itself, and only after those reads have
+// returned their data.
+constexpr int kPfTokens = 4;
+template <int D>
+struct MultiPf {
+    using MS = MultiStage<D>;
+    static constexpr int kState = kMultiRows * D * 4;   // one item's state rows, fp32
+    static constexpr int kStage = kPfTokens * MS::kBytes;
+    static constexpr int kWarp = kState + 2 * kStage;   // per warp
+    static constexpr int kBlock = (kMultiThreads / 32) * kWarp;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kMultiThreads, 2)
+decode_multi_pf_kernel(const DecodeMultiArgs a) {
+    constexpr int V4 = D / 32;
+    constexpr int kItemsPerHead = D / kMultiRows;
+    using MS = MultiStage<D>;
+    using PF = MultiPf<D>;
+    extern __shared__ __align__(128) uint8_t pf_smem[];
+    const int lane = threadIdx.x & 31;
+    const int sub = lane >> 3;
+    const int l8 = lane & 7;
+    const int T = a.tokens_per_row;
+    const int64_t n_items = static_cast<int64_t>(a.num_rows) * a.h_v * kItemsPerHead;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int group = a.h_v / a.h_k;
+    uint8_t *wbuf = pf_smem + (threadIdx.x >> 5) * PF::kWarp;
+    uint8_t *sstate = wbuf;
+
+    // Copies of item iit (one commit group): the lane's own state pieces (rows
+    // 4 i + sub, float4 columns l8 + 8 m) and the item's token inputs.
+    auto issue = [&](int64_t iit, uint8_t *stage) {
+        const int row0_ = static_cast<int>(iit % kItemsPerHead) * kMultiRows;
+        const int64_t rh_ = iit / kItemsPerHead;
+        const int h_ = static_cast<int>(rh_ % a.h_v), r_ = static_cast<int>(rh_ / a.h_v), kh_ = h_ / group;
+        const int src_ = a.src_slot[r_];
+        if (src_ >= 0 && src_ < a.num_slots) {
+            const float *sp = a.state + ((static_cast<size_t>(src_) * a.h_v + h_) * D + row0_) * D;
+#pragma unroll
+            for (int i = 0; i < kMultiGroups; ++i) {
+#pragma unroll
+                for (int m = 0; m < V4; ++m) {
+                    const int off = (i * kRowsPerGroup + sub) * D + 4 * (l8 + 8 * m);
+                    cp_async16(sstate + 4 * off, sp + off);
+                }
+            }
+        }
+        for (int t = 0; t < T; ++t) {
+            uint8_t *st = stage + t * MS::kBytes;
+            const size_t tok = static_cast<size_t>(r_) * T + t;
+            const size_t gh = tok * a.h_v + h_;
+            if (lane < D / 8) {
+                cp_async16(st + MS::kK + 16 * lane, a.k + (tok * a.h_k + kh_) * D + 8 * lane);
+                cp_async16(st + MS::kQ + 16 * lane, a.q + (tok * a.h_k + kh_) * D + 8 * lane);
+            } else if (lane < D / 8 + kMultiRows / 8) {
+                const int pc = lane - D / 8;
+                cp_async16(st + MS::kV + 16 * pc, a.v + gh * D + row0_ + 8 * pc);
+            } else if (lane == 30) {
+                cp_async4(st + MS::kG, a.g + gh);
+            } else if (lane == 31) {
+                cp_async4(st + MS::kB, a.beta + gh);
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+
+    const int64_t first = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (first < n_items) issue(first, wbuf + PF::kState);
+    int cur = 0;
+    for (int64_t it = first; it < n_items; it += nwarps, cur ^= 1) {
+        uint8_t *stage_buf = wbuf + PF::kState + cur * PF::kStage;
+        asm volatile("cp.async.wait_group 0;" ::: "memory");  // this item's copies have landed
+        __syncwarp();
+        const int blk = static_cast<int>(it % kItemsPerHead);
+        const int64_t rh = it / kItemsPerHead;
+        const int h = static_cast<int>(rh % a.h_v);
+        const int r = static_cast<int>(rh / a.h_v);
+        const int row0 = blk * kMultiRows;
+        const int src = a.src_slot[r];
+        const bool valid = src >= 0 && src < a.num_slots;
+        float4 s[kMultiGroups][V4];
+        if (valid) {
+#pragma unroll
+            for (int i = 0; i < kMultiGroups; ++i) {
+#pragma unroll
+                for (int m = 0; m < V4; ++m) {
+                    s[i][m] = *reinterpret_cast<const float4 *>(
+                        sstate + 4 * ((i * kRowsPerGroup + sub) * D + 4 * (l8 + 8 * m)));
+                    // the read has returned its data before the next item's copy
+                    // into the same piece is issued below
+                    asm volatile("" ::"f"(s[i][m].x), "f"(s[i][m].y), "f"(s[i][m].z), "f"(s[i][m].w) : "memory");
+                }
+            }
+        }
+        // The next item's copies: its state into the state buffer (this lane's
+        // pieces, already read above), its token inputs into the other stage.
+        if (it + nwarps < n_items)
+            issue(it + nwarps, wbuf + PF::kState + (cur ^ 1) * PF::kStage);
+        if (!valid) {
+            if (src >= 0) report(a.dev_status, GDN_DEV_BAD_SLOT);
+            for (int t = 0; t < T; ++t) {
+                uint16_t *orow = a.o + ((static_cast<size_t>(r) * T + t) * a.h_v + h) * D;
+                if (lane < kMultiRows) orow[row0 + lane] = 0;
+            }
+        } else {
+            for (int t = 0; t < T; ++t) {
+                const size_t tok = static_cast<size_t>(r) * T + t;
+                float kk[V4 * 4], qq[V4 * 4];
+                const size_t gh = tok * a.h_v + h;
+                const uint8_t *st = stage_buf + t * MS::kBytes;
+                load_bf16_slice<V4>(reinterpret_cast<const uint16_t *>(st + MS::kK), l8, kk);
+                load_bf16_slice<V4>(reinterpret_cast<const uint16_t *>(st + MS::kQ), l8, qq);
+                const float alpha = expf(*reinterpret_cast<const float *>(st + MS::kG));
+                const float beta = *reinterpret_cast<const float *>(st + MS::kB);
+                const uint16_t *vrow = reinterpret_cast<const uint16_t *>(st + MS::kV) - row0;
+                const float kq = octet_dot<V4>(kk, qq);
+                uint16_t *orow = a.o + gh * D;
+                int dst = -1;
+                if (a.dst_slots) {
+                    dst = a.dst_slots[tok];
+                    if (dst >= a.num_slots) {
+                        report(a.dev_status, GDN_DEV_BAD_SLOT);
+                        dst = -1;
+                    }
+                } else if (t == T - 1) {
+                    dst = src;
+                }
+                float *dp = dst >= 0 ? a.state + (static_cast<size_t>(dst) * a.h_v + h) * D * D : nullptr;
+#pragma unroll
+                for (int i = 0; i < kMultiGroups; ++i) {
+                    const int j = row0 + i * kRowsPerGroup + sub;
+                    const float vj = bf16_bits_to_float(vrow[j]);
+                    const float oj = update_row<V4>(s[i], kk, qq, alpha, beta, vj, kq, a.scale);
+                    if (dp) {
+#pragma unroll
+                        for (int m = 0; m < V4; ++m)
+                            __stcs(reinterpret_cast<float4 *>(dp + static_cast<size_t>(j) * D + 4 * (l8 + 8 * m)),
+                                   s[i][m]);
+                    }
+                    if (l8 == 0) orow[j] = float_to_bf16_bits(oj);
+                }
+            }
+        }
+        __syncwarp();  // every lane is done with this stage before it is refilled
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");  // nothing in flight at exit
+}
+
 template <int D>
 cudaError_t launch_decode_multi_d(const DecodeMultiArgs &a, cudaStream_t stream) {
     static int occ[kMaxDevices] = {};
     int dev = 0, sms = 0;
     if (!current_device(&dev, &sms)) return cudaErrorInvalidDevice;
-    const int per_sm = blocks_per_sm(decode_multi_kernel<D>, kMultiThreads, dev, occ);
     const int64_t items = static_cast<int64_t>(a.num_rows) * a.h_v * (D / kMultiRows);
     const int64_t need = (items + (kMultiThreads / 32) - 1) / (kMultiThreads / 32);
+    if (a.dst_slots && a.tokens_per_row <= kPfTokens) {  // snapshots: next item prefetched into shared memory
+        static int occ_pf[kMaxDevices] = {}, set[kMaxDevices] = {};
+        constexpr int smem = MultiPf<D>::kBlock;
+        if (dev < 0 || dev >= kMaxDevices || !__atomic_load_n(&set[dev], __ATOMIC_ACQUIRE)) {
+            const cudaError_t e =
+                cudaFuncSetAttribute(decode_multi_pf_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < kMaxDevices) __atomic_store_n(&set[dev], 1, __ATOMIC_RELEASE);
+        }
+        const int per_sm = blocks_per_sm(decode_multi_pf_kernel<D>, kMultiThreads, dev, occ_pf, smem);
+        const int64_t cap = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
+        const int grid = static_cast<int>(need < cap ? need : cap);
+        decode_multi_pf_kernel<D><<<grid, kMultiThreads, smem, stream>>>(a);
+        return cudaGetLastError();
+    }
+    const int per_sm = blocks_per_sm(decode_multi_kernel<D>, kMultiThreads, dev, occ);
     const int64_t cap = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
     const int grid = static_cast<int>(need < cap ? need : cap);
     decode_multi_kernel<D><<<grid, kMultiThreads, 0, stream>>>(a);

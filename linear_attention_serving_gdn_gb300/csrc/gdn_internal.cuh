@@ -81,14 +81,14 @@ struct PrefillArgs {
 constexpr int kMaxDevices = 64;
 // Current device and its SM count; false if a query failed.
 bool current_device(int *dev, int *sms);
-// Blocks per SM of `kernel` at `threads` threads and no dynamic shared
-// memory on device `dev`, cached in `cache` (one slot per device).
+// Blocks per SM of `kernel` at `threads` threads and `dyn_smem` bytes of
+// dynamic shared memory on device `dev`, cached in `cache` (one slot per device).
 template <typename Kernel>
-int blocks_per_sm(Kernel kernel, int threads, int dev, int (&cache)[kMaxDevices]) {
+int blocks_per_sm(Kernel kernel, int threads, int dev, int (&cache)[kMaxDevices], size_t dyn_smem = 0) {
     if (dev >= 0 && dev < kMaxDevices && __atomic_load_n(&cache[dev], __ATOMIC_ACQUIRE) > 0)
         return cache[dev];
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) n = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, dyn_smem) != cudaSuccess || n < 1) n = 1;
     if (dev >= 0 && dev < kMaxDevices) __atomic_store_n(&cache[dev], n, __ATOMIC_RELEASE);
     return n;
 }
