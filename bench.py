@@ -481,7 +481,9 @@ def prep_case(torch, gdn, dev, peaks, T=131072, h_k=16, h_v=32, reps=20):
 
 def decode_latency_case(torch, gdn, dev, rows_list=(1, 8, 64, 256), iters=200):
     """Decode step latency per padded batch size: eager C-ABI calls from
-    Python versus replay of a CUDA graph holding one step (H=16, d=128)."""
+    Python (checked on every call, and prepared once with
+    prepare_decode_packed) versus replay of a CUDA graph holding one step
+    (H=16, d=128)."""
     cases = []
     for rows in rows_list:
         b = gi.token_batch([1] * rows, H, H, D, 5, init_state=True)
@@ -510,11 +512,13 @@ def decode_latency_case(torch, gdn, dev, rows_list=(1, 8, 64, 256), iters=200):
             return a.elapsed_time(z) * 1e3 / iters
 
         eager = per_step_us(call)
+        prepared = per_step_us(gdn.prepare_decode_packed(q, k, v, g, beta, cache, src_t, o))
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             call()
         replay = per_step_us(graph.replay)
-        cases.append({"rows": rows, "eager_us_per_step": eager, "graph_us_per_step": replay,
+        cases.append({"rows": rows, "eager_us_per_step": eager, "prepared_us_per_step": prepared,
+                      "graph_us_per_step": replay,
                       "graph_rows_per_s": rows / (replay * 1e-6)})
     return {"workload": "decode_latency_h16_d128", "cases": cases}
 

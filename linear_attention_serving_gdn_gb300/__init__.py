@@ -24,7 +24,7 @@ import torch
 from . import _build
 
 __all__ = [
-    "GdnError", "load_library", "library_path",
+    "GdnError", "load_library", "library_path", "prepare_decode_packed",
     "gdn_decode_packed", "gdn_decode_packed_raw", "gdn_prep_inputs", "gdn_decode_multi",
     "gdn_prefill_varlen", "gdn_prefill_varlen_apc", "gdn_mixed_step", "gdn_prefill_num_emits", "gdn_prefill_emit_offsets", "gdn_align_block_size",
     "gdn_floor_prefix_hit", "gdn_grid_emit_every_chunks", "gdn_status_string",
@@ -207,6 +207,49 @@ def gdn_decode_packed(q, k, v, g, beta, state, src_slot, o, dst_slot=None, dev_s
                                  _ptr(beta), _ptr(state), state.shape[0], _ptr(src_slot),
                                  _ptr(dst_slot), _ptr(o), _ptr(dev_status), _stream(stream)),
            "gdn_decode_packed")
+
+
+class _PreparedCall:
+    """A C-ABI call whose arguments were checked and marshalled once: calling
+    it issues the same call again on the same buffers (whatever they hold by
+    then) and the same stream, with no per-call checks in Python.  The
+    buffers must stay alive and keep their shapes and storage."""
+
+    def __init__(self, fn, args, name, keep):
+        self._fn, self._args, self._name, self._keep = fn, args, name, keep
+
+    def __call__(self) -> None:
+        status = self._fn(*self._args)
+        if status != GDN_OK:
+            raise GdnError(status, self._name)
+
+
+def prepare_decode_packed(q, k, v, g, beta, state, src_slot, o, dst_slot=None, dev_status=None,
+                          scale: float = 1.0, stream=None) -> _PreparedCall:
+    """``gdn_decode_packed`` on fixed buffers, checked once: returns a callable
+    that repeats the call (a serving loop refills q, k, v, g, beta and the
+    slot lists in place between steps).  The stream is the one given, or the
+    current stream at preparation."""
+    lib = load_library()
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    q, k, v = _dev(q, "q", bf, 3), _dev(k, "k", bf, 3), _dev(v, "v", bf, 3)
+    g, beta = _dev(g, "g", f32, 2), _dev(beta, "beta", f32, 2)
+    state = _dev(state, "state", f32, 4)
+    src_slot = _dev(src_slot, "src_slot", i32, 1)
+    dst_slot = _dev(dst_slot, "dst_slot", i32, 1, optional=True)
+    o = _dev(o, "o", bf, 3)
+    dev_status = _dev(dev_status, "dev_status", i32, optional=True)
+    rows = q.shape[0]
+    if not (k.shape == q.shape and v.shape[0] == rows and o.shape == v.shape
+            and g.shape == (rows, v.shape[1]) and beta.shape == g.shape
+            and src_slot.shape[0] == rows and (dst_slot is None or dst_slot.shape[0] == rows)
+            and state.shape[1:] == (v.shape[1], v.shape[2], q.shape[2])):
+        raise ValueError("inconsistent decode shapes")
+    d = _dims(q, v, scale)
+    args = (ctypes.byref(d), rows, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+            state.shape[0], _ptr(src_slot), _ptr(dst_slot), _ptr(o), _ptr(dev_status), _stream(stream))
+    keep = (d, q, k, v, g, beta, state, src_slot, dst_slot, o, dev_status)
+    return _PreparedCall(lib.gdn_decode_packed, args, "gdn_decode_packed", keep)
 
 
 def gdn_prep_inputs(q_raw, k_raw, a, b, A_log, dt_bias, q, k, g, beta, eps: float = 1e-6,

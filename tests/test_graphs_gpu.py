@@ -188,3 +188,30 @@ def test_end_to_end_step_in_row_groups_matches_single_call(gdn, parts):
     assert (i1, d1) == (i2, d2)
     assert torch.equal(_bits(o1), _bits(o2))
     assert torch.equal(s1, s2)
+
+
+def test_prepared_decode_call_matches_checked_call(gdn):
+    """prepare_decode_packed: the buffers checked once, then three steps with
+    new inputs copied into them in place; outputs and states equal the
+    checked call's bit for bit."""
+    rows, h, d, steps = 24, 16, 128, 3
+    seqs = gi.token_batch([steps] * rows, h, h, d, seed=12, init_state=True)
+    src, n_slots = gi.slots(rows, 12)
+    cache_c = gu.empty_cache(n_slots, h, d)
+    gu.put_states(cache_c, src, seqs.init_state)
+    cache_p = cache_c.clone()
+    src_t = torch.from_numpy(src).cuda()
+    static = {k: torch.zeros_like(v) for k, v in _step_inputs(seqs, 0).items()}
+    o_p = torch.empty((rows, h, d), dtype=torch.bfloat16, device="cuda")
+    step = gdn.prepare_decode_packed(static["q"], static["k"], static["v"], static["g"], static["beta"],
+                                     cache_p, src_t, o_p)
+    for t in range(steps):
+        x = _step_inputs(seqs, t)
+        for n in static:
+            static[n].copy_(x[n])
+        step()
+        o_c = torch.empty_like(o_p)
+        gdn.gdn_decode_packed(x["q"], x["k"], x["v"], x["g"], x["beta"], cache_c, src_t, o_c)
+        torch.cuda.synchronize()
+        assert torch.equal(_bits(o_p), _bits(o_c)), t
+        assert torch.equal(cache_p, cache_c), t
