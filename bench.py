@@ -383,20 +383,12 @@ def mixed_case(torch, gdn, dev, reps, peaks):
     def call():
         gdn.gdn_mixed_step(nd, q, k, v, g, beta, cu, cu_h, cache, slots[:nd], o, pre_dst_slot=slots[nd:])
 
-    s_dec, s_pre = torch.cuda.Stream(), torch.cuda.Stream()
+    aux, fork, join = torch.cuda.Stream(), torch.cuda.Event(), torch.cuda.Event()
 
     def colaunch():
-        # decode rows and prefills on two streams at once (same kernels)
-        main = torch.cuda.current_stream()
-        s_dec.wait_stream(main)
-        s_pre.wait_stream(main)
-        with torch.cuda.stream(s_dec):
-            gdn.gdn_decode_packed(q[:nd], k[:nd], v[:nd], g[:nd], beta[:nd], cache, slots[:nd], o[:nd])
-        with torch.cuda.stream(s_pre):
-            gdn.gdn_prefill_varlen(q[nd:], k[nd:], v[nd:], g[nd:], beta[nd:], cu, cu_h, o[nd:], state=cache,
-                                   dst_slot=slots[nd:])
-        main.wait_stream(s_dec)
-        main.wait_stream(s_pre)
+        # the same step with the decode rows on a second stream beside the prefill
+        gdn.gdn_mixed_step_colaunch(nd, q, k, v, g, beta, cu, cu_h, cache, slots[:nd], o, aux, fork, join,
+                                    pre_dst_slot=slots[nd:])
 
     ms, clocks = timed_median(torch, call, reps=reps)
     ms2, _ = timed_median(torch, colaunch, reps=reps)

@@ -321,6 +321,38 @@ gdn_status_t gdn_mixed_step(const gdn_dims_t *dims, int32_t num_decodes, int32_t
                             void *workspace, size_t workspace_bytes,
                             int32_t *dev_status, void *stream);
 
+/*
+ * The same step with its two halves running at the same time: the prefill
+ * on `stream`, the decode rows on `aux_stream` (cudaStream_t), so that the
+ * decode blocks fill the SMs the prefill chains leave free.  Same page and
+ * sections as gdn_mixed_step; the decode rows still run the decode kernel,
+ * so their results are bitwise identical to gdn_mixed_step's.
+ *
+ *   fork_event, join_event: caller-created cudaEvent_t (no timing needed).
+ *   The call records fork_event on `stream` and makes aux_stream wait for
+ *   it, launches both halves, records join_event on aux_stream and makes
+ *   `stream` wait for it: work issued on `stream` after the call sees both
+ *   halves finished.  All of it can be captured in a CUDA graph.
+ *   The decode half's slots must be disjoint from the prefill half's
+ *   (the halves run concurrently).  aux_stream == NULL runs the step as
+ *   gdn_mixed_step does, on `stream` alone; otherwise both events are
+ *   required (GDN_ERR_INVALID_ARG).  Both halves are validated before
+ *   anything is recorded or launched.
+ */
+gdn_status_t gdn_mixed_step_colaunch(const gdn_dims_t *dims, int32_t num_decodes, int32_t num_prefills,
+                                     const int32_t *cu_seqlens_p, const int32_t *cu_seqlens_p_host,
+                                     const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                                     const float *g, const float *beta,
+                                     float *state, int64_t num_slots,
+                                     const int32_t *dec_src_slot, const int32_t *dec_dst_slot,
+                                     const int32_t *pre_src_slot, const int32_t *pre_dst_slot,
+                                     gdn_bf16 *o,
+                                     float *chunk_states, int32_t emit_every_chunks,
+                                     int64_t chunk_states_capacity,
+                                     void *workspace, size_t workspace_bytes,
+                                     int32_t *dev_status, void *stream,
+                                     void *aux_stream, void *fork_event, void *join_event);
+
 /* ---- host-only helpers (no device work) ------------------------------- */
 
 /* Total emitted states of a prefill call: sum_s floor(L_s / (64 E)); 0 when

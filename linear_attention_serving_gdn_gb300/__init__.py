@@ -26,7 +26,7 @@ from . import _build
 __all__ = [
     "GdnError", "load_library", "library_path", "prepare_decode_packed",
     "gdn_decode_packed", "gdn_decode_packed_raw", "gdn_prep_inputs", "gdn_decode_multi",
-    "gdn_prefill_varlen", "gdn_prefill_varlen_apc", "gdn_mixed_step", "gdn_prefill_num_emits", "gdn_prefill_emit_offsets", "gdn_align_block_size",
+    "gdn_prefill_varlen", "gdn_prefill_varlen_apc", "gdn_mixed_step", "gdn_mixed_step_colaunch", "gdn_prefill_num_emits", "gdn_prefill_emit_offsets", "gdn_align_block_size",
     "gdn_floor_prefix_hit", "gdn_grid_emit_every_chunks", "gdn_status_string",
     "gdn_prefill_workspace_bytes", "gdn_status_from_device",
     "EXPORTED_SYMBOLS", "GDN_DEV_BAD_SLOT", "GDN_DEV_TIMEOUT",
@@ -38,7 +38,7 @@ GDN_DEV_BAD_SLOT, GDN_DEV_TIMEOUT = 0x1, 0x2
 
 EXPORTED_SYMBOLS = (
     "gdn_decode_packed", "gdn_decode_packed_raw", "gdn_prep_inputs", "gdn_decode_multi",
-    "gdn_prefill_varlen", "gdn_prefill_varlen_apc", "gdn_mixed_step", "gdn_prefill_num_emits", "gdn_prefill_emit_offsets", "gdn_align_block_size",
+    "gdn_prefill_varlen", "gdn_prefill_varlen_apc", "gdn_mixed_step", "gdn_mixed_step_colaunch", "gdn_prefill_num_emits", "gdn_prefill_emit_offsets", "gdn_align_block_size",
     "gdn_floor_prefix_hit", "gdn_grid_emit_every_chunks", "gdn_status_string",
     "gdn_prefill_workspace_bytes", "gdn_status_from_device",
 )
@@ -100,6 +100,8 @@ def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gdn_mixed_step.restype = ctypes.c_int
     lib.gdn_mixed_step.argtypes = [ctypes.POINTER(Dims), _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
                                    _P, _I64, _P, _P, _P, _P, _P, _P, _I32, _I64, _P, _SZ, _P, _P]
+    lib.gdn_mixed_step_colaunch.restype = ctypes.c_int
+    lib.gdn_mixed_step_colaunch.argtypes = lib.gdn_mixed_step.argtypes + [_P, _P, _P]
     lib.gdn_prefill_workspace_bytes.restype = _SZ
     lib.gdn_prefill_workspace_bytes.argtypes = [ctypes.POINTER(Dims), _I32, _I64]
     lib.gdn_status_from_device.restype = ctypes.c_int
@@ -405,12 +407,9 @@ def gdn_prefill_varlen_apc(q, k, v, g, beta, cu_seqlens, cu_seqlens_host, o, sta
            "gdn_prefill_varlen_apc")
 
 
-def gdn_mixed_step(num_decodes: int, q, k, v, g, beta, cu_seqlens_p, cu_seqlens_p_host, state,
-                   dec_src_slot, o, dec_dst_slot=None, pre_src_slot=None, pre_dst_slot=None,
-                   chunk_states=None, emit_every_chunks: int = 0, dev_status=None,
-                   scale: float = 1.0, stream=None, workspace=None) -> None:
-    """Mixed step: decode rows [0, num_decodes) then prefill sequences."""
-    lib = load_library()
+def _mixed_args(num_decodes, q, k, v, g, beta, cu_seqlens_p, cu_seqlens_p_host, state, dec_src_slot, o,
+                dec_dst_slot, pre_src_slot, pre_dst_slot, chunk_states, emit_every_chunks, dev_status,
+                scale, stream, workspace):
     bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
     q, k, v = _dev(q, "q", bf, 3), _dev(k, "k", bf, 3), _dev(v, "v", bf, 3)
     g, beta = _dev(g, "g", f32, 2), _dev(beta, "beta", f32, 2)
@@ -436,13 +435,53 @@ def gdn_mixed_step(num_decodes: int, q, k, v, g, beta, cu_seqlens_p, cu_seqlens_
     d = _dims(q, v, scale)
     cap = 0 if chunk_states is None else chunk_states.shape[0]
     ws, ws_bytes = _workspace(workspace, d, n_p, T - int(num_decodes))
-    _check(lib.gdn_mixed_step(ctypes.byref(d), int(num_decodes), n_p, _ptr(cu_seqlens_p), cu_h,
-                              _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
-                              state.shape[0], _ptr(dec_src_slot), _ptr(dec_dst_slot),
-                              _ptr(pre_src_slot), _ptr(pre_dst_slot), _ptr(o), _ptr(chunk_states),
-                              int(emit_every_chunks), cap, ws, ws_bytes, _ptr(dev_status),
-                              _stream(stream)),
-           "gdn_mixed_step")
+    # `keep` and `d` hold the memory that cu_h and byref(d) point into.
+    return (keep, d), [ctypes.byref(d), int(num_decodes), n_p, _ptr(cu_seqlens_p), cu_h,
+                       _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+                       state.shape[0], _ptr(dec_src_slot), _ptr(dec_dst_slot),
+                       _ptr(pre_src_slot), _ptr(pre_dst_slot), _ptr(o), _ptr(chunk_states),
+                       int(emit_every_chunks), cap, ws, ws_bytes, _ptr(dev_status), _stream(stream)]
+
+
+def gdn_mixed_step(num_decodes: int, q, k, v, g, beta, cu_seqlens_p, cu_seqlens_p_host, state,
+                   dec_src_slot, o, dec_dst_slot=None, pre_src_slot=None, pre_dst_slot=None,
+                   chunk_states=None, emit_every_chunks: int = 0, dev_status=None,
+                   scale: float = 1.0, stream=None, workspace=None) -> None:
+    """Mixed step: decode rows [0, num_decodes) then prefill sequences."""
+    lib = load_library()
+    _keep, args = _mixed_args(num_decodes, q, k, v, g, beta, cu_seqlens_p, cu_seqlens_p_host, state,
+                              dec_src_slot, o, dec_dst_slot, pre_src_slot, pre_dst_slot, chunk_states,
+                              emit_every_chunks, dev_status, scale, stream, workspace)
+    _check(lib.gdn_mixed_step(*args), "gdn_mixed_step")
+
+
+def _event_handle(ev, stream):
+    # torch creates the CUDA event on its first record; recording it once on
+    # `stream` here is harmless because the library records it again.
+    if ev.cuda_event == 0:
+        ev.record(stream if stream is not None else torch.cuda.current_stream())
+    return ctypes.c_void_p(ev.cuda_event)
+
+
+def gdn_mixed_step_colaunch(num_decodes: int, q, k, v, g, beta, cu_seqlens_p, cu_seqlens_p_host, state,
+                            dec_src_slot, o, aux_stream, fork_event, join_event, dec_dst_slot=None,
+                            pre_src_slot=None, pre_dst_slot=None, chunk_states=None,
+                            emit_every_chunks: int = 0, dev_status=None, scale: float = 1.0,
+                            stream=None, workspace=None) -> None:
+    """Mixed step with the decode rows on `aux_stream` (a torch.cuda.Stream)
+    running beside the prefill on `stream`; `fork_event` and `join_event` are
+    torch.cuda.Event objects the call records (fork on `stream`, join on
+    `aux_stream`).  The decode and prefill slots must not overlap."""
+    lib = load_library()
+    _keep, args = _mixed_args(num_decodes, q, k, v, g, beta, cu_seqlens_p, cu_seqlens_p_host, state,
+                              dec_src_slot, o, dec_dst_slot, pre_src_slot, pre_dst_slot, chunk_states,
+                              emit_every_chunks, dev_status, scale, stream, workspace)
+    if aux_stream is None:
+        extra = [None, None, None]
+    else:
+        extra = [ctypes.c_void_p(aux_stream.cuda_stream), _event_handle(fork_event, stream),
+                 _event_handle(join_event, stream)]
+    _check(lib.gdn_mixed_step_colaunch(*args, *extra), "gdn_mixed_step_colaunch")
 
 
 # ---------------------------------------------------------------------------

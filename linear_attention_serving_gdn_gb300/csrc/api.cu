@@ -339,21 +339,29 @@ gdn_status_t gdn_prefill_varlen_apc(const gdn_dims_t *dims, int32_t num_seqs,
                         block_table_stride, block_first);
 }
 
-gdn_status_t gdn_mixed_step(const gdn_dims_t *dims, int32_t num_decodes, int32_t num_prefills,
-                            const int32_t *cu_seqlens_p, const int32_t *cu_seqlens_p_host,
-                            const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
-                            const float *g, const float *beta, float *state, int64_t num_slots,
-                            const int32_t *dec_src_slot, const int32_t *dec_dst_slot,
-                            const int32_t *pre_src_slot, const int32_t *pre_dst_slot,
-                            gdn_bf16 *o, float *chunk_states, int32_t emit_every_chunks,
-                            int64_t chunk_states_capacity, void *workspace, size_t workspace_bytes,
-                            int32_t *dev_status, void *stream) {
+namespace {
+
+// Both halves of a mixed step validated, then launched: the decode rows on
+// `dec_st` and the prefill on `st`; with a separate `dec_st`, the two are
+// forked from and joined back into `st` through the caller's events.
+gdn_status_t mixed_impl(const gdn_dims_t *dims, int32_t num_decodes, int32_t num_prefills,
+                        const int32_t *cu_seqlens_p, const int32_t *cu_seqlens_p_host,
+                        const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                        const float *g, const float *beta, float *state, int64_t num_slots,
+                        const int32_t *dec_src_slot, const int32_t *dec_dst_slot,
+                        const int32_t *pre_src_slot, const int32_t *pre_dst_slot,
+                        gdn_bf16 *o, float *chunk_states, int32_t emit_every_chunks,
+                        int64_t chunk_states_capacity, void *workspace, size_t workspace_bytes,
+                        int32_t *dev_status, cudaStream_t st, cudaStream_t dec_st,
+                        cudaEvent_t fork_event, cudaEvent_t join_event) {
     gdn_status_t why = GDN_OK;
     if (!dims_ok(dims, &why)) return why;
     if (num_decodes < 0 || num_prefills < 0) return GDN_ERR_INVALID_ARG;
     if (num_prefills > 0 && !cu_ok(cu_seqlens_p_host, num_prefills)) return GDN_ERR_INVALID_ARG;
     if (num_decodes > 0 && (!dec_src_slot || !state)) return GDN_ERR_INVALID_ARG;
     if (num_prefills > 0 && !cu_seqlens_p) return GDN_ERR_INVALID_ARG;
+    const bool forked = dec_st != st;
+    if (forked && (!fork_event || !join_event)) return GDN_ERR_INVALID_ARG;
     // The prefill part starts num_decodes rows into every token-major tensor;
     // rows are 16-byte multiples for the supported head dims.
     const size_t hk = static_cast<size_t>(dims->h_k) * dims->d_k;
@@ -361,7 +369,6 @@ gdn_status_t gdn_mixed_step(const gdn_dims_t *dims, int32_t num_decodes, int32_t
     const size_t nd = static_cast<size_t>(num_decodes);
     auto off16 = [&](const gdn_bf16 *p, size_t row) { return p ? p + nd * row : nullptr; };
     auto offf = [&](const float *p) { return p ? p + nd * dims->h_v : nullptr; };
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     // Both halves are validated completely before either is launched.
     gdn::DecodeArgs da{};
     gdn_status_t s = decode_check(dims, num_decodes, q, k, v, g, beta, state, num_slots, dec_src_slot,
@@ -373,10 +380,52 @@ gdn_status_t gdn_mixed_step(const gdn_dims_t *dims, int32_t num_decodes, int32_t
                       o ? o + nd * hv : nullptr, chunk_states, emit_every_chunks, chunk_states_capacity,
                       workspace, workspace_bytes, dev_status, &pa);
     if (s != GDN_OK) return s;
-    if (num_decodes > 0 && gdn::launch_decode(da, dims->d_k, st) != cudaSuccess) return GDN_ERR_CUDA;
+    if (forked && (cudaEventRecord(fork_event, st) != cudaSuccess ||
+                   cudaStreamWaitEvent(dec_st, fork_event, 0) != cudaSuccess))
+        return GDN_ERR_CUDA;
+    if (num_decodes > 0 && gdn::launch_decode(da, dims->d_k, dec_st) != cudaSuccess) return GDN_ERR_CUDA;
     if (num_prefills > 0 && gdn::launch_prefill(pa, dims->d_k, cu_seqlens_p_host, st) != cudaSuccess)
         return GDN_ERR_CUDA;
+    if (forked && (cudaEventRecord(join_event, dec_st) != cudaSuccess ||
+                   cudaStreamWaitEvent(st, join_event, 0) != cudaSuccess))
+        return GDN_ERR_CUDA;
     return GDN_OK;
+}
+
+}  // namespace
+
+gdn_status_t gdn_mixed_step(const gdn_dims_t *dims, int32_t num_decodes, int32_t num_prefills,
+                            const int32_t *cu_seqlens_p, const int32_t *cu_seqlens_p_host,
+                            const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                            const float *g, const float *beta, float *state, int64_t num_slots,
+                            const int32_t *dec_src_slot, const int32_t *dec_dst_slot,
+                            const int32_t *pre_src_slot, const int32_t *pre_dst_slot,
+                            gdn_bf16 *o, float *chunk_states, int32_t emit_every_chunks,
+                            int64_t chunk_states_capacity, void *workspace, size_t workspace_bytes,
+                            int32_t *dev_status, void *stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return mixed_impl(dims, num_decodes, num_prefills, cu_seqlens_p, cu_seqlens_p_host, q, k, v, g, beta, state,
+                      num_slots, dec_src_slot, dec_dst_slot, pre_src_slot, pre_dst_slot, o, chunk_states,
+                      emit_every_chunks, chunk_states_capacity, workspace, workspace_bytes, dev_status, st, st,
+                      nullptr, nullptr);
+}
+
+gdn_status_t gdn_mixed_step_colaunch(const gdn_dims_t *dims, int32_t num_decodes, int32_t num_prefills,
+                                     const int32_t *cu_seqlens_p, const int32_t *cu_seqlens_p_host,
+                                     const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                                     const float *g, const float *beta, float *state, int64_t num_slots,
+                                     const int32_t *dec_src_slot, const int32_t *dec_dst_slot,
+                                     const int32_t *pre_src_slot, const int32_t *pre_dst_slot,
+                                     gdn_bf16 *o, float *chunk_states, int32_t emit_every_chunks,
+                                     int64_t chunk_states_capacity, void *workspace, size_t workspace_bytes,
+                                     int32_t *dev_status, void *stream, void *aux_stream, void *fork_event,
+                                     void *join_event) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaStream_t dec_st = aux_stream ? static_cast<cudaStream_t>(aux_stream) : st;
+    return mixed_impl(dims, num_decodes, num_prefills, cu_seqlens_p, cu_seqlens_p_host, q, k, v, g, beta, state,
+                      num_slots, dec_src_slot, dec_dst_slot, pre_src_slot, pre_dst_slot, o, chunk_states,
+                      emit_every_chunks, chunk_states_capacity, workspace, workspace_bytes, dev_status, st, dec_st,
+                      static_cast<cudaEvent_t>(fork_event), static_cast<cudaEvent_t>(join_event));
 }
 
 int64_t gdn_prefill_num_emits(const int32_t *cu_seqlens_host, int32_t num_seqs,

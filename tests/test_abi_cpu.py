@@ -208,6 +208,26 @@ def test_mixed_step_validates_the_prefill_half_before_launching_decode(lib):
     assert _mixed(lib, dims, 4, 1, cu, ws=ctypes.c_void_p(0x10010)) == 4               # workspace alignment
 
 
+def _colaunch(lib, dims, nd, n_p, cu, aux=FAKE, fork=FAKE, join=FAKE, cs=None, E=0, cap=0):
+    return lib.gdn_mixed_step_colaunch(ctypes.byref(dims), nd, n_p, FAKE, cu, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                       FAKE, 8, FAKE, None, None, None, FAKE, cs, E, cap, None, 0, None,
+                                       None, aux, fork, join)
+
+
+def test_mixed_step_colaunch_validates_before_forking(lib):
+    # A separate decode stream needs both events; a bad half of the step is
+    # rejected before any event is recorded or kernel launched (either would
+    # have returned GDN_ERR_CUDA without a GPU).
+    dims = _Dims(16, 16, 128, 128, 1.0)
+    cu = (ctypes.c_int32 * 2)(0, 2000)
+    assert _colaunch(lib, dims, 4, 1, cu, fork=None) == 1
+    assert _colaunch(lib, dims, 4, 1, cu, join=None) == 1
+    assert _colaunch(lib, dims, 4, 1, cu, cs=FAKE, E=1, cap=30) == 1      # 31 emits needed
+    assert _colaunch(lib, dims, -1, 1, cu) == 1
+    bad = (ctypes.c_int32 * 3)(0, 7, 2)
+    assert _colaunch(lib, dims, 4, 2, bad) == 1
+
+
 def test_status_from_device_word(lib):
     import linear_attention_serving_gdn_gb300 as gdn
     assert gdn.gdn_status_from_device(0) == 0

@@ -169,6 +169,48 @@ def test_decode_prefill_colaunch_on_two_streams(gdn):
     assert st.item() == 0
 
 
+@pytest.mark.parametrize("which", ["tiny", "full"])
+def test_mixed_step_colaunch_entry_point(gdn, which):
+    """gdn_mixed_step_colaunch (decode on an aux stream, prefill on the
+    caller's, fork/join through the caller's events): eager, captured in a
+    CUDA graph and replayed twice, and with no aux stream; each equals the
+    single-stream mixed step bit for bit, step after step."""
+    wl = gi.tiny_mixed(0) if which == "tiny" else gi.mixed_step(0)
+    b = _mixed_buffers(wl)
+    arrs = b["arrs"]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    caches = {n: b["cache"].clone() for n in ("ref", "eager", "noaux")}
+    outs = {n: torch.empty((b["T"], b["h"], b["d"]), dtype=torch.bfloat16, device="cuda")
+            for n in ("ref", "eager", "noaux", "graph")}
+    aux, fork, join = torch.cuda.Stream(), torch.cuda.Event(), torch.cuda.Event()
+
+    def co(cache, o, aux_stream):
+        gdn.gdn_mixed_step_colaunch(b["nd"], arrs["q"], arrs["k"], arrs["v"], arrs["g"], arrs["beta"],
+                                    b["cu_p"], b["cu_h"], cache, b["dsrc"], o, aux_stream, fork, join,
+                                    pre_dst_slot=b["pdst"], dev_status=st)
+
+    graph = torch.cuda.CUDAGraph()
+    g_aux = torch.cuda.Stream()
+    graph_cache = b["cache"].clone()
+    with torch.cuda.graph(graph):
+        co(graph_cache, outs["graph"], g_aux)
+    # capture does not run the work; restore the states for the replays
+    graph_cache.copy_(b["cache"])
+    torch.cuda.synchronize()
+    for rep in range(2):
+        _run_mixed(gdn, b, caches["ref"], arrs, outs["ref"], st)
+        co(caches["eager"], outs["eager"], aux)
+        co(caches["noaux"], outs["noaux"], None)
+        graph.replay()
+        torch.cuda.synchronize()
+        for n in ("eager", "noaux"):
+            assert torch.equal(_bits(outs[n]), _bits(outs["ref"])), f"{n} rep {rep}: o differs"
+            assert torch.equal(caches[n], caches["ref"]), f"{n} rep {rep}: states differ"
+        assert torch.equal(_bits(outs["graph"]), _bits(outs["ref"])), f"graph rep {rep}: o differs"
+        assert torch.equal(graph_cache, caches["ref"]), f"graph rep {rep}: states differ"
+    assert st.item() == 0
+
+
 @pytest.mark.parametrize("parts", [2, 4])
 def test_end_to_end_step_in_row_groups_matches_single_call(gdn, parts):
     """The benchmark's end-to-end decode step with its rows split into groups
