@@ -257,18 +257,20 @@ decode_multi_kernel(const DecodeMultiArgs a) {
                 dst = src;
             }
             float *dp = dst >= 0 ? a.state + (static_cast<size_t>(dst) * a.h_v + h) * D * D : nullptr;
+            float vj[kMultiGroups], oj[kMultiGroups];
+#pragma unroll
+            for (int i = 0; i < kMultiGroups; ++i) vj[i] = bf16_bits_to_float(vrow[row0 + i * kRowsPerGroup + sub]);
+            update_rows<V4, kMultiGroups>(s, kk, qq, alpha, beta, vj, kq, a.scale, oj);
 #pragma unroll
             for (int i = 0; i < kMultiGroups; ++i) {
                 const int j = row0 + i * kRowsPerGroup + sub;
-                const float vj = bf16_bits_to_float(vrow[j]);
-                const float oj = update_row<V4>(s[i], kk, qq, alpha, beta, vj, kq, a.scale);
                 if (dp) {
 #pragma unroll
                     for (int m = 0; m < V4; ++m)
                         __stcs(reinterpret_cast<float4 *>(dp + static_cast<size_t>(j) * D + 4 * (l8 + 8 * m)),
                                s[i][m]);
                 }
-                if (l8 == 0) orow[j] = float_to_bf16_bits(oj);
+                if (l8 == 0) orow[j] = float_to_bf16_bits(oj[i]);
             }
         }
     }

@@ -144,4 +144,51 @@ __device__ __forceinline__ float update_row(float4 (&s)[V4], const float (&kk)[V
     return scale * fmaf(u, kq, alpha * b);
 }
 
+// update_row on G rows at once, phase by phase (all dot products, then the G
+// pairs of octet reductions level by level, then all updates), so that the
+// rows' independent dependency chains overlap.  Each row's arithmetic is
+// update_row's, operation for operation: the results are the same bits.
+template <int V4, int G>
+__device__ __forceinline__ void update_rows(float4 (&s)[G][V4], const float (&kk)[V4 * 4],
+                                            const float (&qq)[V4 * 4], float alpha, float beta,
+                                            const float (&vj)[G], float kq, float scale, float (&oj)[G]) {
+    float a[G], b[G];
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+        float2 a2 = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int m = 0; m < V4; ++m) {
+            const float2 s01 = make_float2(s[i][m].x, s[i][m].y), s23 = make_float2(s[i][m].z, s[i][m].w);
+            a2 = fma2(s01, make_float2(kk[4 * m + 0], kk[4 * m + 1]), a2);
+            b2 = fma2(s01, make_float2(qq[4 * m + 0], qq[4 * m + 1]), b2);
+            a2 = fma2(s23, make_float2(kk[4 * m + 2], kk[4 * m + 3]), a2);
+            b2 = fma2(s23, make_float2(qq[4 * m + 2], qq[4 * m + 3]), b2);
+        }
+        a[i] = a2.x + a2.y;
+        b[i] = b2.x + b2.y;
+    }
+#pragma unroll
+    for (int lvl = 4; lvl >= 1; lvl >>= 1) {
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+            a[i] += __shfl_xor_sync(0xffffffffu, a[i], lvl);
+            b[i] += __shfl_xor_sync(0xffffffffu, b[i], lvl);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+        const float u = beta * (vj[i] - alpha * a[i]);
+        const float2 al = make_float2(alpha, alpha), uu = make_float2(u, u);
+#pragma unroll
+        for (int m = 0; m < V4; ++m) {
+            const float2 s01 =
+                fma2(make_float2(kk[4 * m + 0], kk[4 * m + 1]), uu, mul2(al, make_float2(s[i][m].x, s[i][m].y)));
+            const float2 s23 =
+                fma2(make_float2(kk[4 * m + 2], kk[4 * m + 3]), uu, mul2(al, make_float2(s[i][m].z, s[i][m].w)));
+            s[i][m] = make_float4(s01.x, s01.y, s23.x, s23.y);
+        }
+        oj[i] = scale * fmaf(u, kq, alpha * b[i]);
+    }
+}
+
 }  // namespace gdn
