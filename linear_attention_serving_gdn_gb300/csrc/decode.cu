@@ -100,7 +100,7 @@ decode_kernel(const DecodeArgs a) {
 // Items of the multi-token form: 16 rows, since every token of the row adds
 // q, k, v loads and reductions to the item (measured: 8-row items are ~15 %
 // slower here, unlike the single-token decode).
-constexpr int kMultiGroups = 4;
+constexpr int kMultiGroups = 4;  // update_rows4_scatter takes the four rows of an octet
 constexpr int kMultiRows = kRowsPerGroup * kMultiGroups;  // 16
 
 // Multi-token decode (speculative tokens): the item's 16 state rows stay in
@@ -109,8 +109,10 @@ constexpr int kMultiRows = kRowsPerGroup * kMultiGroups;  // 16
 // is loaded; after token t the state is stored at
 // dst_slots[r * T + t] when that entry is >= 0 (a snapshot a verifier can
 // roll back to), or, with dst_slots == NULL, once after the last token back
-// to src_slot[r].  Every step is the same update_row as the packed decode, so
-// T tokens here equal T packed-decode calls bit for bit.
+// to src_slot[r].  Every step has the packed decode's per-row arithmetic
+// (update_row; here the reductions of an item's rows are done together as a
+// reduce-scatter of the same sums), so T tokens here equal T packed-decode
+// calls bit for bit.
 // Per warp, the inputs of up to kStageTokens tokens of its current row are
 // staged in shared memory by asynchronous copies issued when the item starts:
 // one memory round trip per item instead of one per token.
@@ -199,6 +201,8 @@ decode_multi_kernel(const DecodeMultiArgs a) {
                 uint16_t *orow = a.o + ((static_cast<size_t>(r) * T + t) * a.h_v + h) * D;
                 if (lane < kMultiRows) orow[row0 + lane] = 0;
             }
+            // the stage is refilled by the next item only after these copies land
+            if (staged) asm volatile("cp.async.wait_group 0;" ::: "memory");
             continue;
         }
         const float *sp = a.state + (static_cast<size_t>(src) * a.h_v + h) * D * D;
@@ -257,21 +261,21 @@ decode_multi_kernel(const DecodeMultiArgs a) {
                 dst = src;
             }
             float *dp = dst >= 0 ? a.state + (static_cast<size_t>(dst) * a.h_v + h) * D * D : nullptr;
-            float vj[kMultiGroups], oj[kMultiGroups];
+            // lane l8 of the octet takes v of, and writes o of, row (l8 & 3) * 4 + octet
+            const int jo = row0 + (l8 & 3) * kRowsPerGroup + sub;
+            const float oj = update_rows4_scatter<V4>(s, kk, qq, alpha, beta, bf16_bits_to_float(vrow[jo]), kq,
+                                                      a.scale, lane);
+            if (dp) {
 #pragma unroll
-            for (int i = 0; i < kMultiGroups; ++i) vj[i] = bf16_bits_to_float(vrow[row0 + i * kRowsPerGroup + sub]);
-            update_rows<V4, kMultiGroups>(s, kk, qq, alpha, beta, vj, kq, a.scale, oj);
-#pragma unroll
-            for (int i = 0; i < kMultiGroups; ++i) {
-                const int j = row0 + i * kRowsPerGroup + sub;
-                if (dp) {
+                for (int i = 0; i < kMultiGroups; ++i) {
+                    const int j = row0 + i * kRowsPerGroup + sub;
 #pragma unroll
                     for (int m = 0; m < V4; ++m)
                         __stcs(reinterpret_cast<float4 *>(dp + static_cast<size_t>(j) * D + 4 * (l8 + 8 * m)),
                                s[i][m]);
                 }
-                if (l8 == 0) orow[j] = float_to_bf16_bits(oj[i]);
             }
+            if (l8 >= 4) orow[jo] = float_to_bf16_bits(oj);
         }
     }
 }

@@ -115,6 +115,15 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
     return d;
 }
 
+// u_j and o_j with every rounding explicit, so that the kernels sharing them
+// give the same bits whatever the compiler contracts or shares around them.
+__device__ __forceinline__ float row_u(float beta, float vj, float alpha, float a) {
+    return __fmul_rn(beta, __fmaf_rn(-alpha, a, vj));
+}
+__device__ __forceinline__ float row_o(float scale, float u, float kq, float alpha, float b) {
+    return __fmul_rn(scale, __fmaf_rn(u, kq, __fmul_rn(alpha, b)));
+}
+
 // Updates the lane's slice of one row in place and returns o_j.  The two dot
 // products run as packed pairs: even and odd elements of the slice are summed
 // in separate halves, which are added before the octet reduction.
@@ -133,7 +142,7 @@ __device__ __forceinline__ float update_row(float4 (&s)[V4], const float (&kk)[V
     }
     const float a = octet_sum(a2.x + a2.y);
     const float b = octet_sum(b2.x + b2.y);
-    const float u = beta * (vj - alpha * a);
+    const float u = row_u(beta, vj, alpha, a);
     const float2 al = make_float2(alpha, alpha), uu = make_float2(u, u);
 #pragma unroll
     for (int m = 0; m < V4; ++m) {
@@ -141,7 +150,7 @@ __device__ __forceinline__ float update_row(float4 (&s)[V4], const float (&kk)[V
         const float2 s23 = fma2(make_float2(kk[4 * m + 2], kk[4 * m + 3]), uu, mul2(al, make_float2(s[m].z, s[m].w)));
         s[m] = make_float4(s01.x, s01.y, s23.x, s23.y);
     }
-    return scale * fmaf(u, kq, alpha * b);
+    return row_o(scale, u, kq, alpha, b);
 }
 
 // update_row on G rows at once, phase by phase (all dot products, then the G
@@ -177,7 +186,7 @@ __device__ __forceinline__ void update_rows(float4 (&s)[G][V4], const float (&kk
     }
 #pragma unroll
     for (int i = 0; i < G; ++i) {
-        const float u = beta * (vj[i] - alpha * a[i]);
+        const float u = row_u(beta, vj[i], alpha, a[i]);
         const float2 al = make_float2(alpha, alpha), uu = make_float2(u, u);
 #pragma unroll
         for (int m = 0; m < V4; ++m) {
@@ -187,8 +196,72 @@ __device__ __forceinline__ void update_rows(float4 (&s)[G][V4], const float (&kk
                 fma2(make_float2(kk[4 * m + 2], kk[4 * m + 3]), uu, mul2(al, make_float2(s[i][m].z, s[i][m].w)));
             s[i][m] = make_float4(s01.x, s01.y, s23.x, s23.y);
         }
-        oj[i] = scale * fmaf(u, kq, alpha * b[i]);
+        oj[i] = row_o(scale, u, kq, alpha, b[i]);
     }
+}
+
+// update_rows for the four rows of a lane octet's 16-row item (rows
+// 4 i + octet, i = 0..3) with the eight octet reductions done as one
+// reduce-scatter: at each xor level (4, 2, 1) a lane keeps half of its partial
+// sums and sends the other half to its partner, so that lane l8 ends with
+// a_{l8} (l8 < 4) or b_{l8-4} (l8 >= 4).  Each sum is built from the same
+// pairs in the same order as octet_sum's butterfly, so it has the same bits.
+// u_i is formed on lane i of the octet and broadcast; o of row l8 & 3 is
+// returned on lanes l8 >= 4.  vj_own is v of row l8 & 3.
+template <int V4>
+__device__ __forceinline__ float update_rows4_scatter(float4 (&s)[4][V4], const float (&kk)[V4 * 4],
+                                                      const float (&qq)[V4 * 4], float alpha, float beta,
+                                                      float vj_own, float kq, float scale, int lane) {
+    const int l8 = lane & 7, base = lane & ~7;
+    float a[4], b[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 a2 = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int m = 0; m < V4; ++m) {
+            const float2 s01 = make_float2(s[i][m].x, s[i][m].y), s23 = make_float2(s[i][m].z, s[i][m].w);
+            a2 = fma2(s01, make_float2(kk[4 * m + 0], kk[4 * m + 1]), a2);
+            b2 = fma2(s01, make_float2(qq[4 * m + 0], qq[4 * m + 1]), b2);
+            a2 = fma2(s23, make_float2(kk[4 * m + 2], kk[4 * m + 3]), a2);
+            b2 = fma2(s23, make_float2(qq[4 * m + 2], qq[4 * m + 3]), b2);
+        }
+        a[i] = a2.x + a2.y;
+        b[i] = b2.x + b2.y;
+    }
+    const bool h4 = l8 & 4, h2 = l8 & 2, h1 = l8 & 1;
+    float c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float send = h4 ? a[i] : b[i];
+        c[i] = (h4 ? b[i] : a[i]) + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    float d[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = h2 ? c[i] : c[i + 2];
+        d[i] = (h2 ? c[i + 2] : c[i]) + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    const float e = (h1 ? d[1] : d[0]) + __shfl_xor_sync(0xffffffffu, h1 ? d[0] : d[1], 1);
+    const float u_own = row_u(beta, vj_own, alpha, e);  // meaningful on lanes l8 < 4
+    float u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) u[i] = __shfl_sync(0xffffffffu, u_own, base | i);
+    const float u_row = __shfl_sync(0xffffffffu, u_own, base | (l8 & 3));
+    const float o = row_o(scale, u_row, kq, alpha, e);  // meaningful on lanes l8 >= 4
+    const float2 al = make_float2(alpha, alpha);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 uu = make_float2(u[i], u[i]);
+#pragma unroll
+        for (int m = 0; m < V4; ++m) {
+            const float2 s01 =
+                fma2(make_float2(kk[4 * m + 0], kk[4 * m + 1]), uu, mul2(al, make_float2(s[i][m].x, s[i][m].y)));
+            const float2 s23 =
+                fma2(make_float2(kk[4 * m + 2], kk[4 * m + 3]), uu, mul2(al, make_float2(s[i][m].z, s[i][m].w)));
+            s[i][m] = make_float4(s01.x, s01.y, s23.x, s23.y);
+        }
+    }
+    return o;
 }
 
 }  // namespace gdn

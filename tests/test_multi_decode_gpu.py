@@ -157,3 +157,39 @@ def test_multi_decode_final_only_with_next_item_prefetch(gdn):
     assert o_m.reshape(rows, T, h, d)[5].float().abs().max().item() == 0.0
     gu.assert_state_close(gu.get_states_math(cache_m, src[live]),
                           ref["s_final"].reshape(rows, h, d, d)[live], "final states")
+
+
+@pytest.mark.parametrize("T,d,snapshots", [(4, 128, False), (6, 128, True), (4, 64, False)])
+def test_multi_decode_many_items_with_padded_row_bitwise(gdn, T, d, snapshots):
+    """More items than resident warps (5120 of them on 152 SMs, so warps take
+    a second and third item, the last round partly filled), with a padded row
+    whose skipped item is followed by live ones in the same warps: outputs
+    and states equal T packed-decode calls bit for bit, the padded row writes
+    zeros and leaves every state untouched."""
+    h = 16
+    rows = 40 if d == 128 else 80
+    b, src, dst, cache_m, x = _setup(rows, T, 16, h, d, seed=31)
+    src = src.copy()
+    src[1] = -1
+    cache_p = cache_m.clone()
+    src_t = torch.from_numpy(src).cuda()
+    o_m = torch.empty((rows * T, h, d), dtype=torch.bfloat16, device="cuda")
+    dst_t = torch.from_numpy(dst.reshape(-1).copy()).cuda() if snapshots else None
+    gdn.gdn_decode_multi(T, x["q"], x["k"], x["v"], x["g"], x["beta"], cache_m, src_t, o_m, dst_slots=dst_t)
+    o_p = torch.empty((rows, T, h, d), dtype=torch.bfloat16, device="cuda")
+    prev = src
+    for t in range(T):
+        idx = torch.from_numpy(np.arange(rows) * T + t).cuda()
+        step = {n: x[n].index_select(0, idx).contiguous() for n in ("q", "k", "v", "g", "beta")}
+        ot = torch.empty((rows, h, d), dtype=torch.bfloat16, device="cuda")
+        nxt = dst[:, t].copy() if snapshots else prev
+        if snapshots:
+            nxt[1] = -1
+        gdn.gdn_decode_packed(step["q"], step["k"], step["v"], step["g"], step["beta"], cache_p,
+                              torch.from_numpy(prev).cuda(), ot, dst_slot=torch.from_numpy(nxt).cuda())
+        o_p[:, t] = ot
+        prev = nxt
+    torch.cuda.synchronize()
+    assert torch.equal(o_m.view(torch.int16), o_p.reshape(rows * T, h, d).view(torch.int16))
+    assert torch.equal(cache_m, cache_p)
+    assert o_m.reshape(rows, T, h, d)[1].float().abs().max().item() == 0.0
