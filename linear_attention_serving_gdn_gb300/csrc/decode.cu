@@ -134,6 +134,30 @@ __device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
                  : "memory");
 }
 
+// Position of a multi-token item, item = (r * h_v + h) * (D / kMultiRows) + b,
+// advanced from one of a warp's items to its next by mixed-radix addition
+// (no divisions in the loop).
+struct ItemPos {
+    int b, h, r;
+};
+struct ItemStep {
+    int db, dh, dr;
+};
+__device__ __forceinline__ ItemPos item_pos(int64_t it, int items_per_head, int h_v) {
+    const int64_t rh = it / items_per_head;
+    return ItemPos{static_cast<int>(it % items_per_head), static_cast<int>(rh % h_v), static_cast<int>(rh / h_v)};
+}
+__device__ __forceinline__ ItemPos item_next(ItemPos p, ItemStep s, int items_per_head, int h_v) {
+    p.b += s.db;
+    const int cb = p.b >= items_per_head;
+    p.b -= cb ? items_per_head : 0;
+    p.h += s.dh + cb;
+    const int ch = p.h >= h_v;
+    p.h -= ch ? h_v : 0;
+    p.r += s.dr + ch;
+    return p;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kMultiThreads, 2)
 decode_multi_kernel(const DecodeMultiArgs a) {
@@ -145,9 +169,12 @@ decode_multi_kernel(const DecodeMultiArgs a) {
     const int sub = lane >> 3;
     const int l8 = lane & 7;
     const int T = a.tokens_per_row;
-    const int64_t n_items = static_cast<int64_t>(a.num_rows) * a.h_v * kItemsPerHead;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int group = a.h_v / a.h_k;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const ItemPos dpos = item_pos(nwarps, kItemsPerHead, a.h_v);
+    const ItemStep step{dpos.b, dpos.h, dpos.r};
+    // per-token strides of the token-major inputs and outputs
+    const size_t kq_stride = static_cast<size_t>(a.h_k) * D, hv_stride = static_cast<size_t>(a.h_v) * D;
 
     const bool staged = T <= kStageTokens;
     // With several tokens per row and only the final state written, an item's
@@ -155,52 +182,43 @@ decode_multi_kernel(const DecodeMultiArgs a) {
     // L2 ahead of time (measured: with snapshots, or at one or two tokens, the
     // extra requests only compete with the kernel's own traffic).
     const bool prefetch = a.dst_slots == nullptr && T >= 3;
-    // Copies of item iit's token inputs into this warp's stage (one commit
-    // group): rows of k and q (D / 8 16-byte pieces each), the item's v
-    // (kMultiRows / 8 pieces), g and beta.
-    auto issue_stage = [&](int64_t iit) {
-        const int row0_ = static_cast<int>(iit % kItemsPerHead) * kMultiRows;
-        const int64_t rh_ = iit / kItemsPerHead;
-        const int h_ = static_cast<int>(rh_ % a.h_v), r_ = static_cast<int>(rh_ / a.h_v), kh_ = h_ / group;
-        uint8_t(*st)[MS::kBytes] = stage_all[threadIdx.x >> 5];
-        for (int t = 0; t < T; ++t) {
-            const size_t tok = static_cast<size_t>(r_) * T + t;
-            const size_t gh = tok * a.h_v + h_;
+    uint8_t(*stage)[MS::kBytes] = stage_all[threadIdx.x >> 5];
+
+    ItemPos cur = item_pos((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5, kItemsPerHead, a.h_v);
+    for (; cur.r < a.num_rows; cur = item_next(cur, step, kItemsPerHead, a.h_v)) {
+        const int h = cur.h, r = cur.r, row0 = cur.b * kMultiRows;
+        const int kh = h / group;
+        const size_t tok0 = static_cast<size_t>(r) * T;  // the row's first token
+        if (staged) {
+            // Copies of the item's token inputs into this warp's stage (one
+            // commit group): rows of k and q (D / 8 16-byte pieces each), the
+            // item's v (kMultiRows / 8 pieces), g and beta.
+            __syncwarp();  // the previous item's reads of the stage are done
             if (lane < D / 8) {
-                cp_async16(st[t] + MS::kK + 16 * lane, a.k + (tok * a.h_k + kh_) * D + 8 * lane);
-                cp_async16(st[t] + MS::kQ + 16 * lane, a.q + (tok * a.h_k + kh_) * D + 8 * lane);
+                const uint16_t *pk = a.k + (tok0 * a.h_k + kh) * D + 8 * lane;
+                const uint16_t *pq = a.q + (tok0 * a.h_k + kh) * D + 8 * lane;
+                for (int t = 0; t < T; ++t, pk += kq_stride, pq += kq_stride) {
+                    cp_async16(stage[t] + MS::kK + 16 * lane, pk);
+                    cp_async16(stage[t] + MS::kQ + 16 * lane, pq);
+                }
             } else if (lane < D / 8 + kMultiRows / 8) {
                 const int pc = lane - D / 8;
-                cp_async16(st[t] + MS::kV + 16 * pc, a.v + gh * D + row0_ + 8 * pc);
-            } else if (lane == 30) {
-                cp_async4(st[t] + MS::kG, a.g + gh);
-            } else if (lane == 31) {
-                cp_async4(st[t] + MS::kB, a.beta + gh);
+                const uint16_t *pv = a.v + (tok0 * a.h_v + h) * D + row0 + 8 * pc;
+                for (int t = 0; t < T; ++t, pv += hv_stride) cp_async16(stage[t] + MS::kV + 16 * pc, pv);
+            } else if (lane >= 30) {
+                const float *pg = (lane == 30 ? a.g : a.beta) + tok0 * a.h_v + h;
+                const int off = lane == 30 ? MS::kG : MS::kB;
+                for (int t = 0; t < T; ++t, pg += a.h_v) cp_async4(stage[t] + off, pg);
             }
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    };
-    for (int64_t it = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; it < n_items;
-         it += nwarps) {
-        const int blk = static_cast<int>(it % kItemsPerHead);
-        const int64_t rh = it / kItemsPerHead;
-        const int h = static_cast<int>(rh % a.h_v);
-        const int r = static_cast<int>(rh / a.h_v);
-        const int row0 = blk * kMultiRows;
-        const int kh = h / group;
-        uint8_t(*stage)[MS::kBytes] = stage_all[threadIdx.x >> 5];
-        if (staged) {
-            __syncwarp();  // the previous item's reads of the stage are done
-            issue_stage(it);
+            asm volatile("cp.async.commit_group;" ::: "memory");
         }
 
+        uint16_t *orow = a.o + (tok0 * a.h_v + h) * D;  // token t: + t * hv_stride
         const int src = a.src_slot[r];
         if (src < 0 || src >= a.num_slots) {
             if (src >= 0) report(a.dev_status, GDN_DEV_BAD_SLOT);
-            for (int t = 0; t < T; ++t) {
-                uint16_t *orow = a.o + ((static_cast<size_t>(r) * T + t) * a.h_v + h) * D;
+            for (int t = 0; t < T; ++t, orow += hv_stride)
                 if (lane < kMultiRows) orow[row0 + lane] = 0;
-            }
             // the stage is refilled by the next item only after these copies land
             if (staged) asm volatile("cp.async.wait_group 0;" ::: "memory");
             continue;
@@ -216,43 +234,45 @@ decode_multi_kernel(const DecodeMultiArgs a) {
         }
         // The next item's state rows (8 KB, contiguous) are requested into L2
         // with one bulk prefetch while this item's tokens run.
-        if (prefetch && lane == 0 && it + nwarps < n_items) {
-            const int64_t nit = it + nwarps, nrh = nit / kItemsPerHead;
-            const int nsrc = a.src_slot[nrh / a.h_v];
-            if (nsrc >= 0 && nsrc < a.num_slots) {
-                const float *np = a.state + ((static_cast<size_t>(nsrc) * a.h_v + static_cast<int>(nrh % a.h_v)) * D +
-                                             static_cast<int>(nit % kItemsPerHead) * kMultiRows) * D;
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(np), "r"(kMultiRows * D * 4) : "memory");
+        if (prefetch && lane == 0) {
+            const ItemPos nx = item_next(cur, step, kItemsPerHead, a.h_v);
+            if (nx.r < a.num_rows) {
+                const int nsrc = a.src_slot[nx.r];
+                if (nsrc >= 0 && nsrc < a.num_slots) {
+                    const float *np =
+                        a.state + ((static_cast<size_t>(nsrc) * a.h_v + nx.h) * D + nx.b * kMultiRows) * D;
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(np), "r"(kMultiRows * D * 4)
+                                 : "memory");
+                }
             }
         }
         if (staged) {
             asm volatile("cp.async.wait_group 0;" ::: "memory");
             __syncwarp();
         }
-        for (int t = 0; t < T; ++t) {
-            const size_t tok = static_cast<size_t>(r) * T + t;
+        // lane l8 of the octet takes v of, and writes o of, row (l8 & 3) * 4 + octet
+        const int jo = row0 + (l8 & 3) * kRowsPerGroup + sub;
+        for (int t = 0; t < T; ++t, orow += hv_stride) {
             float kk[V4 * 4], qq[V4 * 4];
-            const size_t gh = tok * a.h_v + h;
-            float alpha, beta;
-            const uint16_t *vrow;
+            float alpha, beta, vj;
             if (staged) {
                 load_bf16_slice<V4>(reinterpret_cast<const uint16_t *>(stage[t] + MS::kK), l8, kk);
                 load_bf16_slice<V4>(reinterpret_cast<const uint16_t *>(stage[t] + MS::kQ), l8, qq);
                 alpha = expf(*reinterpret_cast<const float *>(stage[t] + MS::kG));
                 beta = *reinterpret_cast<const float *>(stage[t] + MS::kB);
-                vrow = reinterpret_cast<const uint16_t *>(stage[t] + MS::kV) - row0;
+                vj = bf16_bits_to_float(reinterpret_cast<const uint16_t *>(stage[t] + MS::kV)[jo - row0]);
             } else {
+                const size_t tok = tok0 + t, gh = tok * a.h_v + h;
                 load_bf16_slice<V4>(a.k + (tok * a.h_k + kh) * D, l8, kk);
                 load_bf16_slice<V4>(a.q + (tok * a.h_k + kh) * D, l8, qq);
                 alpha = expf(a.g[gh]);
                 beta = a.beta[gh];
-                vrow = a.v + gh * D;
+                vj = bf16_bits_to_float(a.v[gh * D + jo]);
             }
             const float kq = octet_dot<V4>(kk, qq);
-            uint16_t *orow = a.o + gh * D;
             int dst = -1;
             if (a.dst_slots) {
-                dst = a.dst_slots[tok];
+                dst = a.dst_slots[tok0 + t];
                 if (dst >= a.num_slots) {
                     report(a.dev_status, GDN_DEV_BAD_SLOT);
                     dst = -1;
@@ -260,12 +280,9 @@ decode_multi_kernel(const DecodeMultiArgs a) {
             } else if (t == T - 1) {
                 dst = src;
             }
-            float *dp = dst >= 0 ? a.state + (static_cast<size_t>(dst) * a.h_v + h) * D * D : nullptr;
-            // lane l8 of the octet takes v of, and writes o of, row (l8 & 3) * 4 + octet
-            const int jo = row0 + (l8 & 3) * kRowsPerGroup + sub;
-            const float oj = update_rows4_scatter<V4>(s, kk, qq, alpha, beta, bf16_bits_to_float(vrow[jo]), kq,
-                                                      a.scale, lane);
-            if (dp) {
+            const float oj = update_rows4_scatter<V4>(s, kk, qq, alpha, beta, vj, kq, a.scale, lane);
+            if (dst >= 0) {
+                float *dp = a.state + (static_cast<size_t>(dst) * a.h_v + h) * D * D;
 #pragma unroll
                 for (int i = 0; i < kMultiGroups; ++i) {
                     const int j = row0 + i * kRowsPerGroup + sub;
@@ -310,21 +327,22 @@ decode_multi_pf_kernel(const DecodeMultiArgs a) {
     const int sub = lane >> 3;
     const int l8 = lane & 7;
     const int T = a.tokens_per_row;
-    const int64_t n_items = static_cast<int64_t>(a.num_rows) * a.h_v * kItemsPerHead;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int group = a.h_v / a.h_k;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const ItemPos dpos = item_pos(nwarps, kItemsPerHead, a.h_v);
+    const ItemStep step{dpos.b, dpos.h, dpos.r};
+    const size_t kq_stride = static_cast<size_t>(a.h_k) * D, hv_stride = static_cast<size_t>(a.h_v) * D;
     uint8_t *wbuf = pf_smem + (threadIdx.x >> 5) * PF::kWarp;
     uint8_t *sstate = wbuf;
 
-    // Copies of item iit (one commit group): the lane's own state pieces (rows
+    // Copies of item p (one commit group): the lane's own state pieces (rows
     // 4 i + sub, float4 columns l8 + 8 m) and the item's token inputs.
-    auto issue = [&](int64_t iit, uint8_t *stage) {
-        const int row0_ = static_cast<int>(iit % kItemsPerHead) * kMultiRows;
-        const int64_t rh_ = iit / kItemsPerHead;
-        const int h_ = static_cast<int>(rh_ % a.h_v), r_ = static_cast<int>(rh_ / a.h_v), kh_ = h_ / group;
-        const int src_ = a.src_slot[r_];
+    auto issue = [&](ItemPos p, uint8_t *stage) {
+        const int row0_ = p.b * kMultiRows, kh_ = p.h / group;
+        const size_t tok0_ = static_cast<size_t>(p.r) * T;
+        const int src_ = a.src_slot[p.r];
         if (src_ >= 0 && src_ < a.num_slots) {
-            const float *sp = a.state + ((static_cast<size_t>(src_) * a.h_v + h_) * D + row0_) * D;
+            const float *sp = a.state + ((static_cast<size_t>(src_) * a.h_v + p.h) * D + row0_) * D;
 #pragma unroll
             for (int i = 0; i < kMultiGroups; ++i) {
 #pragma unroll
@@ -334,37 +352,34 @@ decode_multi_pf_kernel(const DecodeMultiArgs a) {
                 }
             }
         }
-        for (int t = 0; t < T; ++t) {
-            uint8_t *st = stage + t * MS::kBytes;
-            const size_t tok = static_cast<size_t>(r_) * T + t;
-            const size_t gh = tok * a.h_v + h_;
-            if (lane < D / 8) {
-                cp_async16(st + MS::kK + 16 * lane, a.k + (tok * a.h_k + kh_) * D + 8 * lane);
-                cp_async16(st + MS::kQ + 16 * lane, a.q + (tok * a.h_k + kh_) * D + 8 * lane);
-            } else if (lane < D / 8 + kMultiRows / 8) {
-                const int pc = lane - D / 8;
-                cp_async16(st + MS::kV + 16 * pc, a.v + gh * D + row0_ + 8 * pc);
-            } else if (lane == 30) {
-                cp_async4(st + MS::kG, a.g + gh);
-            } else if (lane == 31) {
-                cp_async4(st + MS::kB, a.beta + gh);
+        if (lane < D / 8) {
+            const uint16_t *pk = a.k + (tok0_ * a.h_k + kh_) * D + 8 * lane;
+            const uint16_t *pq = a.q + (tok0_ * a.h_k + kh_) * D + 8 * lane;
+            for (int t = 0; t < T; ++t, pk += kq_stride, pq += kq_stride) {
+                cp_async16(stage + t * MS::kBytes + MS::kK + 16 * lane, pk);
+                cp_async16(stage + t * MS::kBytes + MS::kQ + 16 * lane, pq);
             }
+        } else if (lane < D / 8 + kMultiRows / 8) {
+            const int pc = lane - D / 8;
+            const uint16_t *pv = a.v + (tok0_ * a.h_v + p.h) * D + row0_ + 8 * pc;
+            for (int t = 0; t < T; ++t, pv += hv_stride) cp_async16(stage + t * MS::kBytes + MS::kV + 16 * pc, pv);
+        } else if (lane >= 30) {
+            const float *pg = (lane == 30 ? a.g : a.beta) + tok0_ * a.h_v + p.h;
+            const int off = lane == 30 ? MS::kG : MS::kB;
+            for (int t = 0; t < T; ++t, pg += a.h_v) cp_async4(stage + t * MS::kBytes + off, pg);
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
 
-    const int64_t first = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    if (first < n_items) issue(first, wbuf + PF::kState);
-    int cur = 0;
-    for (int64_t it = first; it < n_items; it += nwarps, cur ^= 1) {
-        uint8_t *stage_buf = wbuf + PF::kState + cur * PF::kStage;
+    ItemPos cur = item_pos((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5, kItemsPerHead, a.h_v);
+    if (cur.r < a.num_rows) issue(cur, wbuf + PF::kState);
+    int buf = 0;
+    for (; cur.r < a.num_rows; buf ^= 1) {
+        uint8_t *stage_buf = wbuf + PF::kState + buf * PF::kStage;
         asm volatile("cp.async.wait_group 0;" ::: "memory");  // this item's copies have landed
         __syncwarp();
-        const int blk = static_cast<int>(it % kItemsPerHead);
-        const int64_t rh = it / kItemsPerHead;
-        const int h = static_cast<int>(rh % a.h_v);
-        const int r = static_cast<int>(rh / a.h_v);
-        const int row0 = blk * kMultiRows;
+        const int h = cur.h, r = cur.r, row0 = cur.b * kMultiRows;
+        const size_t tok0 = static_cast<size_t>(r) * T;
         const int src = a.src_slot[r];
         const bool valid = src >= 0 && src < a.num_slots;
         float4 s[kMultiGroups][V4];
@@ -383,19 +398,16 @@ decode_multi_pf_kernel(const DecodeMultiArgs a) {
         }
         // The next item's copies: its state into the state buffer (this lane's
         // pieces, already read above), its token inputs into the other stage.
-        if (it + nwarps < n_items)
-            issue(it + nwarps, wbuf + PF::kState + (cur ^ 1) * PF::kStage);
+        const ItemPos nx = item_next(cur, step, kItemsPerHead, a.h_v);
+        if (nx.r < a.num_rows) issue(nx, wbuf + PF::kState + (buf ^ 1) * PF::kStage);
+        uint16_t *orow = a.o + (tok0 * a.h_v + h) * D;  // token t: + t * hv_stride
         if (!valid) {
             if (src >= 0) report(a.dev_status, GDN_DEV_BAD_SLOT);
-            for (int t = 0; t < T; ++t) {
-                uint16_t *orow = a.o + ((static_cast<size_t>(r) * T + t) * a.h_v + h) * D;
+            for (int t = 0; t < T; ++t, orow += hv_stride)
                 if (lane < kMultiRows) orow[row0 + lane] = 0;
-            }
         } else {
-            for (int t = 0; t < T; ++t) {
-                const size_t tok = static_cast<size_t>(r) * T + t;
+            for (int t = 0; t < T; ++t, orow += hv_stride) {
                 float kk[V4 * 4], qq[V4 * 4];
-                const size_t gh = tok * a.h_v + h;
                 const uint8_t *st = stage_buf + t * MS::kBytes;
                 load_bf16_slice<V4>(reinterpret_cast<const uint16_t *>(st + MS::kK), l8, kk);
                 load_bf16_slice<V4>(reinterpret_cast<const uint16_t *>(st + MS::kQ), l8, qq);
@@ -403,10 +415,9 @@ decode_multi_pf_kernel(const DecodeMultiArgs a) {
                 const float beta = *reinterpret_cast<const float *>(st + MS::kB);
                 const uint16_t *vrow = reinterpret_cast<const uint16_t *>(st + MS::kV) - row0;
                 const float kq = octet_dot<V4>(kk, qq);
-                uint16_t *orow = a.o + gh * D;
                 int dst = -1;
                 if (a.dst_slots) {
-                    dst = a.dst_slots[tok];
+                    dst = a.dst_slots[tok0 + t];
                     if (dst >= a.num_slots) {
                         report(a.dev_status, GDN_DEV_BAD_SLOT);
                         dst = -1;
@@ -431,6 +442,7 @@ decode_multi_pf_kernel(const DecodeMultiArgs a) {
             }
         }
         __syncwarp();  // every lane is done with this stage before it is refilled
+        cur = nx;
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");  // nothing in flight at exit
 }
