@@ -134,6 +134,29 @@ __device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
                  : "memory");
 }
 
+// Stage of decode_multi_kernel: per token, k and q as fp32 (converted once
+// per token by the warp from the bf16 rows the copies land in the upper half
+// of the same bytes), the item's v (bf16), g and beta.
+template <int D>
+struct MultiStageF {
+    static constexpr int kK = 0, kQ = 4 * D, kKraw = 4 * D, kQraw = 6 * D, kV = 8 * D, kG = kV + 2 * kMultiRows,
+                         kB = kG + 16;
+    static constexpr int kBytes = kB + 16;
+    static constexpr int kBlock = (kMultiThreads / 32) * kStageTokens * kBytes;
+};
+
+template <int V4>
+__device__ __forceinline__ void load_f32_slice(const float *p, int l8, float (&x)[V4 * 4]) {
+#pragma unroll
+    for (int m = 0; m < V4; ++m) {
+        const float4 w = *reinterpret_cast<const float4 *>(p + 4 * (l8 + 8 * m));
+        x[4 * m + 0] = w.x;
+        x[4 * m + 1] = w.y;
+        x[4 * m + 2] = w.z;
+        x[4 * m + 3] = w.w;
+    }
+}
+
 // Position of a multi-token item, item = (r * h_v + h) * (D / kMultiRows) + b,
 // advanced from one of a warp's items to its next by mixed-radix addition
 // (no divisions in the loop).
@@ -163,8 +186,8 @@ __global__ void __launch_bounds__(kMultiThreads, 2)
 decode_multi_kernel(const DecodeMultiArgs a) {
     constexpr int V4 = D / 32;
     constexpr int kItemsPerHead = D / kMultiRows;
-    using MS = MultiStage<D>;
-    __shared__ __align__(16) uint8_t stage_all[kMultiThreads / 32][kStageTokens][MS::kBytes];
+    using MS = MultiStageF<D>;
+    extern __shared__ __align__(16) uint8_t multi_smem[];
     const int lane = threadIdx.x & 31;
     const int sub = lane >> 3;
     const int l8 = lane & 7;
@@ -182,7 +205,8 @@ decode_multi_kernel(const DecodeMultiArgs a) {
     // L2 ahead of time (measured: with snapshots, or at one or two tokens, the
     // extra requests only compete with the kernel's own traffic).
     const bool prefetch = a.dst_slots == nullptr && T >= 3;
-    uint8_t(*stage)[MS::kBytes] = stage_all[threadIdx.x >> 5];
+    uint8_t(*stage)[MS::kBytes] =
+        reinterpret_cast<uint8_t(*)[MS::kBytes]>(multi_smem + (threadIdx.x >> 5) * kStageTokens * MS::kBytes);
 
     ItemPos cur = item_pos((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5, kItemsPerHead, a.h_v);
     for (; cur.r < a.num_rows; cur = item_next(cur, step, kItemsPerHead, a.h_v)) {
@@ -198,8 +222,8 @@ decode_multi_kernel(const DecodeMultiArgs a) {
                 const uint16_t *pk = a.k + (tok0 * a.h_k + kh) * D + 8 * lane;
                 const uint16_t *pq = a.q + (tok0 * a.h_k + kh) * D + 8 * lane;
                 for (int t = 0; t < T; ++t, pk += kq_stride, pq += kq_stride) {
-                    cp_async16(stage[t] + MS::kK + 16 * lane, pk);
-                    cp_async16(stage[t] + MS::kQ + 16 * lane, pq);
+                    cp_async16(stage[t] + MS::kKraw + 16 * lane, pk);
+                    cp_async16(stage[t] + MS::kQraw + 16 * lane, pq);
                 }
             } else if (lane < D / 8 + kMultiRows / 8) {
                 const int pc = lane - D / 8;
@@ -249,6 +273,21 @@ decode_multi_kernel(const DecodeMultiArgs a) {
         if (staged) {
             asm volatile("cp.async.wait_group 0;" ::: "memory");
             __syncwarp();
+            // k and q of every token to fp32, in place: lane L reads 8 bf16 of
+            // the upper half and, once all lanes have read, writes them as 8 floats
+            for (int t = 0; t < T; ++t) {
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (lane < D / 4) w = *reinterpret_cast<const uint4 *>(stage[t] + MS::kKraw + 16 * lane);
+                __syncwarp();
+                if (lane < D / 4) {
+                    float4 *dst = reinterpret_cast<float4 *>(stage[t] + 32 * lane);
+                    dst[0] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                                         __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+                    dst[1] = make_float4(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u),
+                                         __uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
+                }
+            }
+            __syncwarp();
         }
         // lane l8 of the octet takes v of, and writes o of, row (l8 & 3) * 4 + octet
         const int jo = row0 + (l8 & 3) * kRowsPerGroup + sub;
@@ -256,8 +295,8 @@ decode_multi_kernel(const DecodeMultiArgs a) {
             float kk[V4 * 4], qq[V4 * 4];
             float alpha, beta, vj;
             if (staged) {
-                load_bf16_slice<V4>(reinterpret_cast<const uint16_t *>(stage[t] + MS::kK), l8, kk);
-                load_bf16_slice<V4>(reinterpret_cast<const uint16_t *>(stage[t] + MS::kQ), l8, qq);
+                load_f32_slice<V4>(reinterpret_cast<const float *>(stage[t] + MS::kK), l8, kk);
+                load_f32_slice<V4>(reinterpret_cast<const float *>(stage[t] + MS::kQ), l8, qq);
                 alpha = expf(*reinterpret_cast<const float *>(stage[t] + MS::kG));
                 beta = *reinterpret_cast<const float *>(stage[t] + MS::kB);
                 vj = bf16_bits_to_float(reinterpret_cast<const uint16_t *>(stage[t] + MS::kV)[jo - row0]);
@@ -469,10 +508,18 @@ cudaError_t launch_decode_multi_d(const DecodeMultiArgs &a, cudaStream_t stream)
         decode_multi_pf_kernel<D><<<grid, kMultiThreads, smem, stream>>>(a);
         return cudaGetLastError();
     }
-    const int per_sm = blocks_per_sm(decode_multi_kernel<D>, kMultiThreads, dev, occ);
+    static int set_m[kMaxDevices] = {};
+    constexpr int smem_m = MultiStageF<D>::kBlock;
+    if (dev < 0 || dev >= kMaxDevices || !__atomic_load_n(&set_m[dev], __ATOMIC_ACQUIRE)) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(decode_multi_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_m);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDevices) __atomic_store_n(&set_m[dev], 1, __ATOMIC_RELEASE);
+    }
+    const int per_sm = blocks_per_sm(decode_multi_kernel<D>, kMultiThreads, dev, occ, smem_m);
     const int64_t cap = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
     const int grid = static_cast<int>(need < cap ? need : cap);
-    decode_multi_kernel<D><<<grid, kMultiThreads, 0, stream>>>(a);
+    decode_multi_kernel<D><<<grid, kMultiThreads, smem_m, stream>>>(a);
     return cudaGetLastError();
 }
 
