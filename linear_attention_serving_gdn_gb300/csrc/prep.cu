@@ -14,7 +14,7 @@ namespace {
 constexpr int kPrepThreads = 256;
 
 template <int D>
-__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
+__global__ void __launch_bounds__(kPrepThreads, 5) prep_kernel(const PrepArgs a) {
     constexpr int V4 = D / 32;
     const int lane = threadIdx.x & 31;
     const int sub = lane >> 3, l8 = lane & 7;
@@ -49,9 +49,58 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
             if (live[u]) store_bf16_slice<V4>((is_k[u] ? a.k : a.q) + rr[u] * D, l8, x[u]);
         }
     }
+    // Gates: a, b -> g, beta over the flat [token][value head] arrays.  With
+    // 16-byte aligned arrays each thread takes runs of four elements (float4
+    // loads and stores), kGateRuns runs at a time with all their loads issued
+    // first while whole sets remain, then single runs; the last n_gate % 4
+    // elements, and unaligned arrays, go one element at a time.  The head of
+    // element e is e % h_v, stepped by the stride's residue.
     const int64_t n_gate = a.num_tokens * a.h_v;
-    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_gate;
-         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const bool vec = ((reinterpret_cast<uintptr_t>(a.a) | reinterpret_cast<uintptr_t>(a.b) |
+                       reinterpret_cast<uintptr_t>(a.g) | reinterpret_cast<uintptr_t>(a.beta)) & 15u) == 0;
+    int64_t done = 0;  // elements [0, done) are handled by the vector loops
+    if (vec) {
+        constexpr int kGateRuns = 2;
+        const int64_t n4 = n_gate / 4;  // runs of four
+        const int dh = static_cast<int>((4 * nthreads) % a.h_v);
+        auto adv = [&](int hh, int d) {
+            hh += d;
+            return hh >= a.h_v ? hh - a.h_v : hh;
+        };
+        auto run = [&](int64_t j, float4 av, float4 bv, int h) {
+            float4 gv, btv;
+            gate_inputs(av.x, bv.x, a.A_log[h], a.dt_bias[h], gv.x, btv.x);
+            h = adv(h, 1);
+            gate_inputs(av.y, bv.y, a.A_log[h], a.dt_bias[h], gv.y, btv.y);
+            h = adv(h, 1);
+            gate_inputs(av.z, bv.z, a.A_log[h], a.dt_bias[h], gv.z, btv.z);
+            h = adv(h, 1);
+            gate_inputs(av.w, bv.w, a.A_log[h], a.dt_bias[h], gv.w, btv.w);
+            reinterpret_cast<float4 *>(a.g)[j] = gv;
+            reinterpret_cast<float4 *>(a.beta)[j] = btv;
+        };
+        int64_t j = tid;
+        int h = static_cast<int>((4 * j) % a.h_v);
+        for (; j + (kGateRuns - 1) * nthreads < n4; j += kGateRuns * nthreads) {
+            float4 av[kGateRuns], bv[kGateRuns];
+#pragma unroll
+            for (int u = 0; u < kGateRuns; ++u) {
+                av[u] = reinterpret_cast<const float4 *>(a.a)[j + u * nthreads];
+                bv[u] = reinterpret_cast<const float4 *>(a.b)[j + u * nthreads];
+            }
+#pragma unroll
+            for (int u = 0; u < kGateRuns; ++u) {
+                run(j + u * nthreads, av[u], bv[u], h);
+                h = adv(h, dh);
+            }
+        }
+        for (; j < n4; j += nthreads, h = adv(h, dh))
+            run(j, reinterpret_cast<const float4 *>(a.a)[j], reinterpret_cast<const float4 *>(a.b)[j], h);
+        done = 4 * n4;
+    }
+    for (int64_t e = done + tid; e < n_gate; e += nthreads) {
         const int h = static_cast<int>(e % a.h_v);
         float g, beta;
         gate_inputs(a.a[e], a.b[e], a.A_log[h], a.dt_bias[h], g, beta);

@@ -61,6 +61,37 @@ def test_prep_kernel_vs_oracle(gdn, T, h_k, h_v, d):
     assert np.allclose(beta.cpu().numpy(), b_ref, rtol=2e-6, atol=1e-9)
 
 
+def _at_offset(t):
+    """A contiguous copy of t starting 4 bytes past a 16-byte boundary."""
+    buf = torch.empty(t.numel() + 1, dtype=t.dtype, device="cuda")
+    v = buf[1:].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+@pytest.mark.parametrize("T,h_k,h_v,d", [(4099, 1, 66, 64), (20001, 16, 32, 128)])
+def test_prep_gate_vector_and_scalar_paths_bitwise(gdn, T, h_k, h_v, d):
+    """The gates of 16-byte aligned arrays go through float4 runs of four
+    (two runs at a time while whole sets remain, then single runs) and the
+    last n_gate % 4 elements one by one (4099 x 66 leaves 2); the same arrays
+    at a 4-byte offset go element by element.  Both give the same bits, and
+    both match the oracle."""
+    raw = gi.raw_inputs(T, h_k, h_v, d, seed=14)
+    x = _raw_to_device(raw)
+    q, k, g, beta = _prep(gdn, x)
+    g_s = _at_offset(torch.zeros_like(g))
+    beta_s = _at_offset(torch.zeros_like(beta))
+    q_s, k_s = torch.empty_like(q), torch.empty_like(k)
+    gdn.gdn_prep_inputs(x["q_raw"], x["k_raw"], _at_offset(x["a"]), _at_offset(x["b"]), x["A_log"],
+                        x["dt_bias"], q_s, k_s, g_s, beta_s)
+    torch.cuda.synchronize()
+    assert torch.equal(g, g_s) and torch.equal(beta, beta_s)
+    assert torch.equal(q.view(torch.int16), q_s.view(torch.int16))
+    _, _, g_ref, b_ref = oprep.prep(raw)
+    assert np.allclose(g.cpu().numpy(), g_ref, rtol=2e-6, atol=1e-9)
+    assert np.allclose(beta.cpu().numpy(), b_ref, rtol=2e-6, atol=1e-9)
+
+
 def test_fused_decode_equals_prep_then_decode_bitwise(gdn):
     rows, h, d = 256, 16, 128
     raw = gi.raw_inputs(rows, h, h, d, seed=12)
