@@ -210,7 +210,8 @@ def decode_e2e_graphs(torch, gdn, t, parts):
     device input buffers), captured from the public entry point: the step's
     q, k, v, g, beta go from pinned host memory to the device, the decode
     runs, o comes back to pinned host memory.  The step's rows are split into
-    `parts` groups (parts = 1: one copy, one call, one copy): group i's inputs
+    `parts` equal groups, or groups of the row counts `parts` lists (parts =
+    1: one copy, one call, one copy): group i's inputs
     are copied on an input stream, its decode runs on the capturing stream
     once they have landed, and its o is copied back on an output stream once
     its decode has finished, so the copies of one group overlap the decode of
@@ -219,24 +220,35 @@ def decode_e2e_graphs(torch, gdn, t, parts):
     Returns (graphs, h2d bytes per step, d2h bytes per step, o_host)."""
     names = ("q", "k", "v", "g", "beta")
     rows = t["q"].shape[0]
-    if rows % parts:
-        raise ValueError(f"{rows} rows do not split into {parts} equal groups")
-    pr = rows // parts
-    sizes = [t[n][:pr].numel() * t[n].element_size() for n in names]
-    offs = [0]
-    for sz in sizes:
-        offs.append(offs[-1] + (sz + 255) // 256 * 256)
-    stride = offs[-1]  # one group's packed inputs
-    host = torch.empty(stride * parts, dtype=torch.uint8).pin_memory()
-    for p in range(parts):
-        for n, o0, sz in zip(names, offs, sizes):
-            src = t[n][p * pr:(p + 1) * pr].contiguous().view(torch.uint8).reshape(-1).cpu()
-            host[p * stride + o0:p * stride + o0 + sz].copy_(src)
+    if isinstance(parts, int):
+        if rows % parts:
+            raise ValueError(f"{rows} rows do not split into {parts} equal groups")
+        counts = [rows // parts] * parts
+    else:  # explicit row counts of the groups
+        counts = [int(c) for c in parts]
+        if sum(counts) != rows or min(counts) <= 0:
+            raise ValueError(f"group sizes {counts} do not partition {rows} rows")
+    first = [sum(counts[:p]) for p in range(len(counts))]
+    # each group's inputs packed one after the other, every tensor 256-byte aligned
+    layout, pos = [], 0
+    for p, c in enumerate(counts):
+        ent = []
+        for n in names:
+            sz = t[n][:c].numel() * t[n].element_size()
+            ent.append((n, pos, sz))
+            pos += (sz + 255) // 256 * 256
+        layout.append(ent)
+    starts = [ent[0][1] for ent in layout] + [pos]
+    host = torch.empty(pos, dtype=torch.uint8).pin_memory()
+    for p, c in enumerate(counts):
+        for n, o0, sz in layout[p]:
+            src = t[n][first[p]:first[p] + c].contiguous().view(torch.uint8).reshape(-1).cpu()
+            host[o0:o0 + sz].copy_(src)
     o_host = torch.empty(t["o"].shape, dtype=t["o"].dtype).pin_memory()
-    h2d = sum(sizes) * parts
+    h2d = sum(sz for ent in layout for _, _, sz in ent)
     d2h = o_host.numel() * o_host.element_size()
     dev = t["q"].device
-    dev_in = [torch.empty(stride * parts, dtype=torch.uint8, device=dev) for _ in range(2)]
+    dev_in = [torch.empty(pos, dtype=torch.uint8, device=dev) for _ in range(2)]
     outs = [torch.empty_like(t["o"]) for _ in range(2)]
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     graphs = []
@@ -248,16 +260,16 @@ def decode_e2e_graphs(torch, gdn, t, parts):
             s_out.wait_stream(main)
             landed = []
             with torch.cuda.stream(s_in):
-                for p in range(parts):
-                    dev_in[b][p * stride:(p + 1) * stride].copy_(host[p * stride:(p + 1) * stride], non_blocking=True)
+                for p in range(len(counts)):
+                    dev_in[b][starts[p]:starts[p + 1]].copy_(host[starts[p]:starts[p + 1]], non_blocking=True)
                     ev = torch.cuda.Event()
                     ev.record(s_in)
                     landed.append(ev)
-            for p in range(parts):
+            for p, c in enumerate(counts):
                 main.wait_event(landed[p])
-                x = {n: dev_in[b][p * stride + o0:p * stride + o0 + sz].view(t[n].dtype).view((pr,) + tuple(t[n].shape[1:]))
-                     for n, o0, sz in zip(names, offs, sizes)}
-                rs = slice(p * pr, (p + 1) * pr)
+                x = {n: dev_in[b][o0:o0 + sz].view(t[n].dtype).view((c,) + tuple(t[n].shape[1:]))
+                     for n, o0, sz in layout[p]}
+                rs = slice(first[p], first[p] + c)
                 gdn.gdn_decode_packed(x["q"], x["k"], x["v"], x["g"], x["beta"], t["cache"], t["src"][rs], outs[b][rs])
                 done = torch.cuda.Event()
                 done.record(main)

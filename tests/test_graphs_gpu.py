@@ -211,7 +211,7 @@ def test_mixed_step_colaunch_entry_point(gdn, which):
     assert st.item() == 0
 
 
-@pytest.mark.parametrize("parts", [2, 4])
+@pytest.mark.parametrize("parts", [2, 4, [32, 224]], ids=["2", "4", "32+224"])
 def test_end_to_end_step_in_row_groups_matches_single_call(gdn, parts):
     """The benchmark's end-to-end decode step with its rows split into groups
     (host copies of one group overlapping the decode of another, on three
