@@ -117,6 +117,7 @@ constexpr int kMultiRows = kRowsPerGroup * kMultiGroups;  // 16
 // staged in shared memory by asynchronous copies issued when the item starts:
 // one memory round trip per item instead of one per token.
 constexpr int kStageTokens = 8;
+// Stage of the snapshot form (decode_multi_pf_kernel), per token.
 template <int D>
 struct MultiStage {
     static constexpr int kK = 0, kQ = 2 * D, kV = 4 * D, kG = kV + 2 * kMultiRows, kB = kG + 16;

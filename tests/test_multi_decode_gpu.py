@@ -159,13 +159,14 @@ def test_multi_decode_final_only_with_next_item_prefetch(gdn):
                           ref["s_final"].reshape(rows, h, d, d)[live], "final states")
 
 
-@pytest.mark.parametrize("T,d,snapshots", [(4, 128, False), (6, 128, True), (4, 64, False)])
+@pytest.mark.parametrize("T,d,snapshots", [(4, 128, False), (6, 128, True), (4, 64, False), (11, 128, False)])
 def test_multi_decode_many_items_with_padded_row_bitwise(gdn, T, d, snapshots):
     """More items than resident warps (5120 of them on 152 SMs, so warps take
     a second and third item, the last round partly filled), with a padded row
-    whose skipped item is followed by live ones in the same warps: outputs
-    and states equal T packed-decode calls bit for bit, the padded row writes
-    zeros and leaves every state untouched."""
+    whose skipped item is followed by live ones in the same warps (T = 11:
+    more tokens than the stage holds, read directly): outputs and states
+    equal T packed-decode calls bit for bit, the padded row writes zeros and
+    leaves every state untouched."""
     h = 16
     rows = 40 if d == 128 else 80
     b, src, dst, cache_m, x = _setup(rows, T, 16, h, d, seed=31)
