@@ -301,7 +301,7 @@ def test_chunked_form_matches_token_oracle(C):
         assert rel_s < 1e-10, rel_s
         assert len(emits) == len(r["emits"][p])
         for e1, e2 in zip(emits, r["emits"][p]):
-            assert np.linalg.norm(e1 - e2) / np.linalg.norm(e2) < 1e-10
+            assert np.linalg.norm(e1 - e2) < 1e-10 * np.linalg.norm(e2)
 
 
 def test_chunked_form_with_gates_from_the_workload_recipe():
