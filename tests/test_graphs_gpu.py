@@ -211,6 +211,38 @@ def test_mixed_step_colaunch_entry_point(gdn, which):
     assert st.item() == 0
 
 
+@pytest.mark.parametrize("E", [1, 17])
+def test_mixed_step_colaunch_with_emitted_states(gdn, E):
+    """The co-launched step with the prefills emitting their states every E
+    chunks: outputs, final states and every emitted state equal the
+    single-stream mixed step's bit for bit."""
+    b = _mixed_buffers(gi.mixed_step(0))
+    arrs = b["arrs"]
+    n_emit = gdn.gdn_prefill_num_emits(b["cu_h"], E)
+    assert n_emit > 0
+    res = []
+    for colaunch in (False, True):
+        cache = b["cache"].clone()
+        o = torch.empty((b["T"], b["h"], b["d"]), dtype=torch.bfloat16, device="cuda")
+        cs = torch.full((n_emit, b["h"], b["d"], b["d"]), 7.0, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        kw = dict(pre_dst_slot=b["pdst"], chunk_states=cs, emit_every_chunks=E, dev_status=st)
+        if colaunch:
+            gdn.gdn_mixed_step_colaunch(b["nd"], arrs["q"], arrs["k"], arrs["v"], arrs["g"], arrs["beta"],
+                                        b["cu_p"], b["cu_h"], cache, b["dsrc"], o, torch.cuda.Stream(),
+                                        torch.cuda.Event(), torch.cuda.Event(), **kw)
+        else:
+            gdn.gdn_mixed_step(b["nd"], arrs["q"], arrs["k"], arrs["v"], arrs["g"], arrs["beta"], b["cu_p"],
+                               b["cu_h"], cache, b["dsrc"], o, **kw)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        res.append((o, cache, cs))
+    (o1, c1, s1), (o2, c2, s2) = res
+    assert torch.equal(_bits(o1), _bits(o2))
+    assert torch.equal(c1, c2)
+    assert torch.equal(s1, s2)
+
+
 @pytest.mark.parametrize("parts", [2, 4, [32, 224]], ids=["2", "4", "32+224"])
 def test_end_to_end_step_in_row_groups_matches_single_call(gdn, parts):
     """The benchmark's end-to-end decode step with its rows split into groups
