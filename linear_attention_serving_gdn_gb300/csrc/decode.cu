@@ -117,12 +117,6 @@ constexpr int kMultiRows = kRowsPerGroup * kMultiGroups;  // 16
 // staged in shared memory by asynchronous copies issued when the item starts:
 // one memory round trip per item instead of one per token.
 constexpr int kStageTokens = 8;
-// Stage of the snapshot form (decode_multi_pf_kernel), per token.
-template <int D>
-struct MultiStage {
-    static constexpr int kK = 0, kQ = 2 * D, kV = 4 * D, kG = kV + 2 * kMultiRows, kB = kG + 16;
-    static constexpr int kBytes = kB + 16;  // per token: k, q rows (bf16), the item's v, g, beta
-};
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
@@ -135,13 +129,18 @@ __device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
                  : "memory");
 }
 
-// Stage of decode_multi_kernel: per token, k and q as fp32 (converted once
-// per token by the warp from the bf16 rows the copies land in the upper half
-// of the same bytes), the item's v (bf16), g and beta.
-template <int D>
-struct MultiStageF {
-    static constexpr int kK = 0, kQ = 4 * D, kKraw = 4 * D, kQraw = 6 * D, kV = 8 * D, kG = kV + 2 * kMultiRows,
-                         kB = kG + 16;
+// Stage of decode_multi_kernel, per token.  kF32: k and q as fp32 (the
+// copies land as bf16 in the upper half of the same bytes and the warp
+// converts them once per token), else k and q as the bf16 rows the copies
+// bring; then the item's v (bf16), g and beta.  The fp32 form measured faster
+// at 3-4 tokens per row and slower at 1-2 and 8 (its per-item conversion
+// round is not overlapped with arithmetic), so the launcher picks it for rows
+// of 3 or 4 tokens.
+template <int D, bool kF32>
+struct MultiStageT {
+    static constexpr int kK = 0, kQ = kF32 ? 4 * D : 2 * D;
+    static constexpr int kKraw = kF32 ? 4 * D : 0, kQraw = kF32 ? 6 * D : 2 * D;
+    static constexpr int kV = kF32 ? 8 * D : 4 * D, kG = kV + 2 * kMultiRows, kB = kG + 16;
     static constexpr int kBytes = kB + 16;
     static constexpr int kBlock = (kMultiThreads / 32) * kStageTokens * kBytes;
 };
@@ -182,12 +181,12 @@ __device__ __forceinline__ ItemPos item_next(ItemPos p, ItemStep s, int items_pe
     return p;
 }
 
-template <int D>
+template <int D, bool kF32>
 __global__ void __launch_bounds__(kMultiThreads, 2)
 decode_multi_kernel(const DecodeMultiArgs a) {
     constexpr int V4 = D / 32;
     constexpr int kItemsPerHead = D / kMultiRows;
-    using MS = MultiStageF<D>;
+    using MS = MultiStageT<D, kF32>;
     extern __shared__ __align__(16) uint8_t multi_smem[];
     const int lane = threadIdx.x & 31;
     const int sub = lane >> 3;
@@ -274,6 +273,8 @@ decode_multi_kernel(const DecodeMultiArgs a) {
         if (staged) {
             asm volatile("cp.async.wait_group 0;" ::: "memory");
             __syncwarp();
+        }
+        if (kF32 && staged) {
             // k and q of every token to fp32, in place: lane L reads 8 bf16 of
             // the upper half and, once all lanes have read, writes them as 8 floats
             for (int t = 0; t < T; ++t) {
@@ -296,8 +297,13 @@ decode_multi_kernel(const DecodeMultiArgs a) {
             float kk[V4 * 4], qq[V4 * 4];
             float alpha, beta, vj;
             if (staged) {
-                load_f32_slice<V4>(reinterpret_cast<const float *>(stage[t] + MS::kK), l8, kk);
-                load_f32_slice<V4>(reinterpret_cast<const float *>(stage[t] + MS::kQ), l8, qq);
+                if constexpr (kF32) {
+                    load_f32_slice<V4>(reinterpret_cast<const float *>(stage[t] + MS::kK), l8, kk);
+                    load_f32_slice<V4>(reinterpret_cast<const float *>(stage[t] + MS::kQ), l8, qq);
+                } else {
+                    load_bf16_slice<V4>(reinterpret_cast<const uint16_t *>(stage[t] + MS::kK), l8, kk);
+                    load_bf16_slice<V4>(reinterpret_cast<const uint16_t *>(stage[t] + MS::kQ), l8, qq);
+                }
                 alpha = expf(*reinterpret_cast<const float *>(stage[t] + MS::kG));
                 beta = *reinterpret_cast<const float *>(stage[t] + MS::kB);
                 vj = bf16_bits_to_float(reinterpret_cast<const uint16_t *>(stage[t] + MS::kV)[jo - row0]);
@@ -348,7 +354,7 @@ decode_multi_kernel(const DecodeMultiArgs a) {
 constexpr int kPfTokens = 4;
 template <int D>
 struct MultiPf {
-    using MS = MultiStage<D>;
+    using MS = MultiStageT<D, false>;
     static constexpr int kState = kMultiRows * D * 4;   // one item's state rows, fp32
     static constexpr int kStage = kPfTokens * MS::kBytes;
     static constexpr int kWarp = kState + 2 * kStage;   // per warp
@@ -360,7 +366,7 @@ __global__ void __launch_bounds__(kMultiThreads, 2)
 decode_multi_pf_kernel(const DecodeMultiArgs a) {
     constexpr int V4 = D / 32;
     constexpr int kItemsPerHead = D / kMultiRows;
-    using MS = MultiStage<D>;
+    using MS = MultiStageT<D, false>;
     using PF = MultiPf<D>;
     extern __shared__ __align__(128) uint8_t pf_smem[];
     const int lane = threadIdx.x & 31;
@@ -487,9 +493,25 @@ decode_multi_pf_kernel(const DecodeMultiArgs a) {
     asm volatile("cp.async.wait_group 0;" ::: "memory");  // nothing in flight at exit
 }
 
+template <int D, bool kF32>
+cudaError_t launch_multi_form(const DecodeMultiArgs &a, int dev, int sms, int64_t need, cudaStream_t stream) {
+    static int occ[kMaxDevices] = {}, set[kMaxDevices] = {};
+    constexpr int smem = MultiStageT<D, kF32>::kBlock;
+    if (dev < 0 || dev >= kMaxDevices || !__atomic_load_n(&set[dev], __ATOMIC_ACQUIRE)) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(decode_multi_kernel<D, kF32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDevices) __atomic_store_n(&set[dev], 1, __ATOMIC_RELEASE);
+    }
+    const int per_sm = blocks_per_sm(decode_multi_kernel<D, kF32>, kMultiThreads, dev, occ, smem);
+    const int64_t cap = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
+    const int grid = static_cast<int>(need < cap ? need : cap);
+    decode_multi_kernel<D, kF32><<<grid, kMultiThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_decode_multi_d(const DecodeMultiArgs &a, cudaStream_t stream) {
-    static int occ[kMaxDevices] = {};
     int dev = 0, sms = 0;
     if (!current_device(&dev, &sms)) return cudaErrorInvalidDevice;
     const int64_t items = static_cast<int64_t>(a.num_rows) * a.h_v * (D / kMultiRows);
@@ -509,19 +531,8 @@ cudaError_t launch_decode_multi_d(const DecodeMultiArgs &a, cudaStream_t stream)
         decode_multi_pf_kernel<D><<<grid, kMultiThreads, smem, stream>>>(a);
         return cudaGetLastError();
     }
-    static int set_m[kMaxDevices] = {};
-    constexpr int smem_m = MultiStageF<D>::kBlock;
-    if (dev < 0 || dev >= kMaxDevices || !__atomic_load_n(&set_m[dev], __ATOMIC_ACQUIRE)) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(decode_multi_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_m);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < kMaxDevices) __atomic_store_n(&set_m[dev], 1, __ATOMIC_RELEASE);
-    }
-    const int per_sm = blocks_per_sm(decode_multi_kernel<D>, kMultiThreads, dev, occ, smem_m);
-    const int64_t cap = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
-    const int grid = static_cast<int>(need < cap ? need : cap);
-    decode_multi_kernel<D><<<grid, kMultiThreads, smem_m, stream>>>(a);
-    return cudaGetLastError();
+    if (a.tokens_per_row >= 3 && a.tokens_per_row <= 4) return launch_multi_form<D, true>(a, dev, sms, need, stream);
+    return launch_multi_form<D, false>(a, dev, sms, need, stream);
 }
 
 template <int D, bool kRaw>
