@@ -415,6 +415,7 @@ def mixed_case(torch, gdn, dev, reps, peaks):
             "tokens_per_s": (nd + pre.total_tokens) / (ms * 1e-3), "colaunch_two_streams_ms": ms2,
             "roofline": {"bound": "hbm (decode rows) + tensor (prefill)", "decode_bytes": dec_bytes,
                          "prefill_flops": pre_flops, "floor_ms": floor_ms, "frac": floor_ms / ms,
+                         "frac_colaunch": floor_ms / ms2,
                          "peak_hbm_gbs": peaks["hbm_gbs"], "peak_tflops": peaks["bf16_tflops"],
                          "peak_source": peaks["source"]},
             "clocks": clocks}
