@@ -144,12 +144,21 @@ def _dev(t, name, dtype, ndim=None, optional=False):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # a plain int: the argtypes (c_void_p) convert it
+    return None if t is None else t.data_ptr()
+
+
+# The current stream's handle without building a Stream object (a third of
+# a small call's Python time); the public route where torch lacks it.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(stream):
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _host_i32(x, name):
@@ -178,8 +187,15 @@ def _check(status, fn):
         raise GdnError(status, fn)
 
 
+_dims_cache = {}
+
+
 def _dims(q, v, scale):
-    return Dims(q.shape[1], v.shape[1], q.shape[2], v.shape[2], float(scale))
+    key = (q.shape[1], v.shape[1], q.shape[2], v.shape[2], float(scale))
+    d = _dims_cache.get(key)
+    if d is None:  # read-only on the C side, so one object per shape serves every call
+        d = _dims_cache[key] = Dims(*key)
+    return d
 
 
 # ---------------------------------------------------------------------------
