@@ -130,6 +130,10 @@ def _dev(t, name, dtype, ndim=None, optional=False):
         if optional:
             return None
         raise ValueError(f"{name} is required")
+    # the common case in one expression; the checks below name what is wrong
+    if (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype is dtype and t.is_contiguous()
+            and (ndim is None or t.dim() == ndim)):
+        return t
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
