@@ -683,20 +683,23 @@ def reference_arm(args):
     # GPU is needed, so the other ranks of a torchrun launch exit at once.
     # Each step is one oracle call on the same sample shape as the decode
     # cpu_baseline: all 256 rows x S recurrent steps (S sized so that a call
-    # takes about two seconds), so the two CPU figures measure the same work.
+    # takes about a second), so the two CPU figures measure the same work.
     import oracle
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     threads = oracle.max_threads()
-    steps = decode_steps_for(2.0, threads)
+    steps = decode_steps_for(1.0, threads)
+    # one sample, built once: generating it costs several times the oracle call
+    b = gi.token_batch([steps] * DECODE_ROWS, H, H, D, 0, init_state=True)
     for _ in range(args.warmup):
-        oracle_decode_rate(DECODE_ROWS, steps, threads)
+        oracle.run_chains(b, n_threads=threads)
     times = []
     for _ in range(args.steps):
-        _, d = oracle_decode_rate(DECODE_ROWS, steps, threads)
-        times.append(d)
+        t0 = time.perf_counter()
+        oracle.run_chains(b, n_threads=threads)
+        times.append(time.perf_counter() - t0)
     tot = sum(times)
     value = DECODE_ROWS * steps * args.steps / tot
     line = {"impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "rows/s",
