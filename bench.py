@@ -333,15 +333,34 @@ def time_decode_e2e_eager(torch, gdn, t, steps, warmup, world):
     return s.elapsed_time(e), h2d, d2h
 
 
+_FLUSH = {}
+FLUSH_NOTE = "each call preceded by a 256 MiB read on its stream (L2 flushed, host issue hidden)"
+
+
+def l2_flush(torch):
+    """Read 256 MiB on the current stream (a max-reduction).  It evicts the
+    129 MB L2 before a timed call without leaving dirty lines to write back,
+    and it keeps the device busy for ~40 us while the host issues the call
+    (binding checks, C-ABI validation, launch), so that host time does not
+    fall between the call's events."""
+    dev = torch.cuda.current_device()
+    buf = _FLUSH.get(dev)
+    if buf is None:
+        buf = _FLUSH[dev] = torch.ones(64 << 20, dtype=torch.float32, device=f"cuda:{dev}")
+    buf.amax()
+
+
 def timed_median(torch, fn, reps=20, warm=10):
     """Median device time (ms) of `reps` calls after `warm` untimed ones, each
-    bracketed by CUDA events on the current stream; clocks sampled meanwhile."""
+    bracketed by CUDA events on the current stream after an L2 flush; clocks
+    sampled meanwhile."""
     for _ in range(warm):
         fn()
     torch.cuda.synchronize()
     with Clocks(torch.cuda.current_device()) as clk:
         ev = []
         for _ in range(reps):
+            l2_flush(torch)
             a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             fn()
@@ -372,7 +391,7 @@ def prefill_case(torch, gdn, wl, dev, reps, E=0):
     T = b.total_tokens
     fl = prefill_flops_per_token(b.h_k, b.h_v, b.d) * T
     return {"workload": wl["name"], "seqlens": b.seqlens if n <= 16 else f"{n} x {b.seqlens[0]}",
-            "tokens": T, "ms": ms, "timing": f"median of {reps} calls after 10 warm-up calls",
+            "tokens": T, "ms": ms, "timing": f"median of {reps} calls after 10 warm-up calls, {FLUSH_NOTE}",
             "tokens_per_s": T / (ms * 1e-3),
             "algorithmic_tflops": fl / (ms * 1e-3) / 1e12, "emit_every_chunks": E,
             "emitted_states": n_emit, "clocks": clocks}
@@ -415,7 +434,7 @@ def mixed_case(torch, gdn, dev, reps, peaks):
     # co-launched, the halves overlap: the floor is the longer of the two
     floor_co_ms = max(dec_floor_ms, pre_floor_ms)
     return {"workload": wl["name"], "decode_rows": nd, "prefill_seqlens": pre.seqlens, "ms": ms,
-            "timing": f"median of {reps} calls after 10 warm-up calls",
+            "timing": f"median of {reps} calls after 10 warm-up calls, {FLUSH_NOTE}",
             "tokens_per_s": (nd + pre.total_tokens) / (ms * 1e-3), "colaunch_two_streams_ms": ms2,
             "roofline": {"bound": "hbm (decode rows) + tensor (prefill)", "decode_bytes": dec_bytes,
                          "prefill_flops": pre_flops, "floor_ms": floor_ms, "frac": floor_ms / ms,
@@ -443,7 +462,8 @@ def multi_decode_case(torch, gdn, dev, peaks, rows=256, T=4, reps=10):
     o = torch.empty((rows * T, H, D), dtype=torch.bfloat16, device=dev)
     state_b = H * D * D * 4
     tok_b = H * D * 2 * 4 + H * 4 * 2
-    out = {"workload": f"decode_multi_r{rows}_t{T}_h16_d128", "rows": rows, "tokens_per_row": T}
+    out = {"workload": f"decode_multi_r{rows}_t{T}_h16_d128", "rows": rows, "tokens_per_row": T,
+           "timing": f"median of {reps} calls after 1 warm-up call, {FLUSH_NOTE}"}
     for name, dst, writes in (("snapshots", dst_t, T), ("final_only", None, 1)):
         def call():
             gdn.gdn_decode_multi(T, q, k, v, g, beta, cache, src_t, o, dst_slots=dst)
@@ -451,6 +471,7 @@ def multi_decode_case(torch, gdn, dev, peaks, rows=256, T=4, reps=10):
         torch.cuda.synchronize()
         ev = []
         for _ in range(reps):
+            l2_flush(torch)
             a0, z0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a0.record()
             call()
@@ -483,7 +504,7 @@ def prep_case(torch, gdn, dev, peaks, T=131072, h_k=16, h_v=32, reps=20):
     byts = T * (2 * 2 * h_k * D * 2 + 4 * h_v * 4)
     gbs = byts / (ms * 1e-3) / 1e9
     return {"workload": f"prep_inputs_t{T}_hk{h_k}_hv{h_v}_d128", "ms": ms, "tokens_per_s": T / (ms * 1e-3),
-            "bytes_per_launch": byts, "timing": f"median of {reps} calls after 10 warm-up calls", "clocks": clocks,
+            "bytes_per_launch": byts, "timing": f"median of {reps} calls after 10 warm-up calls, {FLUSH_NOTE}", "clocks": clocks,
             "roofline": {"bound": "hbm", "kernel": "prep_kernel<128>", "achieved": gbs, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"]}}
 
